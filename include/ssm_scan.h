@@ -1,0 +1,121 @@
+/*
+ * ssm_scan.h -- C-ABI of the B300 (sm_103a) selective-scan library.
+ *
+ * Two operations of the Mamba selective state-space model (S6):
+ *
+ *  ssm_scan_fwd      The selective scan over a whole sequence.  For every batch
+ *                    row b, channel d and state n:
+ *                      Delta_t = softplus(delta_t + dt_bias[d])       (optional softplus / bias)
+ *                      Abar_t  = exp(Delta_t * A[d,n])                 (zero-order hold, diagonal A)
+ *                      h_t     = Abar_t * h_{t-1} + Delta_t * B_t[n] * u_t,   h_{-1} = 0
+ *                      y_t     = sum_n C_t[n] * h_t[n] + D[d] * u_t  (optional D)
+ *                      out_t   = y_t * silu(z_t)                       (optional gate)
+ *                    and the state after the last step.
+ *                    Sources: "Mamba 状态空间模型深度解析" (gsyq.cn), sections
+ *                    "连续到离散的转换" (discrete recurrence, ZOH A_bar = exp(Delta A)),
+ *                    "选择性机制的设计理念" (B, C, Delta = Softplus(Linear(x)) depend on the
+ *                    input) and "硬件优化并行扫描算法" (A_bar = exp(Delta*A), B_bar = Delta*B,
+ *                    h = scan(A_bar, B_bar*x), y = C*h); VMamba notes (genhiy.github.io),
+ *                    "S4中三个矩阵的维度表示、维度变化" (one SSM per channel; B, C of shape
+ *                    (B,L,N) shared by all channels; Delta of shape (B,L,D)) and
+ *                    "简化的SSM架构" (the gated block that the silu(z) gate closes).
+ *
+ *  ssm_state_update  One decode step of the same recurrence on a stored state
+ *                    (constant-memory inference: gsyq.cn page, complexity table
+ *                    row "推理内存 O(d) 状态向量"; 53ai.com Mamba article, §1 on
+ *                    RNN-style inference from the previous hidden state only).
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer is a DEVICE pointer owned by the caller.  The library never
+ *    allocates, never frees and keeps no global state between calls.
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream).  Kernel-time errors surface on the caller's next
+ *    synchronisation of that stream.
+ *  - All arguments are validated on the host before anything is launched.  A
+ *    non-zero return means nothing was launched, except SSM_ERR_LAUNCH (the
+ *    launch itself failed; see ssm_status_string).
+ *  - There is no CPU fallback: every call runs the sm_103a kernels.
+ *  - io dtype (SSM_F32 or SSM_BF16) applies to u/delta/z/y/B/C (scan) and to
+ *    x/dt/z/out/B/C (decode).  A, D, dt_bias and the states are always float32;
+ *    all arithmetic is float32.  bf16 outputs are rounded to nearest-even.
+ *  - Pointers must be aligned to their element size.  Rows that are 16-byte
+ *    aligned (base 16-byte aligned and a row length in bytes that is a multiple
+ *    of 16) take a vectorised copy path; anything else takes an element-wise
+ *    copy path inside the same kernels.  Results are identical.
+ *  - dstate may be 1..16.  Sizes of zero are allowed and launch nothing (except
+ *    that seqlen == 0 still writes the zero final state when last_state is given).
+ */
+#ifndef SSM_SCAN_H_
+#define SSM_SCAN_H_
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SSM_OK = 0,
+  SSM_ERR_NULL = -1,        /* a required pointer is NULL */
+  SSM_ERR_SHAPE = -2,       /* a size is negative, or dstate < 1 */
+  SSM_ERR_DTYPE = -3,       /* io_dtype is not an ssm_dtype value */
+  SSM_ERR_ALIGN = -4,       /* a pointer is not aligned to its element size */
+  SSM_ERR_UNSUPPORTED = -5, /* dstate > 16, or a grid dimension would overflow */
+  SSM_ERR_LAUNCH = -6,      /* the CUDA launch failed (no device, bad stream, ...) */
+  SSM_ERR_TIMEOUT = -7      /* reserved: a bounded in-kernel wait gave up */
+} ssm_status;
+
+typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/* Version of this ABI (bumped when a signature changes). */
+int ssm_abi_version(void);
+
+/*
+ * Selective scan forward.
+ *   u, delta, z, y : [batch][dim][seqlen], io dtype, contiguous (seqlen innermost).
+ *                    delta is the raw step size before dt_bias and softplus.
+ *   A              : [dim][dstate] float32, the continuous (negative) A, e.g. -exp(A_log).
+ *   B, C           : [batch][dstate][seqlen], io dtype, shared by all channels of a batch row.
+ *   D, dt_bias     : [dim] float32.
+ *   last_state     : [batch][dim][dstate] float32, receives h after the last step.
+ *   delta_softplus : non-zero applies softplus to delta + dt_bias.
+ * Required: u, delta, A, B, C, y.  Nullable: D (no skip), z (no gate), dt_bias (no
+ * bias), last_state (not written).  y must not alias any input.
+ * Returns an ssm_status.
+ */
+int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* dt_bias, int delta_softplus, void* y, float* last_state, int batch,
+                 int dim, int dstate, int seqlen, int io_dtype, void* stream);
+
+/*
+ * Selective scan forward from a given initial state h0 ([batch][dim][dstate] float32,
+ * nullable = zero state).  Otherwise identical to ssm_scan_fwd.  Scanning L1 steps,
+ * then L2 steps from the returned last_state, equals one scan over L1 + L2 steps:
+ * the chunked streaming of long documents (gsyq.cn page, "长序列处理的最佳实践",
+ * LongDocumentProcessor) at the level of one scan.  last_state may equal h0 (in place).
+ */
+int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, void* stream);
+
+/*
+ * Single-token decode step, state updated in place.
+ *   state          : [batch][dim][dstate] float32, read and written.
+ *   x, dt, z, out  : [batch][dim], io dtype.  dt is the raw step size.
+ *   A              : [dim][dstate] float32.   B, C : [batch][dstate], io dtype.
+ *   D, dt_bias     : [dim] float32.
+ *   dt_softplus    : non-zero applies softplus to dt + dt_bias.
+ * Required: state, x, dt, A, B, C, out.  Nullable: D, z, dt_bias.  With dt_bias
+ * NULL and dt_softplus 0 the step size is dt itself.
+ * Returns an ssm_status.
+ */
+int ssm_state_update(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+                     const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
+                     int dim, int dstate, int io_dtype, void* stream);
+
+/* Static, NUL-terminated description of a status code (never NULL). */
+const char* ssm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H_ */

@@ -1,0 +1,180 @@
+"""float64 CPU oracle for the Mamba selective scan -- TEST INFRASTRUCTURE ONLY.
+
+Only the tests, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this module.  The product path (the CUDA library and its
+Python binding) never touches it, and it shares no code with that path: the
+arithmetic lives in ``ssm_oracle.c`` (plain loops, float64, libm ``exp`` and
+``log1p``), compiled here with gcc ``-O2 -fno-fast-math -ffp-contract=off``.
+
+Every function takes numpy arrays in the layouts documented in ``ssm_oracle.c``
+and returns float64 numpy arrays.  Inputs are widened to float64 exactly (fp32
+and bf16 values are representable in float64), so the oracle sees the very same
+numbers as the GPU.
+
+Parity status per function (what pins it, see tests/test_oracle_pins.py):
+  scan            pinned: prefix-sum worked example, closed-form y2/y3 expansions,
+                  brute-force convolution form, unrolled time-varying sum, Delta->0,
+                  exact halving with Delta = ln 2, softplus/silu special values.
+  state_update    pinned: equals the pinned scan step by step; exact halving case.
+  assoc_scan      pinned: prefix-sum worked example; equals the closed-form products.
+  scan_tree       pinned: equals the sequential scan (associativity).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ssm_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+_DP = ctypes.POINTER(ctypes.c_double)
+
+
+def build(force: bool = False) -> str:
+    """Compile ssm_oracle.c into liboracle.so next to it (OpenMP over channels)."""
+    if not force and os.path.exists(_LIB) and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC):
+        return _LIB
+    cmd = ["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+           "-o", _LIB, _SRC, "-lm"]
+    subprocess.run(cmd, check=True)
+    return _LIB
+
+
+def use_library(path: str | None) -> None:
+    """Point this module at another build of ssm_oracle.c (the mutation tests use it to check
+    that the pins reject planted mistakes); None restores the default build."""
+    global _lib, _LIB
+    with _lock:
+        _lib = None
+        _LIB = path if path is not None else os.path.join(_HERE, "liboracle.so")
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            if _LIB == os.path.join(_HERE, "liboracle.so"):
+                build()
+            lib = ctypes.CDLL(_LIB)
+            lib.oracle_scan_f64.restype = ctypes.c_int
+            lib.oracle_scan_f64.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP, _DP] + [ctypes.c_int] * 5
+            lib.oracle_state_update_f64.restype = ctypes.c_int
+            lib.oracle_state_update_f64.argtypes = [_DP] * 9 + [ctypes.c_int, _DP] + [ctypes.c_int] * 4
+            lib.oracle_assoc_scan_pairs_f64.restype = ctypes.c_int
+            lib.oracle_assoc_scan_pairs_f64.argtypes = [_DP] * 4 + [ctypes.c_int]
+            lib.oracle_scan_tree_f64.restype = ctypes.c_int
+            lib.oracle_scan_tree_f64.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP] + [ctypes.c_int] * 4
+            lib.oracle_softplus_f64.restype = ctypes.c_double
+            lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
+            lib.oracle_silu_f64.restype = ctypes.c_double
+            lib.oracle_silu_f64.argtypes = [ctypes.c_double]
+            _lib = lib
+    return _lib
+
+
+def _f64(a, shape=None):
+    if a is None:
+        return None
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if shape is not None and arr.shape != tuple(shape):
+        raise ValueError(f"expected shape {tuple(shape)}, got {arr.shape}")
+    return arr
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(_DP)
+
+
+def scan(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, nthreads=0):
+    """Selective scan.  Returns (y [batch,dim,L], last_state [batch,dim,N])."""
+    u = _f64(u)
+    batch, dim, seqlen = u.shape
+    A = _f64(A)
+    dstate = A.shape[1]
+    delta = _f64(delta, (batch, dim, seqlen))
+    A = _f64(A, (dim, dstate))
+    B = _f64(B, (batch, dstate, seqlen))
+    C = _f64(C, (batch, dstate, seqlen))
+    D = _f64(D, (dim,))
+    z = _f64(z, (batch, dim, seqlen))
+    dt_bias = _f64(dt_bias, (dim,))
+    h0 = _f64(h0, (batch, dim, dstate))
+    y = np.zeros((batch, dim, seqlen), dtype=np.float64)
+    last = np.zeros((batch, dim, dstate), dtype=np.float64)
+    rc = _load().oracle_scan_f64(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
+                                 int(bool(delta_softplus)), _ptr(h0), _ptr(y), _ptr(last),
+                                 batch, dim, dstate, seqlen, int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_scan_f64 failed: {rc}")
+    return y, last
+
+
+def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, nthreads=0):
+    """One decode step.  Returns (new_state [batch,dim,N], out [batch,dim]); `state` is not modified."""
+    s = np.array(state, dtype=np.float64, copy=True, order="C")
+    batch, dim, dstate = s.shape
+    x = _f64(x, (batch, dim))
+    dt = _f64(dt, (batch, dim))
+    A = _f64(A, (dim, dstate))
+    B = _f64(B, (batch, dstate))
+    C = _f64(C, (batch, dstate))
+    D = _f64(D, (dim,))
+    z = _f64(z, (batch, dim))
+    dt_bias = _f64(dt_bias, (dim,))
+    out = np.zeros((batch, dim), dtype=np.float64)
+    rc = _load().oracle_state_update_f64(_ptr(s), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                         _ptr(dt_bias), int(bool(dt_softplus)), _ptr(out), batch, dim, dstate,
+                                         int(nthreads))
+    if rc != 0:
+        raise RuntimeError(f"oracle_state_update_f64 failed: {rc}")
+    return s, out
+
+
+def assoc_scan(a, b):
+    """Tree-order inclusive scan of pairs (a_t, b_t).  Returns (prod_a, h)."""
+    a = _f64(a)
+    b = _f64(b, a.shape)
+    n = a.shape[0]
+    oa = np.zeros(n, dtype=np.float64)
+    ob = np.zeros(n, dtype=np.float64)
+    rc = _load().oracle_assoc_scan_pairs_f64(_ptr(a), _ptr(b), _ptr(oa), _ptr(ob), n)
+    if rc != 0:
+        raise RuntimeError(f"oracle_assoc_scan_pairs_f64 failed: {rc}")
+    return oa, ob
+
+
+def scan_tree(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True):
+    """The selective scan with the recurrence evaluated in tree order."""
+    u = _f64(u)
+    batch, dim, seqlen = u.shape
+    A = _f64(A)
+    dstate = A.shape[1]
+    delta = _f64(delta, (batch, dim, seqlen))
+    B = _f64(B, (batch, dstate, seqlen))
+    C = _f64(C, (batch, dstate, seqlen))
+    D = _f64(D, (dim,))
+    z = _f64(z, (batch, dim, seqlen))
+    dt_bias = _f64(dt_bias, (dim,))
+    y = np.zeros((batch, dim, seqlen), dtype=np.float64)
+    last = np.zeros((batch, dim, dstate), dtype=np.float64)
+    rc = _load().oracle_scan_tree_f64(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+                                      _ptr(dt_bias), int(bool(delta_softplus)), _ptr(y), _ptr(last),
+                                      batch, dim, dstate, seqlen)
+    if rc != 0:
+        raise RuntimeError(f"oracle_scan_tree_f64 failed: {rc}")
+    return y, last
+
+
+def softplus(x: float) -> float:
+    return _load().oracle_softplus_f64(float(x))
+
+
+def silu(x: float) -> float:
+    return _load().oracle_silu_f64(float(x))

@@ -1,0 +1,215 @@
+/*
+ * ssm_oracle.c -- float64 CPU oracle for the Mamba selective scan.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
+ * call this file; only the tests, the smoke check and the CPU-baseline leg of
+ * the benchmark use it.  It shares no code, header or table with the CUDA
+ * library: both sides only receive the same seeded input arrays.
+ *
+ * What it computes (plain definitions, no blocking, fusion or reordering):
+ *
+ *   Step size      Delta = softplus(delta + dt_bias[d])  (softplus optional,
+ *                  dt_bias optional).  Selection makes Delta input dependent:
+ *                  "Mamba 状态空间模型深度解析" (gsyq.cn), section
+ *                  "选择性机制的设计理念" (Delta = Softplus(Linear(x))), and the
+ *                  VMamba notes (genhiy.github.io), section
+ *                  "mamba：从S4到S6的算法变化流程" (tau_Delta = softplus).
+ *   Discretisation Abar = exp(Delta * A[d,n]) (zero-order hold for a diagonal
+ *                  A) and Bbar*x = Delta * B[n] * u: gsyq.cn page, sections
+ *                  "连续到离散的转换" and "硬件优化并行扫描算法" (A_bar =
+ *                  exp(Delta*A), B_bar = Delta*B); VMamba notes, "离散化SSM".
+ *   Recurrence     h_t = Abar_t * h_{t-1} + Bbar_t * x_t, h_{-1} = h0 (zero
+ *                  when not given): gsyq.cn page, the sequential loop in
+ *                  "计算复杂度分析"; VMamba notes, "循环结构表示以快速推理".
+ *   Readout        y_t = sum_n C_t[n] h_t[n] + D[d] * u_t: gsyq.cn page,
+ *                  "核心数学形式" (y = C h + D x) and the D*x skip returned
+ *                  by the SelectiveSSM sketch.
+ *   Gate           out_t = y_t * silu(z_t), silu(z) = z / (1 + exp(-z)), the
+ *                  gated-MLP merge of the Mamba block (VMamba notes,
+ *                  "简化的SSM架构").
+ *   Channels       every (batch, channel d) runs its own SSM; B and C are
+ *                  shared by all channels of a batch row (VMamba notes,
+ *                  "S4中三个矩阵的维度表示、维度变化": B, C of shape (B,L,N),
+ *                  Delta of shape (B,L,D)).
+ *   Decode step    the same single recurrence step applied to a stored state
+ *                  (constant-memory inference: gsyq.cn page, complexity table
+ *                  row "推理内存 O(d) 状态向量").
+ *   Associative    the pair operator (a1,b1) o (a2,b2) = (a1*a2, a2*b1 + b2)
+ *   scan           evaluated in tree order (53ai.com Mamba article, section
+ *                  3.3 "Parallel Associative Scan": grouping does not change a
+ *                  prefix result; gsyq.cn page, "硬件优化并行扫描算法").
+ *
+ * Layouts (all row-major, all float64, all host memory owned by the caller):
+ *   u, delta, z, y          [batch][dim][seqlen]
+ *   B, C                    [batch][dstate][seqlen]
+ *   A                       [dim][dstate]      (continuous A, e.g. -exp(A_log))
+ *   D, dt_bias              [dim]
+ *   h0, last_state, state   [batch][dim][dstate]
+ *   decode x, dt, z, out    [batch][dim];  decode B, C [batch][dstate]
+ *
+ * Channels are independent and each runs sequentially in t, so results do not
+ * depend on the OpenMP thread count.
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdlib.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* softplus(x) = log(1 + e^x), written so that neither branch overflows. */
+static double softplus_f64(double x) {
+  if (x > 0.0) return x + log1p(exp(-x));
+  return log1p(exp(x));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double silu_f64(double z) { return z / (1.0 + exp(-z)); }
+
+static double step_size(double raw, const double* dt_bias, int d, int use_softplus) {
+  double v = raw;
+  if (dt_bias) v += dt_bias[d];
+  if (use_softplus) v = softplus_f64(v);
+  return v;
+}
+
+int oracle_abi_version(void) { return 1; }
+
+/* Selective scan over seqlen steps for every (batch, channel). */
+int oracle_scan_f64(const double* u, const double* delta, const double* A, const double* B, const double* C,
+                    const double* D, const double* z, const double* dt_bias, int delta_softplus, const double* h0,
+                    double* y, double* last_state, int batch, int dim, int dstate, int seqlen, int nthreads) {
+  if (!u || !delta || !A || !B || !C || !y) return -1;
+  if (batch < 0 || dim < 0 || dstate < 1 || seqlen < 0) return -2;
+  long nch = (long)batch * dim;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+  for (long ch = 0; ch < nch; ++ch) {
+    int b = (int)(ch / dim), d = (int)(ch % dim);
+    double* h = (double*)malloc(sizeof(double) * (size_t)dstate);
+    for (int n = 0; n < dstate; ++n) h[n] = h0 ? h0[ch * dstate + n] : 0.0;
+    const double* u_row = u + ch * seqlen;
+    const double* dl_row = delta + ch * seqlen;
+    const double* z_row = z ? z + ch * seqlen : NULL;
+    double* y_row = y + ch * seqlen;
+    for (int t = 0; t < seqlen; ++t) {
+      double dt = step_size(dl_row[t], dt_bias, d, delta_softplus);
+      double x = u_row[t];
+      double acc = 0.0;
+      for (int n = 0; n < dstate; ++n) {
+        double abar = exp(dt * A[(long)d * dstate + n]);
+        double bx = dt * B[((long)b * dstate + n) * seqlen + t] * x;
+        h[n] = abar * h[n] + bx;
+        acc += C[((long)b * dstate + n) * seqlen + t] * h[n];
+      }
+      if (D) acc += D[d] * x;
+      if (z_row) acc *= silu_f64(z_row[t]);
+      y_row[t] = acc;
+    }
+    if (last_state)
+      for (int n = 0; n < dstate; ++n) last_state[ch * dstate + n] = h[n];
+    free(h);
+  }
+  return 0;
+}
+
+/* One decode step: state <- Abar*state + Bbar*x in place, out = (C.state + D x) * silu(z). */
+int oracle_state_update_f64(double* state, const double* x, const double* dt, const double* A, const double* B,
+                            const double* C, const double* D, const double* z, const double* dt_bias,
+                            int dt_softplus, double* out, int batch, int dim, int dstate, int nthreads) {
+  if (!state || !x || !dt || !A || !B || !C || !out) return -1;
+  if (batch < 0 || dim < 0 || dstate < 1) return -2;
+  long nch = (long)batch * dim;
+#ifdef _OPENMP
+  if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(static)
+#endif
+  for (long ch = 0; ch < nch; ++ch) {
+    int b = (int)(ch / dim), d = (int)(ch % dim);
+    double step = step_size(dt[ch], dt_bias, d, dt_softplus);
+    double acc = 0.0;
+    for (int n = 0; n < dstate; ++n) {
+      double* s = &state[ch * dstate + n];
+      double abar = exp(step * A[(long)d * dstate + n]);
+      *s = abar * *s + step * B[(long)b * dstate + n] * x[ch];
+      acc += C[(long)b * dstate + n] * *s;
+    }
+    if (D) acc += D[d] * x[ch];
+    if (z) acc *= silu_f64(z[ch]);
+    out[ch] = acc;
+  }
+  return 0;
+}
+
+/*
+ * Inclusive scan of the pairs (a_t, b_t) under (a1,b1) o (a2,b2) = (a1*a2, a2*b1 + b2),
+ * evaluated in tree order (recursive doubling: after round k every position holds the
+ * combination of the 2^k pairs ending at it).  The b component of the result is the
+ * recurrence h_t = a_t h_{t-1} + b_t from h_{-1} = 0; the a component is the running
+ * product of the a's.  With a == 1 it is a plain prefix sum.
+ */
+int oracle_assoc_scan_pairs_f64(const double* a, const double* b, double* out_a, double* out_b, int n) {
+  if (n < 0 || (n > 0 && (!a || !b || !out_a || !out_b))) return -1;
+  double* pa = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  double* pb = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1));
+  for (int i = 0; i < n; ++i) { out_a[i] = a[i]; out_b[i] = b[i]; }
+  for (int off = 1; off < n; off *= 2) {
+    for (int i = 0; i < n; ++i) { pa[i] = out_a[i]; pb[i] = out_b[i]; }
+    for (int i = off; i < n; ++i) {
+      /* left operand: the block ending at i-off; right operand: the block ending at i */
+      double la = pa[i - off], lb = pb[i - off];
+      double ra = pa[i], rb = pb[i];
+      out_a[i] = la * ra;
+      out_b[i] = ra * lb + rb;
+    }
+  }
+  free(pa);
+  free(pb);
+  return 0;
+}
+
+/*
+ * The selective scan with the recurrence evaluated by the tree-order pair scan
+ * above instead of the sequential loop (same discretisation and readout).
+ */
+int oracle_scan_tree_f64(const double* u, const double* delta, const double* A, const double* B, const double* C,
+                         const double* D, const double* z, const double* dt_bias, int delta_softplus, double* y,
+                         double* last_state, int batch, int dim, int dstate, int seqlen) {
+  if (!u || !delta || !A || !B || !C || !y) return -1;
+  if (batch < 0 || dim < 0 || dstate < 1 || seqlen < 1) return -2;
+  double* a = (double*)malloc(sizeof(double) * (size_t)seqlen);
+  double* bx = (double*)malloc(sizeof(double) * (size_t)seqlen);
+  double* pa = (double*)malloc(sizeof(double) * (size_t)seqlen);
+  double* h = (double*)malloc(sizeof(double) * (size_t)seqlen * dstate);
+  for (long ch = 0; ch < (long)batch * dim; ++ch) {
+    int b = (int)(ch / dim), d = (int)(ch % dim);
+    for (int n = 0; n < dstate; ++n) {
+      for (int t = 0; t < seqlen; ++t) {
+        double dt = step_size(delta[ch * seqlen + t], dt_bias, d, delta_softplus);
+        a[t] = exp(dt * A[(long)d * dstate + n]);
+        bx[t] = dt * B[((long)b * dstate + n) * seqlen + t] * u[ch * seqlen + t];
+      }
+      oracle_assoc_scan_pairs_f64(a, bx, pa, h + (long)n * seqlen, seqlen);
+    }
+    for (int t = 0; t < seqlen; ++t) {
+      double acc = 0.0;
+      for (int n = 0; n < dstate; ++n) acc += C[((long)b * dstate + n) * seqlen + t] * h[(long)n * seqlen + t];
+      if (D) acc += D[d] * u[ch * seqlen + t];
+      if (z) acc *= silu_f64(z[ch * seqlen + t]);
+      y[ch * seqlen + t] = acc;
+    }
+    if (last_state)
+      for (int n = 0; n < dstate; ++n) last_state[ch * dstate + n] = h[(long)n * seqlen + seqlen - 1];
+  }
+  free(a);
+  free(bx);
+  free(pa);
+  free(h);
+  return 0;
+}
+
+/* Exposed for the pin tests: the scalar helpers exactly as the scan uses them. */
+double oracle_softplus_f64(double x) { return softplus_f64(x); }
+double oracle_silu_f64(double z) { return silu_f64(z); }

@@ -1,0 +1,78 @@
+"""The oracle's pins must reject plausible mistakes.
+
+Each case plants one mistake in a copy of the oracle's C source (a dropped term, a wrong
+sign, a transposed index, the readout taken before the update, ...), builds it in a
+temporary directory, and checks that at least one pin test fails against that build.
+"""
+import os
+import subprocess
+
+import pytest
+
+from oracle import oracle
+import tests.test_oracle_pins as pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
+
+MUTANTS = {
+    "drop_D_skip": ("if (D) acc += D[d] * x;\n      if (z_row)", "if (z_row)"),
+    "A_sign": ("double abar = exp(dt * A[(long)d * dstate + n]);\n        double bx",
+               "double abar = exp(-dt * A[(long)d * dstate + n]);\n        double bx"),
+    "B_transposed": ("double bx = dt * B[((long)b * dstate + n) * seqlen + t] * x;",
+                     "double bx = dt * B[((long)b * seqlen + t) * dstate + n] * x;"),
+    "C_from_B": ("acc += C[((long)b * dstate + n) * seqlen + t] * h[n];",
+                 "acc += B[((long)b * dstate + n) * seqlen + t] * h[n];"),
+    "readout_before_update": ("h[n] = abar * h[n] + bx;\n        acc += C[((long)b * dstate + n) * seqlen + t] * h[n];",
+                              "acc += C[((long)b * dstate + n) * seqlen + t] * h[n];\n        h[n] = abar * h[n] + bx;"),
+    "bias_after_softplus": ("if (dt_bias) v += dt_bias[d];\n  if (use_softplus) v = softplus_f64(v);",
+                            "if (use_softplus) v = softplus_f64(v);\n  if (dt_bias) v += dt_bias[d];"),
+    "softplus_wrong_branch": ("if (x > 0.0) return x + log1p(exp(-x));", "if (x > 0.0) return log1p(exp(-x));"),
+    "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
+    "bbar_missing_delta": ("double bx = dt * B[((long)b * dstate + n) * seqlen + t] * x;",
+                           "double bx = B[((long)b * dstate + n) * seqlen + t] * x;"),
+    "gate_additive": ("if (z_row) acc *= silu_f64(z_row[t]);", "if (z_row) acc += silu_f64(z_row[t]);"),
+    "pair_combine_swapped": ("out_b[i] = ra * lb + rb;", "out_b[i] = la * rb + lb;"),
+    "decode_no_state_decay": ("*s = abar * *s + step * B[(long)b * dstate + n] * x[ch];",
+                              "*s = *s + step * B[(long)b * dstate + n] * x[ch];"),
+    "h0_ignored": ("h[n] = h0 ? h0[ch * dstate + n] : 0.0;", "h[n] = 0.0;"),
+}
+
+PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
+
+
+def _run_pins():
+    failures = 0
+    for fn in PIN_TESTS:
+        params = getattr(fn, "pytestmark", [])
+        arglists = [{}]
+        for m in params:
+            if m.name == "parametrize":
+                name, values = m.args
+                arglists = [{name: v} for v in values]
+        for kw in arglists:
+            try:
+                fn(**kw)
+            except Exception:  # an assertion or a numerical error both count as a rejection
+                failures += 1
+    return failures
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_reject_mutant(name, tmp_path):
+    old, new = MUTANTS[name]
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutation anchor for {name} not found exactly once"
+    mut = tmp_path / "mutant.c"
+    mut.write_text(src.replace(old, new))
+    lib = tmp_path / "libmutant.so"
+    subprocess.run(["gcc", "-O2", "-fno-fast-math", "-ffp-contract=off", "-fopenmp", "-fPIC", "-shared", "-std=c99",
+                    "-o", str(lib), str(mut), "-lm"], check=True)
+    oracle.use_library(str(lib))
+    try:
+        assert _run_pins() > 0, f"no pin rejects the planted mistake {name}"
+    finally:
+        oracle.use_library(None)
+
+
+def test_unmutated_oracle_passes_all_pins():
+    assert _run_pins() == 0
