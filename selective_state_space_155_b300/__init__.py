@@ -1,0 +1,113 @@
+"""B300-native (sm_103a) selective scan of the Mamba selective state-space model.
+
+Python binding of the C-ABI in ``include/ssm_scan.h``: the functions below only marshal
+torch CUDA tensors into device pointers and the current stream, then call the library
+(``libssm_scan.so``), which runs every step of the path in its own kernels.  PyTorch
+provides device memory and streams; nothing is computed in Python.
+
+    y, last_state = ssm_scan_fwd(u, delta, A, B, C, D, z, dt_bias, delta_softplus=True)
+    out = ssm_state_update(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus=True)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _native
+from ._native import SsmError, lib, status_string  # noqa: F401
+
+__all__ = ["ssm_scan_fwd", "ssm_state_update", "SsmError", "lib", "status_string", "io_dtype_code"]
+
+_IO = {torch.float32: _native.SSM_F32, torch.bfloat16: _native.SSM_BF16}
+
+
+def io_dtype_code(dtype: torch.dtype) -> int:
+    if dtype not in _IO:
+        raise TypeError(f"unsupported io dtype {dtype}; use float32 or bfloat16")
+    return _IO[dtype]
+
+
+def _ptr(t: torch.Tensor | None, dtype: torch.dtype | None = None, shape=None, name: str = "") -> int | None:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t.data_ptr() or None
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream or None
+    return getattr(stream, "cuda_stream", stream) or None
+
+
+def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, y=None, last_state=None,
+                 h0=None, return_last_state=True, stream=None):
+    """Selective scan forward (``ssm_scan_fwd`` / ``ssm_scan_fwd_h0`` of the C-ABI).
+
+    u, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (float32 or bfloat16, all the same);
+    A: [dim, dstate], D, dt_bias: [dim], h0: [batch, dim, dstate] (float32).
+    Returns (y, last_state); y has u's dtype, last_state is float32 (None if not requested).
+    """
+    batch, dim, L = u.shape
+    dstate = A.shape[1]
+    io = io_dtype_code(u.dtype)
+    if y is None:
+        y = torch.empty_like(u)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=u.device)
+    args = [
+        _ptr(u, u.dtype, (batch, dim, L), "u"),
+        _ptr(delta, u.dtype, (batch, dim, L), "delta"),
+        _ptr(A, torch.float32, (dim, dstate), "A"),
+        _ptr(B, u.dtype, (batch, dstate, L), "B"),
+        _ptr(C, u.dtype, (batch, dstate, L), "C"),
+        _ptr(D, torch.float32, (dim,), "D"),
+        _ptr(z, u.dtype, (batch, dim, L), "z"),
+        _ptr(dt_bias, torch.float32, (dim,), "dt_bias"),
+        int(bool(delta_softplus)),
+    ]
+    tail = [
+        _ptr(y, u.dtype, (batch, dim, L), "y"),
+        _ptr(last_state, torch.float32, (batch, dim, dstate), "last_state"),
+        batch, dim, dstate, L, io, _stream(stream),
+    ]
+    if h0 is None:
+        _native.check("ssm_scan_fwd", lib().ssm_scan_fwd(*args, *tail))
+    else:
+        h0p = _ptr(h0, torch.float32, (batch, dim, dstate), "h0")
+        _native.check("ssm_scan_fwd_h0", lib().ssm_scan_fwd_h0(*args, h0p, *tail))
+    return y, last_state
+
+
+def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, out=None, stream=None):
+    """One decode step (``ssm_state_update`` of the C-ABI); `state` is updated in place.
+
+    state: [batch, dim, dstate] float32; x, dt, z: [batch, dim]; B, C: [batch, dstate]
+    (float32 or bfloat16); A: [dim, dstate], D, dt_bias: [dim] float32.  Returns out [batch, dim].
+    """
+    batch, dim, dstate = state.shape
+    io = io_dtype_code(x.dtype)
+    if out is None:
+        out = torch.empty_like(x)
+    st = lib().ssm_state_update(
+        _ptr(state, torch.float32, (batch, dim, dstate), "state"),
+        _ptr(x, x.dtype, (batch, dim), "x"),
+        _ptr(dt, x.dtype, (batch, dim), "dt"),
+        _ptr(A, torch.float32, (dim, dstate), "A"),
+        _ptr(B, x.dtype, (batch, dstate), "B"),
+        _ptr(C, x.dtype, (batch, dstate), "C"),
+        _ptr(D, torch.float32, (dim,), "D"),
+        _ptr(z, x.dtype, (batch, dim), "z"),
+        _ptr(dt_bias, torch.float32, (dim,), "dt_bias"),
+        int(bool(dt_softplus)),
+        _ptr(out, x.dtype, (batch, dim), "out"),
+        batch, dim, dstate, io, _stream(stream),
+    )
+    _native.check("ssm_state_update", st)
+    return out

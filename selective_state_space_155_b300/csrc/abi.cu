@@ -1,0 +1,98 @@
+// extern "C" entry points of the library: host-side validation, then one launch on the caller's
+// stream.  Nothing here allocates, synchronises or keeps state between calls.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "ssm_scan.h"
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t io_size(int io) { return io == SSM_F32 ? 4 : 2; }
+
+}  // namespace
+
+extern "C" {
+
+int ssm_abi_version(void) { return 1; }
+
+const char* ssm_status_string(int status) {
+  switch (status) {
+    case SSM_OK: return "ok";
+    case SSM_ERR_NULL: return "a required pointer is NULL";
+    case SSM_ERR_SHAPE: return "a size is negative or dstate < 1";
+    case SSM_ERR_DTYPE: return "io_dtype is not SSM_F32 or SSM_BF16";
+    case SSM_ERR_ALIGN: return "a pointer is not aligned to its element size";
+    case SSM_ERR_UNSUPPORTED: return "unsupported size (dstate > 16 or grid overflow)";
+    case SSM_ERR_LAUNCH: return "the CUDA kernel launch failed";
+    case SSM_ERR_TIMEOUT: return "a bounded in-kernel wait gave up";
+    default: return "unknown status";
+  }
+}
+
+int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, void* stream) {
+  if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (dstate > 16) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0) return SSM_OK;
+  if (!A) return SSM_ERR_NULL;
+  if (seqlen > 0 && (!u || !delta || !B || !C || !y)) return SSM_ERR_NULL;
+  if (seqlen == 0 && !last_state) return SSM_OK;
+  const size_t es = io_size(io_dtype);
+  const void* io_ptrs[] = {u, delta, B, C, z, y};
+  for (const void* p : io_ptrs)
+    if (!aligned(p, es)) return SSM_ERR_ALIGN;
+  const void* f_ptrs[] = {A, D, dt_bias, h0, last_state};
+  for (const void* p : f_ptrs)
+    if (!aligned(p, 4)) return SSM_ERR_ALIGN;
+  if ((long long)((dim + 31) / 32) * batch > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+
+  ssm::ScanArgs a{};
+  a.u = u, a.delta = delta, a.A = A, a.B = B, a.C = C, a.D = D, a.z = z, a.dt_bias = dt_bias, a.h0 = h0;
+  a.y = y, a.last_state = last_state;
+  a.batch = batch, a.dim = dim, a.dstate = dstate, a.seqlen = seqlen;
+  a.softplus = delta_softplus ? 1 : 0;
+  a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  const cudaError_t err = ssm::launch_scan_fwd(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* dt_bias, int delta_softplus, void* y, float* last_state, int batch,
+                 int dim, int dstate, int seqlen, int io_dtype, void* stream) {
+  return ssm_scan_fwd_h0(u, delta, A, B, C, D, z, dt_bias, delta_softplus, nullptr, y, last_state, batch, dim, dstate,
+                         seqlen, io_dtype, stream);
+}
+
+int ssm_state_update(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+                     const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
+                     int dim, int dstate, int io_dtype, void* stream) {
+  if (batch < 0 || dim < 0 || dstate < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (dstate > 16) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0) return SSM_OK;
+  if (!state || !x || !dt || !A || !B || !C || !out) return SSM_ERR_NULL;
+  const size_t es = io_size(io_dtype);
+  const void* io_ptrs[] = {x, dt, B, C, z, out};
+  for (const void* p : io_ptrs)
+    if (!aligned(p, es)) return SSM_ERR_ALIGN;
+  const void* f_ptrs[] = {state, A, D, dt_bias};
+  for (const void* p : f_ptrs)
+    if (!aligned(p, 4)) return SSM_ERR_ALIGN;
+  if ((long long)batch * dim * 4 / 256 + 1 > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+
+  ssm::UpdateArgs a{};
+  a.state = state, a.x = x, a.dt = dt, a.A = A, a.B = B, a.C = C, a.D = D, a.z = z, a.dt_bias = dt_bias;
+  a.out = out;
+  a.batch = batch, a.dim = dim, a.dstate = dstate;
+  a.softplus = dt_softplus ? 1 : 0;
+  a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  const cudaError_t err = ssm::launch_state_update(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+}  // extern "C"

@@ -1,0 +1,90 @@
+// Device helpers for the scan kernels: MUFU approximations, softplus, silu, io conversions.
+//
+// Accuracy (float32 arithmetic throughout):
+//  * ex2.approx.ftz.f32 / lg2.approx.ftz.f32 / rcp.approx.ftz.f32 are the PTX special-function
+//    approximations (a few ulp; subnormal results flush to zero).
+//  * softplus(x) = max(x, 0) + log1p(e), e = exp(-|x|) in (0, 1].  log1p(e) uses the alternating
+//    Taylor series e - e^2/2 + ... - e^6/6 when e < 1/16 (truncation below e^7/7 < 5e-10
+//    relative), and lg2(1 + e) * ln 2 otherwise (there 1 + e >= 17/16, so lg2's absolute error
+//    stays small next to the result).  This avoids the relative-precision loss of log(1 + e)
+//    for small e, which feeds Delta and therefore every state update.
+//  * silu(z) = z / (1 + 2^(-z log2 e)).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ float softplus_f32(float x) {
+  const float e = ex2_approx(-fabsf(x) * kLog2e);
+  // Horner form of e - e^2/2 + e^3/3 - e^4/4 + e^5/5 - e^6/6
+  float s = fmaf(e, -1.0f / 6.0f, 1.0f / 5.0f);
+  s = fmaf(e, -s, 1.0f / 4.0f);
+  s = fmaf(e, -s, 1.0f / 3.0f);
+  s = fmaf(e, -s, 1.0f / 2.0f);
+  s = fmaf(e, -s, 1.0f);
+  s *= e;
+  const float viaLog = lg2_approx(1.0f + e) * kLn2;
+  return fmaxf(x, 0.0f) + (e < 0.0625f ? s : viaLog);
+}
+
+__device__ __forceinline__ float silu_f32(float z) { return z * rcp_approx(1.0f + ex2_approx(-z * kLog2e)); }
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T v);
+template <>
+__device__ __forceinline__ float to_f32<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
+  return __bfloat162float(v);
+}
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float v);
+template <>
+__device__ __forceinline__ float from_f32<float>(float v) {
+  return v;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+  return __float2bfloat16_rn(v);
+}
+
+// 16-byte asynchronous global->shared copy; bytes in [0, 16] are read, the rest is zero-filled.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src, int src_bytes) {
+  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(gmem_src), "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+
+}  // namespace ssm

@@ -1,0 +1,51 @@
+// Internal declarations shared by the library's translation units (not part of the C-ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+namespace ssm {
+
+enum Io { kF32 = 0, kBF16 = 1 };
+
+// Arguments of one selective-scan launch; pointer and layout meaning as in ssm_scan.h.
+struct ScanArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* dt_bias;
+  const float* h0;
+  void* y;
+  float* last_state;
+  int batch, dim, dstate, seqlen;
+  int softplus;
+  int io;
+};
+
+// Arguments of one decode step; pointer and layout meaning as in ssm_scan.h.
+struct UpdateArgs {
+  float* state;
+  const void* x;
+  const void* dt;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* dt_bias;
+  void* out;
+  int batch, dim, dstate;
+  int softplus;
+  int io;
+};
+
+// Enqueue the scan on `stream`.  Arguments are already validated.
+cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream);
+
+// Enqueue one decode step on `stream`.  Arguments are already validated.
+cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);
+
+}  // namespace ssm

@@ -191,7 +191,10 @@ def random_scan_case(batch, dim, dstate, seqlen, io="f32", seed=0, gate=True, us
     A_log = rng.uniform(-1.0, 2.5, size=(dim, dstate))
     A = torch.from_numpy((-np.exp(A_log)).astype(np.float32))
     dt = np.exp(rng.uniform(math.log(1e-3), math.log(1e-1), size=dim))
-    dt_bias = torch.from_numpy(np.log(np.expm1(dt)).astype(np.float32)) if use_bias else None
+    # with softplus the bias is log(expm1(dt)) (softplus(bias) = dt); without it the bias is dt
+    # itself, so that Delta = delta + bias stays positive and the system stable
+    bias = np.log(np.expm1(dt)) if softplus else dt
+    dt_bias = torch.from_numpy(bias.astype(np.float32)) if use_bias else None
     u = _round_io(rng.standard_normal(shp) * u_std, io)
     delta = _round_io(rng.standard_normal(shp) if softplus else np.abs(rng.standard_normal(shp)) * 0.1, io)
     z = _round_io(rng.standard_normal(shp), io) if gate else None

@@ -1,0 +1,38 @@
+"""Shared helpers of the GPU parity tests: tolerances and comparisons against the oracle."""
+import numpy as np
+import torch
+
+import ssm_workloads as wl
+from oracle import oracle
+
+# Tolerances (element-wise, |got - ref| <= tol * (1 + |ref|)):
+#   float32 io: 1e-4 on y and on the state;
+#   bf16 io:    2e-2 on y (the bf16 output rounding alone is 2^-9 relative), 1e-4 on the
+#               float32 state.
+TOL = {"f32": (1e-4, 1e-4), "bf16": (2e-2, 1e-4)}
+
+
+def io_name(t: torch.Tensor) -> str:
+    return "f32" if t.dtype == torch.float32 else "bf16"
+
+
+def rel_err(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    return float(np.max(np.abs(got - ref) / (1.0 + np.abs(ref)))) if ref.size else 0.0
+
+
+def assert_close(got, ref, tol, what):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = rel_err(got, ref)
+    assert err <= tol, f"{what}: max |got-ref|/(1+|ref|) = {err:.3e} > {tol:.1e}"
+    return err
+
+
+def oracle_scan(inp, softplus=True, h0=None):
+    f = wl.to_f64
+    return oracle.scan(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), f(inp.get("D")),
+                       f(inp.get("z")), f(inp.get("dt_bias")), delta_softplus=softplus, h0=f(h0))
+
+
+def to_device(inp, dev):
+    return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}

@@ -1,0 +1,125 @@
+"""Host-side checks of the C-ABI library (no GPU needed, nothing is launched).
+
+The library must load on a machine without a driver, export every function that
+include/ssm_scan.h declares, and reject bad arguments on the host before any launch.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from selective_state_space_155_b300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build_library()
+    return _native.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    assert declared_functions() == sorted(
+        ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_state_update", "ssm_status_string"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), f"{name} not exported"
+    assert set(declared_functions()) == set(_native.SIGNATURES)
+
+
+def test_status_strings(lib):
+    assert lib.ssm_abi_version() == 1
+    for code in range(-7, 1):
+        s = lib.ssm_status_string(code).decode()
+        assert s and s != "unknown status"
+    assert lib.ssm_status_string(42).decode() == "unknown status"
+
+
+P = 0x10000  # a fake, 64 KiB aligned "device address": validation never dereferences pointers
+
+
+def scan_args(**over):
+    a = dict(u=P, delta=P, A=P, B=P, C=P, D=P, z=P, dt_bias=P, softplus=1, y=P, last=P, batch=2, dim=3, dstate=16,
+             seqlen=5, io=_native.SSM_F32, stream=None)
+    a.update(over)
+    return [a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["dt_bias"], a["softplus"], a["y"],
+            a["last"], a["batch"], a["dim"], a["dstate"], a["seqlen"], a["io"], a["stream"]]
+
+
+@pytest.mark.parametrize("over,expected", [
+    (dict(u=None), _native.SSM_ERR_NULL),
+    (dict(delta=None), _native.SSM_ERR_NULL),
+    (dict(A=None), _native.SSM_ERR_NULL),
+    (dict(B=None), _native.SSM_ERR_NULL),
+    (dict(C=None), _native.SSM_ERR_NULL),
+    (dict(y=None), _native.SSM_ERR_NULL),
+    (dict(batch=-1), _native.SSM_ERR_SHAPE),
+    (dict(dim=-1), _native.SSM_ERR_SHAPE),
+    (dict(seqlen=-1), _native.SSM_ERR_SHAPE),
+    (dict(dstate=0), _native.SSM_ERR_SHAPE),
+    (dict(dstate=17), _native.SSM_ERR_UNSUPPORTED),
+    (dict(io=7), _native.SSM_ERR_DTYPE),
+    (dict(u=P + 2), _native.SSM_ERR_ALIGN),
+    (dict(A=P + 2), _native.SSM_ERR_ALIGN),
+    (dict(last=P + 1), _native.SSM_ERR_ALIGN),
+    (dict(io=_native.SSM_BF16, z=P + 1), _native.SSM_ERR_ALIGN),
+    (dict(batch=0), _native.SSM_OK),
+    (dict(dim=0, u=None, y=None), _native.SSM_OK),
+    (dict(seqlen=0, u=None, delta=None, B=None, C=None, y=None, last=None), _native.SSM_OK),
+])
+def test_scan_validation(lib, over, expected):
+    assert lib.ssm_scan_fwd(*scan_args(**over)) == expected
+
+
+def test_scan_h0_validation(lib):
+    args = scan_args()
+    h0_args = args[:9] + [P + 2] + args[9:]
+    assert lib.ssm_scan_fwd_h0(*h0_args) == _native.SSM_ERR_ALIGN
+    h0_args = scan_args(u=None)[:9] + [P] + scan_args(u=None)[9:]
+    assert lib.ssm_scan_fwd_h0(*h0_args) == _native.SSM_ERR_NULL
+
+
+def update_args(**over):
+    a = dict(state=P, x=P, dt=P, A=P, B=P, C=P, D=P, z=P, dt_bias=P, softplus=1, out=P, batch=2, dim=3, dstate=16,
+             io=_native.SSM_BF16, stream=None)
+    a.update(over)
+    return [a[k] for k in ("state", "x", "dt", "A", "B", "C", "D", "z", "dt_bias", "softplus", "out", "batch", "dim",
+                           "dstate", "io", "stream")]
+
+
+@pytest.mark.parametrize("over,expected", [
+    (dict(state=None), _native.SSM_ERR_NULL),
+    (dict(x=None), _native.SSM_ERR_NULL),
+    (dict(dt=None), _native.SSM_ERR_NULL),
+    (dict(out=None), _native.SSM_ERR_NULL),
+    (dict(B=None), _native.SSM_ERR_NULL),
+    (dict(batch=-3), _native.SSM_ERR_SHAPE),
+    (dict(dstate=0), _native.SSM_ERR_SHAPE),
+    (dict(dstate=99), _native.SSM_ERR_UNSUPPORTED),
+    (dict(io=-1), _native.SSM_ERR_DTYPE),
+    (dict(state=P + 2), _native.SSM_ERR_ALIGN),
+    (dict(x=P + 1), _native.SSM_ERR_ALIGN),
+    (dict(batch=0), _native.SSM_OK),
+])
+def test_update_validation(lib, over, expected):
+    assert lib.ssm_state_update(*update_args(**over)) == expected
+
+
+def test_binding_rejects_cpu_tensors():
+    import torch
+    import selective_state_space_155_b300 as ssm
+    u = torch.zeros(1, 2, 3)
+    with pytest.raises(ValueError, match="CUDA"):
+        ssm.ssm_scan_fwd(u, u, torch.zeros(2, 4), torch.zeros(1, 4, 3), torch.zeros(1, 4, 3))
