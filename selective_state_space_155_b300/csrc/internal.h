@@ -42,8 +42,16 @@ struct UpdateArgs {
   int io;
 };
 
-// Enqueue the scan on `stream`.  Arguments are already validated.
+// Enqueue the scan on `stream`.  Arguments are already validated.  Picks the lane-per-channel
+// form when there are enough channels to give every SM two or more of its warps, otherwise the
+// four-lanes-per-channel form; SSM_SCAN_VARIANT=lane|quad in the environment forces one.
 cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream);
+
+// The four-lanes-per-channel form (scan_fwd.cu).
+cudaError_t launch_scan_fwd_quad(const ScanArgs& a, bool vec, cudaStream_t stream);
+
+// The lane-per-channel form (scan_fwd_lane.cu).
+cudaError_t launch_scan_fwd_lane(const ScanArgs& a, bool vec, cudaStream_t stream);
 
 // Enqueue one decode step on `stream`.  Arguments are already validated.
 cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);

@@ -1,30 +1,41 @@
 // Selective scan forward for sm_103a.
 //
-// What it computes (per batch row b, channel d, state n; see ssm_scan.h for the sources):
+// What it computes (per batch row b, channel d, state n; sources cited in ssm_scan.h):
 //   Delta_t = softplus(delta_t + dt_bias[d]);  Abar = exp(Delta_t A[d,n]);  h_t = Abar h_{t-1} + Delta_t B_t[n] u_t
 //   y_t = sum_n C_t[n] h_t[n] + D[d] u_t;  out_t = y_t * silu(z_t);  last_state = h_{L-1}
 //
-// Design (B300: 148 SMs, MUFU ex2 32/clk/SM, FP32 FMA 128/clk/SM, packed f32x2 FMA at the same
-// lane rate).  The path is a scan, not a contraction, so it runs on the SIMT pipes:
-//  * A CTA owns CPB channels of one batch row and walks L in chunks of CHUNK steps.  Chunk k+1
-//    is fetched with 16-byte cp.async (zero-filled past the sequence end) while chunk k is
+// Why it looks like this (B300: 148 SMs; per SM and clock 32 MUFU ex2, 128 FP32 FMA lanes, and
+// packed f32x2 FMA at the same lane rate but half the issue slots).  The scan is not a
+// contraction, so it runs on the SIMT pipes, and it is bound by issue slots, the MUFU pipe
+// (16 exps per element) and the FMA pipe (4 flops per state) well before HBM.  Every design
+// choice below removes instructions per element:
+//  * A CTA owns 32 channels of one batch row and walks L in chunks of 32 steps.  Chunk k+1 is
+//    fetched with 16-byte cp.async (zero-filled past the sequence end) while chunk k is
 //    computed, so HBM sees u, delta, z, B, C once and y once; the expanded (L, D, N) tensors
-//    Abar and Bbar never exist outside registers.
-//  * Four states per lane: a channel spans R = NPAD/4 lanes.  The float32 state lives in
-//    registers for the whole sequence and is the carried prefix between chunks.
-//  * Per chunk, a prologue turns (delta, u) into (Delta, Delta*u) once per (channel, t) and
-//    parks them in shared memory, so softplus is not repeated by the R lanes of a channel.
-//  * The readout sum over n spans the R lanes of a channel: each group of R consecutive steps
-//    is reduced with a transpose-reduce (R-1 shuffles per R outputs per lane), after which lane
-//    g owns step g of the group and runs the D skip, the gate and the output rounding for it.
-//  * Padded states (n >= dstate) get A = 0 and B = C = 0; padded steps (t >= seqlen) get
+//    never exist outside registers.
+//  * Four states per lane, R = NPAD/4 lanes per channel; the float32 state stays in registers
+//    for the whole sequence and is the carried prefix from chunk to chunk.
+//  * Per chunk, a prologue does all per-element work once, two steps at a time with packed
+//    math: softplus, Delta*u, D*u and silu(z).  The recurrence then reads (Delta, Delta, Du,
+//    Du) as one 16-byte shared load per step, already in the register pairs the packed
+//    instructions take.
+//  * The recurrence runs on float2 pairs of states (mul/fma.f32x2) over a window of 16 steps,
+//    fully unrolled, keeping the 16 readout partials C.h (one float2 pair per step) in registers:
+//    the exps of later steps do not depend on the state, so they overlap the state's FMA chain.
+//  * Then the sum over the R lanes of a channel and over the pair halves for all 16 steps at once
+//    goes through shared memory (a rotated layout that is conflict-free for both the 16-byte
+//    stores and the loads), after which lane (c, q) owns 16/R consecutive steps of channel c:
+//    (y + D u) * silu(z), rounded to the io type, leaves as one vector store to HBM.
+//  * Padded states (n >= dstate) have A = 0 and B = C = 0; padded steps (t >= seqlen) have
 //    Delta = 0.  Both leave the state unchanged, so one code path serves every size.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include <algorithm>
 #include <atomic>
+#include <cstdlib>
+#include <cstring>
+#include <type_traits>
 
 #include "device_math.cuh"
 #include "internal.h"
@@ -32,42 +43,114 @@
 namespace ssm {
 namespace {
 
-constexpr int kChunk = 64;
+constexpr int kChunk = 32;  // steps per chunk
+constexpr int kWin = 16;    // steps per recurrence window (readout partials held in registers)
 
 template <typename T, int NPAD>
 struct ScanCfg {
-  static constexpr int R = NPAD / 4;             // lanes per channel
-  static constexpr int WARPS = R;                // so that every CTA holds 32 channels
-  static constexpr int NT = 32 * WARPS;          // threads per CTA
-  static constexpr int CPW = 32 / R;             // channels per warp
-  static constexpr int CPB = CPW * WARPS;        // channels per CTA (32)
-  static constexpr int EPV = 16 / sizeof(T);     // elements per 16-byte vector
-  static constexpr int RS = kChunk + EPV;        // padded row stride (elements) of staged rows
-  static constexpr int VPR = kChunk / EPV;       // vectors per staged row
-  static constexpr int ROWS = 3 * CPB + 2 * NPAD;  // u, delta, z rows, then B rows, then C rows
-  static constexpr int PS = CPB + 4;             // padded row stride (float2) of the (Delta, Delta*u) table
-  // shared memory map (bytes)
+  static constexpr int R = NPAD / 4;                  // lanes per channel
+  static constexpr int WARPS = R;                     // every CTA holds 32 channels
+  static constexpr int NT = 32 * WARPS;               // threads per CTA
+  static constexpr int CPW = 32 / R;                  // channels per warp
+  static constexpr int CPB = CPW * WARPS;             // channels per CTA (32)
+  static constexpr int EPV = 16 / sizeof(T);          // elements per 16-byte vector
+  static constexpr int RS = kChunk + EPV;             // padded row stride (elements) of staged rows
+  static constexpr int VPR = kChunk / EPV;            // 16-byte vectors per staged row
+  static constexpr int ROWS = 3 * CPB + 2 * NPAD;     // u, delta, z rows, then B rows, then C rows
+  static constexpr int DSS = kChunk + 2;              // row stride (float2) of the (Du, silu z) table: an odd
+                                                      // number of 16-byte units keeps its stores conflict-free
   static constexpr size_t kRawStage = size_t(ROWS) * RS * sizeof(T);
-  static constexpr size_t kRaw = 2 * kRawStage;
-  static constexpr size_t kBC = size_t(2) * kChunk * NPAD * sizeof(float);
-  static constexpr size_t kP = size_t(kChunk) * PS * sizeof(float2);
-  static constexpr size_t kY = size_t(CPB) * RS * sizeof(T);
-  static constexpr size_t kSmem = kRaw + kBC + kP + kY;
+  static constexpr size_t kRaw = 2 * kRawStage;                              // [2][ROWS][RS] T
+  static constexpr size_t kBC = size_t(2) * kChunk * NPAD * sizeof(float);   // Bs, Cs [CHUNK][NPAD]
+  static constexpr size_t kP = size_t(kChunk) * CPB * sizeof(float4);        // Ps [CHUNK][CPB]
+  static constexpr size_t kDS = size_t(CPB) * DSS * sizeof(float2);          // DS [CPB][DSS]
+  static constexpr int OPL = kWin / R;                // outputs each lane finishes per window
+  static constexpr int UPB = kWin / 2;                // 16-byte units per lane block of readout partials
+  static constexpr size_t kRed = R > 1 ? size_t(NT) * UPB * 16 : 0;         // red [NT][UPB] float4
+  static constexpr size_t kSmem = kRaw + kBC + kP + kDS + kRed;
 };
+
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+
+// Position of 16-byte unit i (readout partials of steps 2i, 2i+1) in the block of lane (cw, g).
+// For R = 4 the rotation by 2g + (cw & 1) makes both access patterns conflict-free: lane (cw, g)
+// storing unit i, and lane (cw, q) loading units 2q, 2q+1 of partner g's block.
+template <int R>
+__device__ __forceinline__ int red_rot(int cw, int g, int i) {
+  if constexpr (R == 4) return (i + 2 * g + (cw & 1)) & (kWin / 2 - 1);
+  return i;
+}
+
+// softplus of two values with packed arithmetic where it exists (see device_math.cuh for the method)
+__device__ __forceinline__ float2 softplus2(float2 x) {
+  const float2 e = f2(ex2_approx(-fabsf(x.x) * kLog2e), ex2_approx(-fabsf(x.y) * kLog2e));
+  // e * (1 - e/2 + e^2/3 - e^3/4 + e^4/5 - e^5/6) in Horner form
+  float2 s = __ffma2_rn(e, f2(-1.0f / 6.0f, -1.0f / 6.0f), f2(1.0f / 5.0f, 1.0f / 5.0f));
+  s = __ffma2_rn(e, s, f2(-1.0f / 4.0f, -1.0f / 4.0f));
+  s = __ffma2_rn(e, s, f2(1.0f / 3.0f, 1.0f / 3.0f));
+  s = __ffma2_rn(e, s, f2(-1.0f / 2.0f, -1.0f / 2.0f));
+  s = __ffma2_rn(e, s, f2(1.0f, 1.0f));
+  s = __fmul2_rn(s, e);
+  const float2 l = __fmul2_rn(f2(lg2_approx(1.0f + e.x), lg2_approx(1.0f + e.y)), f2(kLn2, kLn2));
+  return f2(fmaxf(x.x, 0.0f) + (e.x < 0.0625f ? s.x : l.x), fmaxf(x.y, 0.0f) + (e.y < 0.0625f ? s.y : l.y));
+}
+
+template <typename T>
+__device__ __forceinline__ float2 load2(const T* p);  // two consecutive io elements as float32
+template <>
+__device__ __forceinline__ float2 load2<float>(const float* p) {
+  return *reinterpret_cast<const float2*>(p);
+}
+template <>
+__device__ __forceinline__ float2 load2<__nv_bfloat16>(const __nv_bfloat16* p) {
+  return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+// Store n consecutive outputs (n <= OPL valid ones of the OPL given) as io type.  With VEC the
+// row is 16-byte aligned and its length a multiple of 16 bytes, so every 16-byte (or, for 8-byte
+// groups, 8-byte) piece is either wholly inside the row or wholly past its end.
+template <typename T, int OPL, bool VEC>
+__device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) {
+  if constexpr (VEC && std::is_same<T, __nv_bfloat16>::value) {
+    uint32_t w[OPL / 2];
+#pragma unroll
+    for (int j = 0; j < OPL / 2; ++j) {
+      const __nv_bfloat162 p = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+      w[j] = *reinterpret_cast<const uint32_t*>(&p);
+    }
+    if constexpr (OPL == 4) {
+      if (n >= 4) *reinterpret_cast<uint2*>(dst) = make_uint2(w[0], w[1]);
+    } else {
+#pragma unroll
+      for (int q = 0; q < OPL / 8; ++q)
+        if (n >= 8 * q + 8)
+          *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(w[4 * q], w[4 * q + 1], w[4 * q + 2], w[4 * q + 3]);
+    }
+  } else if constexpr (VEC) {
+#pragma unroll
+    for (int q = 0; q < OPL / 4; ++q)
+      if (n >= 4 * q + 4)
+        *reinterpret_cast<float4*>(dst + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < OPL; ++j)
+      if (j < n) dst[j] = from_f32<T>(v[j]);
+  }
+}
 
 template <typename T, int NPAD, bool VEC>
 __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const ScanArgs a) {
   using Cfg = ScanCfg<T, NPAD>;
   constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, RS = Cfg::RS, VPR = Cfg::VPR;
-  constexpr int kThreads = Cfg::NT;
-  constexpr int ROWS = Cfg::ROWS, PS = Cfg::PS;
+  constexpr int NT = Cfg::NT, ROWS = Cfg::ROWS, DSS = Cfg::DSS, OPL = Cfg::OPL, UPB = Cfg::UPB;
 
   extern __shared__ __align__(16) unsigned char smem[];
-  T* raw = reinterpret_cast<T*>(smem);  // [2][ROWS][RS]
-  float* Bs = reinterpret_cast<float*>(smem + Cfg::kRaw);  // [CHUNK][NPAD]
-  float* Cs = Bs + kChunk * NPAD;                          // [CHUNK][NPAD]
-  float2* Ps = reinterpret_cast<float2*>(smem + Cfg::kRaw + Cfg::kBC);  // [CHUNK][PS]
-  T* Ys = reinterpret_cast<T*>(smem + Cfg::kRaw + Cfg::kBC + Cfg::kP);   // [CPB][RS]
+  T* raw = reinterpret_cast<T*>(smem);
+  float* Bs = reinterpret_cast<float*>(smem + Cfg::kRaw);
+  float* Cs = Bs + kChunk * NPAD;
+  float4* Ps = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kBC);
+  float2* DS = reinterpret_cast<float2*>(smem + Cfg::kRaw + Cfg::kBC + Cfg::kP);
+  float4* red = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kBC + Cfg::kP + Cfg::kDS);
 
   const int tid = threadIdx.x;
   const int nblk_d = (a.dim + CPB - 1) / CPB;
@@ -75,7 +158,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
   const int d0 = (blockIdx.x % nblk_d) * CPB;
   const int warp = tid >> 5, lane = tid & 31;
   const int cw = lane / R, g = lane % R;
-  const int cl = warp * CPW + cw;  // channel within the CTA
+  const int cl = warp * CPW + cw;  // this lane's channel within the CTA (recurrence mapping)
   const int d = d0 + cl;
   const bool ch_ok = d < a.dim;
   const int L = a.seqlen, N = a.dstate;
@@ -88,18 +171,28 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
   const T* __restrict__ gC = static_cast<const T*>(a.C);
   T* __restrict__ gy = static_cast<T*>(a.y);
 
-  // Per-lane constants and state: states n = 4g .. 4g+3 of channel d.
-  float A2[4], h[4];
+  // Recurrence lane: states n = 4g .. 4g+3 of channel d, as two float2 pairs.
+  float2 A01, A23, h01, h23;
+  {
+    float Av[4], hv[4];
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int n = 4 * g + i;
-    const bool ok = ch_ok && n < N;
-    A2[i] = ok ? a.A[size_t(d) * N + n] * kLog2e : 0.0f;
-    h[i] = (ok && a.h0) ? a.h0[(size_t(b) * a.dim + d) * N + n] : 0.0f;
+    for (int i = 0; i < 4; ++i) {
+      const int n = 4 * g + i;
+      const bool ok = ch_ok && n < N;
+      Av[i] = ok ? a.A[size_t(d) * N + n] * kLog2e : 0.0f;
+      hv[i] = (ok && a.h0) ? a.h0[(size_t(b) * a.dim + d) * N + n] : 0.0f;
+    }
+    A01 = f2(Av[0], Av[1]), A23 = f2(Av[2], Av[3]);
+    h01 = f2(hv[0], hv[1]), h23 = f2(hv[2], hv[3]);
   }
-  const float Dd = (ch_ok && a.D) ? a.D[d] : 0.0f;
 
-  // Source row of staged row r (u, delta, z rows of the CTA's channels, then B and C rows).
+  // Prologue lane: channel pc of this warp (fixed, since 32 is a multiple of CPW), step pairs tp.
+  const int pc = lane % CPW;
+  const int pcl = warp * CPW + pc;
+  const bool pch_ok = d0 + pcl < a.dim;
+  const float p_bias = (pch_ok && a.dt_bias) ? a.dt_bias[d0 + pcl] : 0.0f;
+  const float p_D = (pch_ok && a.D) ? a.D[d0 + pcl] : 0.0f;
+
   auto row_src = [&](int r, bool& ok) -> const T* {
     if (r < 3 * CPB) {
       const int which = r / CPB, c = r % CPB;
@@ -116,7 +209,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
   auto stage_load = [&](int stage, int t0) {
     T* dst = raw + size_t(stage) * ROWS * RS;
     if constexpr (VEC) {
-      for (int v = tid; v < ROWS * VPR; v += kThreads) {
+      for (int v = tid; v < ROWS * VPR; v += NT) {
         const int r = v / VPR, j = v % VPR;
         if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;  // z rows are never read without a gate
         bool ok;
@@ -128,7 +221,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
         cp_async_16(dst + r * RS + j * EPV, bytes > 0 ? static_cast<const void*>(src + t) : gu, bytes);
       }
     } else {
-      for (int e = tid; e < ROWS * kChunk; e += kThreads) {
+      for (int e = tid; e < ROWS * kChunk; e += NT) {
         const int r = e / kChunk, j = e % kChunk;
         if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;
         bool ok;
@@ -142,6 +235,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
   const int nchunks = (L + kChunk - 1) / kChunk;
   if (nchunks > 0) stage_load(0, 0);
   cp_async_commit();
+  T* yrow = gy + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L;  // this lane's output row (finishing mapping)
 
   for (int k = 0; k < nchunks; ++k) {
     const int t0 = k * kChunk;
@@ -157,101 +251,106 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
     const T* sB = st + 3 * CPB * RS;
     const T* sC = sB + NPAD * RS;
 
-    // (a) B, C rows -> float32 [t][n] tables.
-    for (int e = tid; e < 2 * kChunk * NPAD; e += kThreads) {
-      const int which = e / (kChunk * NPAD), rem = e % (kChunk * NPAD);
-      const int t = rem / NPAD, n = rem % NPAD;
-      const T* srow = (which == 0 ? sB : sC) + n * RS;
-      (which == 0 ? Bs : Cs)[t * NPAD + n] = to_f32<T>(srow[t]);
+    // (a) B, C rows -> float32 [t][n] tables, two steps per thread and iteration.
+    for (int e = tid; e < NPAD * kChunk; e += NT) {  // 2 tables x NPAD rows x CHUNK/2 step pairs
+      const int which = e / (NPAD * kChunk / 2), rem = e % (NPAD * kChunk / 2);
+      const int tp = rem / NPAD, n = rem % NPAD;
+      const float2 v = load2<T>((which == 0 ? sB : sC) + n * RS + 2 * tp);
+      float* dst = which == 0 ? Bs : Cs;
+      dst[(2 * tp) * NPAD + n] = v.x;
+      dst[(2 * tp + 1) * NPAD + n] = v.y;
     }
-    // (b) (Delta, Delta*u) for this warp's channels; zero past the sequence end.
-    {
-      for (int e = lane; e < CPW * kChunk; e += 32) {
-        const int c = e % CPW, t = e / CPW;
-        const int clc = warp * CPW + c, dc = d0 + clc;
-        float dl = 0.0f, du = 0.0f;
-        if (t0 + t < L && dc < a.dim) {
-          float x = to_f32<T>(sd[clc * RS + t]);
-          if (a.dt_bias) x += a.dt_bias[dc];
-          dl = a.softplus ? softplus_f32(x) : x;
-          du = dl * to_f32<T>(su[clc * RS + t]);
-        }
-        Ps[t * PS + clc] = make_float2(dl, du);
+    // (b) per-element prologue for this warp's channels, two steps at a time.
+#pragma unroll
+    for (int tp = lane / CPW; tp < kChunk / 2; tp += 32 / CPW) {
+      const int t = 2 * tp;
+      const float2 dl_raw = load2<T>(sd + pcl * RS + t);
+      const float2 uu = load2<T>(su + pcl * RS + t);
+      float2 dl = __fadd2_rn(dl_raw, f2(p_bias, p_bias));
+      if (a.softplus) dl = softplus2(dl);
+      if (t0 + t >= L || !pch_ok) dl.x = 0.0f;
+      if (t0 + t + 1 >= L || !pch_ok) dl.y = 0.0f;
+      const float2 du = __fmul2_rn(dl, uu);
+      const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
+      float2 sg = f2(1.0f, 1.0f);
+      if (has_z) {
+        const float2 zz = load2<T>(sz + pcl * RS + t);
+        sg = f2(silu_f32(zz.x), silu_f32(zz.y));
       }
+      Ps[t * CPB + pcl] = make_float4(dl.x, dl.x, du.x, du.x);
+      Ps[(t + 1) * CPB + pcl] = make_float4(dl.y, dl.y, du.y, du.y);
+      *reinterpret_cast<float4*>(DS + pcl * DSS + t) = make_float4(Du.x, sg.x, Du.y, sg.y);
     }
     __syncthreads();
 
-    // (c) the recurrence, R steps per group; lane g finishes step g of each group.
+    // (c) the recurrence over windows of kWin steps, then the readout sums and the epilogue.
 #pragma unroll 1
-    for (int tt = 0; tt < kChunk; tt += R) {
-      float yp[R];
+    for (int w = 0; w < kChunk; w += kWin) {
+      float2 acc[kWin];
 #pragma unroll
-      for (int j = 0; j < R; ++j) {
-        const int t = tt + j;
-        const float2 p = Ps[t * PS + cl];
+      for (int j = 0; j < kWin; ++j) {
+        const int t = w + j;
+        const float4 p = Ps[t * CPB + cl];
         const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
         const float4 cc = *reinterpret_cast<const float4*>(Cs + t * NPAD + 4 * g);
-        const float a0 = ex2_approx(p.x * A2[0]);
-        const float a1 = ex2_approx(p.x * A2[1]);
-        const float a2 = ex2_approx(p.x * A2[2]);
-        const float a3 = ex2_approx(p.x * A2[3]);
-        h[0] = fmaf(a0, h[0], p.y * bb.x);
-        h[1] = fmaf(a1, h[1], p.y * bb.y);
-        h[2] = fmaf(a2, h[2], p.y * bb.z);
-        h[3] = fmaf(a3, h[3], p.y * bb.w);
-        yp[j] = fmaf(cc.w, h[3], fmaf(cc.z, h[2], fmaf(cc.y, h[1], cc.x * h[0])));
+        const float2 dd = f2(p.x, p.y), uu = f2(p.z, p.w);
+        const float2 g01 = __fmul2_rn(dd, A01), g23 = __fmul2_rn(dd, A23);
+        const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y));
+        const float2 a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
+        h01 = __ffma2_rn(a01, h01, __fmul2_rn(uu, f2(bb.x, bb.y)));
+        h23 = __ffma2_rn(a23, h23, __fmul2_rn(uu, f2(bb.z, bb.w)));
+        acc[j] = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
       }
-      float yv;
+      // sums over the R lanes of the channel and the pair halves; lane (cw, g) finishes the
+      // OPL steps w + g*OPL ... of channel cl
+      float yv[OPL];
       if constexpr (R == 1) {
-        yv = yp[0];
-      } else if constexpr (R == 2) {
-        const bool hi = g & 1;
-        const float send = hi ? yp[0] : yp[1];
-        yv = (hi ? yp[1] : yp[0]) + __shfl_xor_sync(0xffffffffu, send, 1);
+#pragma unroll
+        for (int j = 0; j < kWin; ++j) yv[j] = acc[j].x + acc[j].y;
       } else {
-        const bool hi2 = g & 2;
-        const float s0 = hi2 ? yp[0] : yp[2];
-        const float s1 = hi2 ? yp[1] : yp[3];
-        float k0 = hi2 ? yp[2] : yp[0];
-        float k1 = hi2 ? yp[3] : yp[1];
-        k0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-        k1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-        const bool hi1 = g & 1;
-        const float s = hi1 ? k0 : k1;
-        yv = (hi1 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, s, 1);
+        float4* rb = red + size_t(warp) * 32 * UPB;
+#pragma unroll
+        for (int i = 0; i < UPB; ++i)
+          rb[lane * UPB + red_rot<R>(cw, g, i)] = make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x,
+                                                               acc[2 * i + 1].y);
+        __syncwarp();
+#pragma unroll
+        for (int u = 0; u < OPL / 2; ++u) {
+          const int i = g * (OPL / 2) + u;
+          float4 sm = rb[(cw * R) * UPB + red_rot<R>(cw, 0, i)];
+#pragma unroll
+          for (int gg = 1; gg < R; ++gg) {
+            const float4 o = rb[(cw * R + gg) * UPB + red_rot<R>(cw, gg, i)];
+            const float2 lo = __fadd2_rn(f2(sm.x, sm.y), f2(o.x, o.y));
+            const float2 hi = __fadd2_rn(f2(sm.z, sm.w), f2(o.z, o.w));
+            sm = make_float4(lo.x, lo.y, hi.x, hi.y);
+          }
+          yv[2 * u] = sm.x + sm.y;
+          yv[2 * u + 1] = sm.z + sm.w;
+        }
+        __syncwarp();
       }
-      // epilogue for step tt + g of channel cl
-      const int t = tt + g;
-      float out = fmaf(Dd, to_f32<T>(su[cl * RS + t]), yv);
-      if (has_z) out *= silu_f32(to_f32<T>(sz[cl * RS + t]));
-      Ys[cl * RS + t] = from_f32<T>(out);
-    }
-    __syncthreads();
-
-    // (d) the chunk of y -> global.
-    if constexpr (VEC) {
-      for (int v = tid; v < CPB * VPR; v += kThreads) {
-        const int c = v / VPR, j = v % VPR;
-        const int t = t0 + j * EPV;
-        if (d0 + c < a.dim && t < L)
-          *reinterpret_cast<uint4*>(gy + (size_t(b) * a.dim + d0 + c) * L + t) =
-              *reinterpret_cast<const uint4*>(Ys + c * RS + j * EPV);
+      // epilogue: (y + D u) * silu(z) -> io type, straight to HBM
+      const int tb = w + g * OPL;  // first step (within the chunk) this lane finishes
+      float ov[OPL];
+#pragma unroll
+      for (int j = 0; j < OPL; j += 2) {
+        const float4 ds = *reinterpret_cast<const float4*>(DS + cl * DSS + tb + j);
+        const float2 o = __fmul2_rn(__fadd2_rn(f2(yv[j], yv[j + 1]), f2(ds.x, ds.z)), f2(ds.y, ds.w));
+        ov[j] = o.x, ov[j + 1] = o.y;
       }
-    } else {
-      for (int e = tid; e < CPB * kChunk; e += kThreads) {
-        const int c = e / kChunk, j = e % kChunk;
-        const int t = t0 + j;
-        if (d0 + c < a.dim && t < L) gy[(size_t(b) * a.dim + d0 + c) * L + t] = Ys[c * RS + j];
-      }
+      const int tg = t0 + tb;  // first global step
+      if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, L - tg);
     }
   }
   cp_async_wait<0>();
 
   if (a.last_state && ch_ok) {
+    const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int n = 4 * g + i;
-      if (n < N) a.last_state[(size_t(b) * a.dim + d) * N + n] = h[i];
+      if (n < N) a.last_state[(size_t(b) * a.dim + d) * N + n] = hv[i];
     }
   }
 }
@@ -294,14 +393,39 @@ bool rows_vectorisable(const ScanArgs& a) {
          al(a.y);
 }
 
+int sm_count() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  int v = cached[dev & 63].load(std::memory_order_relaxed);
+  if (v == 0) {
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    cached[dev & 63].store(v, std::memory_order_relaxed);
+  }
+  return v;
+}
+
 }  // namespace
 
-cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
+cudaError_t launch_scan_fwd_quad(const ScanArgs& a, bool vec, cudaStream_t stream) {
   if (a.io == kF32)
-    return rows_vectorisable<float>(a) ? dispatch_npad<float, true>(a, stream)
-                                       : dispatch_npad<float, false>(a, stream);
-  return rows_vectorisable<__nv_bfloat16>(a) ? dispatch_npad<__nv_bfloat16, true>(a, stream)
-                                             : dispatch_npad<__nv_bfloat16, false>(a, stream);
+    return vec ? dispatch_npad<float, true>(a, stream) : dispatch_npad<float, false>(a, stream);
+  return vec ? dispatch_npad<__nv_bfloat16, true>(a, stream) : dispatch_npad<__nv_bfloat16, false>(a, stream);
+}
+
+cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
+  const bool vec = a.io == kF32 ? rows_vectorisable<float>(a) : rows_vectorisable<__nv_bfloat16>(a);
+  const char* force = std::getenv("SSM_SCAN_VARIANT");
+  bool lane;
+  if (force && std::strcmp(force, "lane") == 0) {
+    lane = true;
+  } else if (force && std::strcmp(force, "quad") == 0) {
+    lane = false;
+  } else {
+    const long long warps = ((long long)a.batch * a.dim + 31) / 32;
+    lane = warps >= 2LL * sm_count();
+  }
+  return lane ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);
 }
 
 }  // namespace ssm

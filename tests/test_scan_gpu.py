@@ -11,6 +11,16 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 
 
+@pytest.fixture(params=["auto", "lane", "quad"])
+def variant(request, monkeypatch):
+    """Run a test with the library's choice of scan form, and with each form forced."""
+    if request.param != "auto":
+        monkeypatch.setenv("SSM_SCAN_VARIANT", request.param)
+    else:
+        monkeypatch.delenv("SSM_SCAN_VARIANT", raising=False)
+    return request.param
+
+
 def run(inp, softplus=True, h0=None):
     y, last = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp.get("D"), inp.get("z"),
                                inp.get("dt_bias"), delta_softplus=softplus, h0=h0)
@@ -28,13 +38,13 @@ def check_case(inp, softplus=True, h0=None, what=""):
 
 
 @pytest.mark.parametrize("w", [wl.TINY, wl.SMALL, wl.MID], ids=lambda w: w.name)
-def test_workload_full_parity(w):
+def test_workload_full_parity(w, variant):
     """Every output element of the tiny, small and mid-size workloads against the oracle."""
     inp = wl.scan_inputs(w, device=DEV)
     check_case(inp, what=w.name)
 
 
-def test_long_workload_sampled_channels():
+def test_long_workload_sampled_channels(variant):
     """The 65536-step workload at full size, in the launch configuration the benchmark times;
     the oracle recomputes 24 sampled channels (each channel is independent) end to end."""
     w = wl.LONG
@@ -68,7 +78,7 @@ EDGE = [
 
 
 @pytest.mark.parametrize("shape", EDGE, ids=lambda s: "b{}_d{}_n{}_l{}_{}".format(*s))
-def test_edge_shapes(shape):
+def test_edge_shapes(shape, variant):
     """Ragged lengths (scalar copy path), dim not a multiple of the CTA's 32 channels,
     dstate padded up to 4/8/16, single steps."""
     batch, dim, dstate, seqlen, io = shape
@@ -79,14 +89,14 @@ def test_edge_shapes(shape):
 @pytest.mark.parametrize("gate,use_D,use_bias,softplus", [
     (False, False, False, False), (True, False, True, True), (False, True, False, True), (True, True, True, False)])
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_optional_arguments(gate, use_D, use_bias, softplus, io):
+def test_optional_arguments(gate, use_D, use_bias, softplus, io, variant):
     inp = to_device(wl.random_scan_case(2, 48, 16, 136, io=io, seed=5, gate=gate, use_D=use_D, use_bias=use_bias,
                                         softplus=softplus), DEV)
     check_case(inp, softplus=softplus, what="optional args")
 
 
 @pytest.mark.parametrize("io", ["f32", "bf16"])
-def test_initial_state_and_resume(io):
+def test_initial_state_and_resume(io, variant):
     """h0 input, and scan(L1) then scan(L2) from last_state equals one scan over L1 + L2."""
     inp = to_device(wl.random_scan_case(2, 40, 16, 192, io=io, seed=3, h0=True), DEV)
     check_case(inp, h0=inp["h0"], what="h0")
@@ -130,7 +140,7 @@ def test_empty_sizes():
     assert y.shape == (0, 4, 10)
 
 
-def test_delta_zero_is_skip_only_on_gpu():
+def test_delta_zero_is_skip_only_on_gpu(variant):
     """Delta = 0 (no softplus, no bias): the state never moves and y = D u, i.e. the float32
     product rounded to bf16."""
     inp = to_device(wl.random_scan_case(2, 64, 16, 256, io="bf16", seed=4, gate=False, use_bias=False,
