@@ -83,7 +83,7 @@ int ssm_state_update(float* state, const void* x, const void* dt, const float* A
   const void* f_ptrs[] = {state, A, D, dt_bias};
   for (const void* p : f_ptrs)
     if (!aligned(p, 4)) return SSM_ERR_ALIGN;
-  if ((long long)batch * dim * 4 / 256 + 1 > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+  if ((long long)batch * dim / 128 + 1 > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
 
   ssm::UpdateArgs a{};
   a.state = state, a.x = x, a.dt = dt, a.A = A, a.B = B, a.C = C, a.D = D, a.z = z, a.dt_bias = dt_bias;

@@ -43,7 +43,7 @@ struct UpdateArgs {
 };
 
 // Enqueue the scan on `stream`.  Arguments are already validated.  Picks the lane-per-channel
-// form when there are enough channels to give every SM two or more of its warps, otherwise the
+// form when there are enough channels to give every SM eight or more of its warps, otherwise the
 // four-lanes-per-channel form; SSM_SCAN_VARIANT=lane|quad in the environment forces one.
 cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream);
 

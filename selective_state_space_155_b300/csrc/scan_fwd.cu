@@ -62,24 +62,21 @@ struct ScanCfg {
   static constexpr size_t kRawStage = size_t(ROWS) * RS * sizeof(T);
   static constexpr size_t kRaw = 2 * kRawStage;                              // [2][ROWS][RS] T
   static constexpr size_t kBC = size_t(2) * kChunk * NPAD * sizeof(float);   // Bs, Cs [CHUNK][NPAD]
-  static constexpr size_t kP = size_t(kChunk) * CPB * sizeof(float4);        // Ps [CHUNK][CPB]
+  static constexpr size_t kP = size_t(kChunk) * CPB * sizeof(float2);        // Ps [CHUNK][CPB] (Delta, Delta*u)
   static constexpr size_t kDS = size_t(CPB) * DSS * sizeof(float2);          // DS [CPB][DSS]
   static constexpr int OPL = kWin / R;                // outputs each lane finishes per window
-  static constexpr int UPB = kWin / 2;                // 16-byte units per lane block of readout partials
+  static constexpr int UPB = kWin / 4;                // 16-byte units per lane block of readout partials
   static constexpr size_t kRed = R > 1 ? size_t(NT) * UPB * 16 : 0;         // red [NT][UPB] float4
   static constexpr size_t kSmem = kRaw + kBC + kP + kDS + kRed;
 };
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 
-// Position of 16-byte unit i (readout partials of steps 2i, 2i+1) in the block of lane (cw, g).
-// For R = 4 the rotation by 2g + (cw & 1) makes both access patterns conflict-free: lane (cw, g)
-// storing unit i, and lane (cw, q) loading units 2q, 2q+1 of partner g's block.
-template <int R>
-__device__ __forceinline__ int red_rot(int cw, int g, int i) {
-  if constexpr (R == 4) return (i + 2 * g + (cw & 1)) & (kWin / 2 - 1);
-  return i;
-}
+// Position of 16-byte unit i (readout partials of steps 4i .. 4i+3) in the block of lane
+// (g, cw) = lane g*CPW + cw.  The rotation by cw/2 makes both access patterns conflict-free for
+// R = 4: a quarter-warp (fixed g) storing unit i, and a quarter-warp loading unit g of the
+// blocks of partner gp.
+__device__ __forceinline__ int red_rot(int cw, int i) { return (i + (cw >> 1)) & (kWin / 4 - 1); }
 
 // softplus of two values with packed arithmetic where it exists (see device_math.cuh for the method)
 __device__ __forceinline__ float2 softplus2(float2 x) {
@@ -148,7 +145,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
   T* raw = reinterpret_cast<T*>(smem);
   float* Bs = reinterpret_cast<float*>(smem + Cfg::kRaw);
   float* Cs = Bs + kChunk * NPAD;
-  float4* Ps = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kBC);
+  float2* Ps = reinterpret_cast<float2*>(smem + Cfg::kRaw + Cfg::kBC);
   float2* DS = reinterpret_cast<float2*>(smem + Cfg::kRaw + Cfg::kBC + Cfg::kP);
   float4* red = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kBC + Cfg::kP + Cfg::kDS);
 
@@ -157,7 +154,9 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
   const int b = blockIdx.x / nblk_d;
   const int d0 = (blockIdx.x % nblk_d) * CPB;
   const int warp = tid >> 5, lane = tid & 31;
-  const int cw = lane / R, g = lane % R;
+  // n-group major: the lanes of a quarter-warp (R = 4) share one n-group, so their B and C loads
+  // hit one address; the R lanes of channel cw are cw, cw + CPW, ...
+  const int cw = lane % CPW, g = lane / CPW;
   const int cl = warp * CPW + cw;  // this lane's channel within the CTA (recurrence mapping)
   const int d = d0 + cl;
   const bool ch_ok = d < a.dim;
@@ -277,8 +276,8 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
         const float2 zz = load2<T>(sz + pcl * RS + t);
         sg = f2(silu_f32(zz.x), silu_f32(zz.y));
       }
-      Ps[t * CPB + pcl] = make_float4(dl.x, dl.x, du.x, du.x);
-      Ps[(t + 1) * CPB + pcl] = make_float4(dl.y, dl.y, du.y, du.y);
+      Ps[t * CPB + pcl] = f2(dl.x, du.x);
+      Ps[(t + 1) * CPB + pcl] = f2(dl.y, du.y);
       *reinterpret_cast<float4*>(DS + pcl * DSS + t) = make_float4(Du.x, sg.x, Du.y, sg.y);
     }
     __syncthreads();
@@ -290,10 +289,10 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
 #pragma unroll
       for (int j = 0; j < kWin; ++j) {
         const int t = w + j;
-        const float4 p = Ps[t * CPB + cl];
+        const float2 p = Ps[t * CPB + cl];
         const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
         const float4 cc = *reinterpret_cast<const float4*>(Cs + t * NPAD + 4 * g);
-        const float2 dd = f2(p.x, p.y), uu = f2(p.z, p.w);
+        const float2 dd = f2(p.x, p.x), uu = f2(p.y, p.y);
         const float2 g01 = __fmul2_rn(dd, A01), g23 = __fmul2_rn(dd, A23);
         const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y));
         const float2 a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
@@ -308,25 +307,27 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
 #pragma unroll
         for (int j = 0; j < kWin; ++j) yv[j] = acc[j].x + acc[j].y;
       } else {
+        // this lane's partial for every step of the window, as 4 units of 4 steps
         float4* rb = red + size_t(warp) * 32 * UPB;
 #pragma unroll
         for (int i = 0; i < UPB; ++i)
-          rb[lane * UPB + red_rot<R>(cw, g, i)] = make_float4(acc[2 * i].x, acc[2 * i].y, acc[2 * i + 1].x,
-                                                               acc[2 * i + 1].y);
+          rb[lane * UPB + red_rot(cw, i)] = make_float4(acc[4 * i].x + acc[4 * i].y, acc[4 * i + 1].x + acc[4 * i + 1].y,
+                                                        acc[4 * i + 2].x + acc[4 * i + 2].y,
+                                                        acc[4 * i + 3].x + acc[4 * i + 3].y);
         __syncwarp();
+        // steps g*OPL .. g*OPL + OPL-1: units g*OPL/4 .. of every partner lane gp*CPW + cw
 #pragma unroll
-        for (int u = 0; u < OPL / 2; ++u) {
-          const int i = g * (OPL / 2) + u;
-          float4 sm = rb[(cw * R) * UPB + red_rot<R>(cw, 0, i)];
+        for (int u = 0; u < OPL / 4; ++u) {
+          const int i = g * (OPL / 4) + u;
+          float4 sm = rb[cw * UPB + red_rot(cw, i)];
 #pragma unroll
-          for (int gg = 1; gg < R; ++gg) {
-            const float4 o = rb[(cw * R + gg) * UPB + red_rot<R>(cw, gg, i)];
+          for (int gp = 1; gp < R; ++gp) {
+            const float4 o = rb[(gp * CPW + cw) * UPB + red_rot(cw, i)];
             const float2 lo = __fadd2_rn(f2(sm.x, sm.y), f2(o.x, o.y));
             const float2 hi = __fadd2_rn(f2(sm.z, sm.w), f2(o.z, o.w));
             sm = make_float4(lo.x, lo.y, hi.x, hi.y);
           }
-          yv[2 * u] = sm.x + sm.y;
-          yv[2 * u + 1] = sm.z + sm.w;
+          yv[4 * u] = sm.x, yv[4 * u + 1] = sm.y, yv[4 * u + 2] = sm.z, yv[4 * u + 3] = sm.w;
         }
         __syncwarp();
       }
@@ -422,8 +423,10 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
   } else if (force && std::strcmp(force, "quad") == 0) {
     lane = false;
   } else {
+    // the lane form has no cross-lane work but only one warp per 32 channels; it needs about two
+    // warps per scheduler (8 per SM) to hide its latencies
     const long long warps = ((long long)a.batch * a.dim + 31) / 32;
-    lane = warps >= 2LL * sm_count();
+    lane = warps >= 8LL * sm_count();
   }
   return lane ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);
 }

@@ -5,15 +5,17 @@
 //   y = sum_n C[n] s[n] + D[d] x;  out = y * silu(z)
 // (constant-memory inference from the previous state and the current input only).
 //
-// The step is bound by HBM: the state is read and written once (8 bytes per state element),
-// everything else is small.  A channel's dstate floats are contiguous, so lanes take four states
-// each along the state row (a warp moves 32 x 16 contiguous bytes per access) and the readout sum
-// over n is a butterfly over the R = NPAD/4 lanes of a channel.  Each thread handles two such
-// units, issuing all of their loads before any arithmetic, so that enough bytes are in flight to
-// cover HBM latency at full bandwidth.
+// The step is bound by HBM: the float32 state is read and written once (8 bytes per state
+// element), everything else is small.  One thread owns one (batch, channel) and all NPAD of its
+// states, so the per-channel work (softplus, silu, the readout sum) is done once, with no
+// cross-lane traffic, and each thread keeps NPAD*4 bytes of state in flight (four 16-byte loads
+// issued back to back for dstate 16).  A, B and C rows are small and shared (A by every batch row,
+// B and C by every channel of a batch row), so they come from L1/L2.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <type_traits>
 
 #include "device_math.cuh"
 #include "internal.h"
@@ -21,125 +23,116 @@
 namespace ssm {
 namespace {
 
-constexpr int kBlock = 256;
-constexpr int kItems = 2;
+constexpr int kBlock = 128;
 
-template <typename T>
-__device__ __forceinline__ void load4(const T* p, float (&v)[4]);
-template <>
-__device__ __forceinline__ void load4<float>(const float* p, float (&v)[4]) {
-  const float4 q = __ldg(reinterpret_cast<const float4*>(p));
-  v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
-}
-template <>
-__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[4]) {
-  const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
-  const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
-  const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
-  v[0] = lo.x, v[1] = lo.y, v[2] = hi.x, v[3] = hi.y;
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+
+// NPAD consecutive io values (16-byte aligned) as float32
+template <typename T, int NPAD>
+__device__ __forceinline__ void load_row(const T* p, float (&v)[NPAD]) {
+  if constexpr (std::is_same<T, float>::value) {
+#pragma unroll
+    for (int i = 0; i < NPAD; i += 4) {
+      const float4 q = __ldg(reinterpret_cast<const float4*>(p + i));
+      v[i] = q.x, v[i + 1] = q.y, v[i + 2] = q.z, v[i + 3] = q.w;
+    }
+  } else if constexpr (NPAD >= 8) {
+#pragma unroll
+    for (int i = 0; i < NPAD; i += 8) {
+      const uint4 q = __ldg(reinterpret_cast<const uint4*>(p + i));
+      const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+        v[i + 2 * k] = f.x, v[i + 2 * k + 1] = f.y;
+      }
+    }
+  } else {
+    const uint2 q = __ldg(reinterpret_cast<const uint2*>(p));
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+    v[0] = lo.x, v[1] = lo.y, v[2] = hi.x, v[3] = hi.y;
+  }
 }
 
 template <typename T, int NPAD, bool VEC>
 __global__ void __launch_bounds__(kBlock) state_update_kernel(const UpdateArgs a) {
-  constexpr int R = NPAD / 4;
-  const long long nch = (long long)a.batch * a.dim;
-  const long long lanes = nch * R;
-  const long long stride = (long long)gridDim.x * kBlock;  // a multiple of 32: a channel's R lanes share a warp
+  const long long ch = (long long)blockIdx.x * kBlock + threadIdx.x;
+  if (ch >= (long long)a.batch * a.dim) return;
+  const int b = int(ch / a.dim), d = int(ch % a.dim);
   const int N = a.dstate;
-  const T* __restrict__ gx = static_cast<const T*>(a.x);
-  const T* __restrict__ gdt = static_cast<const T*>(a.dt);
-  const T* __restrict__ gz = static_cast<const T*>(a.z);
-  const T* __restrict__ gB = static_cast<const T*>(a.B);
-  const T* __restrict__ gC = static_cast<const T*>(a.C);
+  float* srow = a.state + ch * N;
+  const float* Arow = a.A + size_t(d) * N;
+  const T* Brow = static_cast<const T*>(a.B) + size_t(b) * N;
+  const T* Crow = static_cast<const T*>(a.C) + size_t(b) * N;
 
-  float s[kItems][4], Av[kItems][4], Bv[kItems][4], Cv[kItems][4], x[kItems], r[kItems], zz[kItems];
-  bool ok[kItems];
-  long long chs[kItems];
-  int gs[kItems], ds[kItems];
-
-  // all loads first
+  // loads first: the state (the HBM stream), then the small operands
+  float s[NPAD], Av[NPAD], Bv[NPAD], Cv[NPAD];
+  if constexpr (VEC) {
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const long long unit = (long long)blockIdx.x * kBlock + threadIdx.x + it * stride;
-    ok[it] = unit < lanes;
-    const long long ch = ok[it] ? unit / R : 0;
-    const int g = int(unit % R);
-    const int b = int(ch / a.dim), d = int(ch % a.dim);
-    chs[it] = ch, gs[it] = g, ds[it] = d;
-    float* srow = a.state + ch * N + 4 * g;
+    for (int i = 0; i < NPAD; i += 4) {
+      const float4 q = *reinterpret_cast<const float4*>(srow + i);
+      s[i] = q.x, s[i + 1] = q.y, s[i + 2] = q.z, s[i + 3] = q.w;
+    }
+    load_row<float, NPAD>(Arow, Av);
+    load_row<T, NPAD>(Brow, Bv);
+    load_row<T, NPAD>(Crow, Cv);
+  } else {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) s[it][i] = Av[it][i] = Bv[it][i] = Cv[it][i] = 0.0f;
-    x[it] = r[it] = 0.0f;
-    zz[it] = 0.0f;
-    if (ok[it]) {
-      if constexpr (VEC) {
-        const float4 v = *reinterpret_cast<const float4*>(srow);
-        s[it][0] = v.x, s[it][1] = v.y, s[it][2] = v.z, s[it][3] = v.w;
-        const float4 q = __ldg(reinterpret_cast<const float4*>(a.A + size_t(d) * N + 4 * g));
-        Av[it][0] = q.x, Av[it][1] = q.y, Av[it][2] = q.z, Av[it][3] = q.w;
-        load4<T>(gB + size_t(b) * N + 4 * g, Bv[it]);
-        load4<T>(gC + size_t(b) * N + 4 * g, Cv[it]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int n = 4 * g + i;
-          if (n < N) {
-            s[it][i] = srow[i];
-            Av[it][i] = __ldg(a.A + size_t(d) * N + n);
-            Bv[it][i] = to_f32<T>(gB[size_t(b) * N + n]);
-            Cv[it][i] = to_f32<T>(gC[size_t(b) * N + n]);
-          }
-        }
-      }
-      x[it] = to_f32<T>(gx[ch]);
-      r[it] = to_f32<T>(gdt[ch]);
-      if (a.dt_bias) r[it] += __ldg(a.dt_bias + d);
-      if (gz) zz[it] = to_f32<T>(gz[ch]);
+    for (int i = 0; i < NPAD; ++i) {
+      const bool ok = i < N;
+      s[i] = ok ? srow[i] : 0.0f;
+      Av[i] = ok ? __ldg(Arow + i) : 0.0f;
+      Bv[i] = ok ? to_f32<T>(Brow[i]) : 0.0f;
+      Cv[i] = ok ? to_f32<T>(Crow[i]) : 0.0f;
     }
   }
+  const float x = to_f32<T>(static_cast<const T*>(a.x)[ch]);
+  float r = to_f32<T>(static_cast<const T*>(a.dt)[ch]);
+  if (a.dt_bias) r += __ldg(a.dt_bias + d);
+  const float zz = a.z ? to_f32<T>(static_cast<const T*>(a.z)[ch]) : 0.0f;
+  const float Dd = a.D ? __ldg(a.D + d) : 0.0f;
 
+  const float step = a.softplus ? softplus_f32(r) : r;
+  const float2 dd = f2(step * kLog2e, step * kLog2e), dx = f2(step * x, step * x);
+  float2 acc = f2(0.0f, 0.0f);
 #pragma unroll
-  for (int it = 0; it < kItems; ++it) {
-    const float step = a.softplus ? softplus_f32(r[it]) : r[it];
-    const float dx = step * x[it];
-    float part = 0.0f;
+  for (int i = 0; i < NPAD; i += 2) {
+    const float2 g = __fmul2_rn(dd, f2(Av[i], Av[i + 1]));
+    const float2 ab = f2(ex2_approx(g.x), ex2_approx(g.y));
+    const float2 sn = __ffma2_rn(ab, f2(s[i], s[i + 1]), __fmul2_rn(dx, f2(Bv[i], Bv[i + 1])));
+    s[i] = sn.x, s[i + 1] = sn.y;
+    acc = __ffma2_rn(f2(Cv[i], Cv[i + 1]), sn, acc);
+  }
+  float y = fmaf(Dd, x, acc.x + acc.y);
+  if (a.z) y *= silu_f32(zz);
+  static_cast<T*>(a.out)[ch] = from_f32<T>(y);
+
+  if constexpr (VEC) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float abar = ex2_approx(step * (Av[it][i] * kLog2e));
-      s[it][i] = fmaf(abar, s[it][i], dx * Bv[it][i]);
-      part = fmaf(Cv[it][i], s[it][i], part);
-    }
+    for (int i = 0; i < NPAD; i += 4)
+      *reinterpret_cast<float4*>(srow + i) = make_float4(s[i], s[i + 1], s[i + 2], s[i + 3]);
+  } else {
 #pragma unroll
-    for (int off = R / 2; off >= 1; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-    if (ok[it]) {
-      float* srow = a.state + chs[it] * N + 4 * gs[it];
-      if constexpr (VEC) {
-        *reinterpret_cast<float4*>(srow) = make_float4(s[it][0], s[it][1], s[it][2], s[it][3]);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          if (4 * gs[it] + i < N) srow[i] = s[it][i];
-      }
-      if (gs[it] == 0) {
-        float y = part;
-        if (a.D) y = fmaf(__ldg(a.D + ds[it]), x[it], y);
-        if (gz) y *= silu_f32(zz[it]);
-        static_cast<T*>(a.out)[chs[it]] = from_f32<T>(y);
-      }
-    }
+    for (int i = 0; i < NPAD; ++i)
+      if (i < N) srow[i] = s[i];
   }
 }
 
 template <typename T, int NPAD>
 cudaError_t launch_npad(const UpdateArgs& a, cudaStream_t stream) {
-  constexpr int R = NPAD / 4;
-  const long long lanes = (long long)a.batch * a.dim * R;
-  const long long nblk = (lanes + kBlock * kItems - 1) / (kBlock * kItems);
+  const long long nch = (long long)a.batch * a.dim;
+  const long long nblk = (nch + kBlock - 1) / kBlock;
   if (nblk <= 0) return cudaSuccess;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  auto al = [](const void* p, uintptr_t m) { return (reinterpret_cast<uintptr_t>(p) & (m - 1)) == 0; };
-  const uintptr_t bc_align = a.io == kF32 ? 16 : 8;
-  const bool vec = a.dstate == NPAD && al(a.state, 16) && al(a.A, 16) && al(a.B, bc_align) && al(a.C, bc_align);
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  // vector rows: every row starts 16-byte aligned (dstate == NPAD) and the bf16 B/C rows are whole
+  // 16-byte (NPAD >= 8) or 8-byte (NPAD == 4) pieces
+  const bool bc_ok = a.io == kF32 ? (al(a.B) && al(a.C))
+                                  : (NPAD >= 8 ? (al(a.B) && al(a.C))
+                                               : ((reinterpret_cast<uintptr_t>(a.B) & 7u) == 0 &&
+                                                  (reinterpret_cast<uintptr_t>(a.C) & 7u) == 0));
+  const bool vec = a.dstate == NPAD && al(a.state) && al(a.A) && bc_ok;
   UpdateArgs args = a;
   void* params[] = {&args};
   const void* fn = vec ? reinterpret_cast<const void*>(state_update_kernel<T, NPAD, true>)
