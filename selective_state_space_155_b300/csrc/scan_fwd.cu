@@ -1,31 +1,26 @@
-// Selective scan forward for sm_103a.
+// Selective scan forward for sm_103a: warp-specialised, four lanes per channel.
 //
 // What it computes (per batch row b, channel d, state n; sources cited in ssm_scan.h):
 //   Delta_t = softplus(delta_t + dt_bias[d]);  Abar = exp(Delta_t A[d,n]);  h_t = Abar h_{t-1} + Delta_t B_t[n] u_t
 //   y_t = sum_n C_t[n] h_t[n] + D[d] u_t;  out_t = y_t * silu(z_t);  last_state = h_{L-1}
 //
-// Why it looks like this (B300: 148 SMs; per SM and clock 32 MUFU ex2, 128 FP32 FMA lanes, and
-// packed f32x2 FMA at the same lane rate but half the issue slots).  The scan is not a
-// contraction, so it runs on the SIMT pipes, and it is bound by issue slots, the MUFU pipe
-// (16 exps per element) and the FMA pipe (4 flops per state) well before HBM.  Every design
-// choice below removes instructions per element:
-//  * A CTA owns 32 channels of one batch row and walks L in chunks of 32 steps.  Chunk k+1 is
-//    fetched with 16-byte cp.async (zero-filled past the sequence end) while chunk k is
-//    computed, so HBM sees u, delta, z, B, C once and y once; the expanded (L, D, N) tensors
-//    never exist outside registers.
-//  * Four states per lane, R = NPAD/4 lanes per channel; the float32 state stays in registers
-//    for the whole sequence and is the carried prefix from chunk to chunk.
-//  * Per chunk, a prologue does all per-element work once, two steps at a time with packed
-//    math: softplus, Delta*u, D*u and silu(z).  The recurrence then reads (Delta, Delta, Du,
-//    Du) as one 16-byte shared load per step, already in the register pairs the packed
-//    instructions take.
-//  * The recurrence runs on float2 pairs of states (mul/fma.f32x2) over a window of 16 steps,
-//    fully unrolled, keeping the 16 readout partials C.h (one float2 pair per step) in registers:
-//    the exps of later steps do not depend on the state, so they overlap the state's FMA chain.
-//  * Then the sum over the R lanes of a channel and over the pair halves for all 16 steps at once
-//    goes through shared memory (a rotated layout that is conflict-free for both the 16-byte
-//    stores and the loads), after which lane (c, q) owns 16/R consecutive steps of channel c:
-//    (y + D u) * silu(z), rounded to the io type, leaves as one vector store to HBM.
+// Why it looks like this.  On B300 the scan is not HBM-bound in practice: per element it needs 16
+// MUFU ex2, ~64 FP32 lane-operations and a cross-lane readout, and a straightforward kernel spends
+// its time in a chain of latency-bound phases (wait for the chunk, convert, per-element prologue,
+// barrier, recurrence, readout reduction, epilogue) that one set of warps walks in turn.  This
+// kernel gives the phases to different warps so that they overlap:
+//  * PREP warps (4) own the HBM traffic and all per-element work.  They stream chunks of 32 steps
+//    of u, delta, z, B, C with 16-byte cp.async into a two-stage raw ring (zero-filled past the
+//    sequence end), convert B and C into float32 [t][n] tables, and compute, once per element,
+//    Delta = softplus(delta + dt_bias), Delta*u, D*u and silu(z) into a two-stage table ring.
+//  * RECURRENCE warps (R = NPAD/4) each own 32/R channels, four states per lane (lanes of a
+//    quarter-warp share one n-group, so their B/C loads hit one address).  The float32 state lives
+//    in registers for the whole sequence.  Per 16-step window the recurrence runs on float2 pairs
+//    (mul/fma.f32x2) keeping the readout partials C.h in registers; the sum over the R lanes of a
+//    channel goes through a rotated, conflict-free shared-memory layout; lane (g, c) then finishes
+//    16/R consecutive steps of channel c, (y + D u) * silu(z), stored straight to HBM.
+//  * Hand-off is by named barriers (bar.arrive / bar.sync; no spin loops): table stage s is FULL
+//    once the prep warps arrive on it and EMPTY once the recurrence warps are done with it.
 //  * Padded states (n >= dstate) have A = 0 and B = C = 0; padded steps (t >= seqlen) have
 //    Delta = 0.  Both leave the state unchanged, so one code path serves every size.
 #include <cuda_bf16.h>
@@ -45,32 +40,46 @@ namespace {
 
 constexpr int kChunk = 32;  // steps per chunk
 constexpr int kWin = 16;    // steps per recurrence window (readout partials held in registers)
+constexpr int kPrepWarps = 4;
+
+// named barrier ids (0 is __syncthreads)
+constexpr int kBarFull0 = 1, kBarEmpty0 = 3, kBarPrep = 5;
 
 template <typename T, int NPAD>
 struct ScanCfg {
   static constexpr int R = NPAD / 4;                  // lanes per channel
-  static constexpr int WARPS = R;                     // every CTA holds 32 channels
-  static constexpr int NT = 32 * WARPS;               // threads per CTA
-  static constexpr int CPW = 32 / R;                  // channels per warp
-  static constexpr int CPB = CPW * WARPS;             // channels per CTA (32)
+  static constexpr int CWARPS = R;                    // recurrence warps: 32 channels per CTA
+  static constexpr int NT = 32 * (CWARPS + kPrepWarps);
+  static constexpr int PT = 32 * kPrepWarps;          // prep threads
+  static constexpr int CPW = 32 / R;                  // channels per recurrence warp
+  static constexpr int CPB = CPW * CWARPS;            // channels per CTA (32)
   static constexpr int EPV = 16 / sizeof(T);          // elements per 16-byte vector
   static constexpr int RS = kChunk + EPV;             // padded row stride (elements) of staged rows
   static constexpr int VPR = kChunk / EPV;            // 16-byte vectors per staged row
   static constexpr int ROWS = 3 * CPB + 2 * NPAD;     // u, delta, z rows, then B rows, then C rows
-  static constexpr int DSS = kChunk + 2;              // row stride (float2) of the (Du, silu z) table: an odd
-                                                      // number of 16-byte units keeps its stores conflict-free
-  static constexpr size_t kRawStage = size_t(ROWS) * RS * sizeof(T);
-  static constexpr size_t kRaw = 2 * kRawStage;                              // [2][ROWS][RS] T
-  static constexpr size_t kBC = size_t(2) * kChunk * NPAD * sizeof(float);   // Bs, Cs [CHUNK][NPAD]
-  static constexpr size_t kP = size_t(kChunk) * CPB * sizeof(float2);        // Ps [CHUNK][CPB] (Delta, Delta*u)
-  static constexpr size_t kDS = size_t(CPB) * DSS * sizeof(float2);          // DS [CPB][DSS]
+  static constexpr int PSS = CPB + 4;                 // row stride (float2) of the (Delta, Delta*u) table
+  static constexpr int DSS = kChunk + 2;              // row stride (float2) of the (D*u, silu z) table
   static constexpr int OPL = kWin / R;                // outputs each lane finishes per window
   static constexpr int UPB = kWin / 4;                // 16-byte units per lane block of readout partials
-  static constexpr size_t kRed = R > 1 ? size_t(NT) * UPB * 16 : 0;         // red [NT][UPB] float4
-  static constexpr size_t kSmem = kRaw + kBC + kP + kDS + kRed;
+  // shared memory map (bytes)
+  static constexpr size_t kRawStage = size_t(ROWS) * RS * sizeof(T);
+  static constexpr size_t kBCStage = size_t(2) * kChunk * NPAD * sizeof(float);  // Bs, Cs [CHUNK][NPAD]
+  static constexpr size_t kPStage = size_t(kChunk) * PSS * sizeof(float2);      // Ps [CHUNK][PSS]
+  static constexpr size_t kDSStage = size_t(CPB) * DSS * sizeof(float2);        // DS [CPB][DSS]
+  static constexpr size_t kTabStage = kBCStage + kPStage + kDSStage;
+  static constexpr size_t kRaw = 2 * kRawStage;
+  static constexpr size_t kTab = 2 * kTabStage;
+  static constexpr size_t kRed = R > 1 ? size_t(32 * CWARPS) * UPB * 16 : 0;    // red [lanes][UPB] float4
+  static constexpr size_t kSmem = kRaw + kTab + kRed;
+  static_assert(kRawStage % 16 == 0 && kBCStage % 16 == 0 && kPStage % 16 == 0 && kDSStage % 16 == 0, "align");
 };
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+
+__device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
+__device__ __forceinline__ void bar_arrive(int id, int n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
 
 // Position of 16-byte unit i (readout partials of steps 4i .. 4i+3) in the block of lane
 // (g, cw) = lane g*CPW + cw.  The rotation by cw/2 makes both access patterns conflict-free for
@@ -136,41 +145,165 @@ __device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) 
 }
 
 template <typename T, int NPAD, bool VEC>
-__global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const ScanArgs a) {
+__global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const ScanArgs a) {
   using Cfg = ScanCfg<T, NPAD>;
   constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, RS = Cfg::RS, VPR = Cfg::VPR;
-  constexpr int NT = Cfg::NT, ROWS = Cfg::ROWS, DSS = Cfg::DSS, OPL = Cfg::OPL, UPB = Cfg::UPB;
+  constexpr int NT = Cfg::NT, PT = Cfg::PT, ROWS = Cfg::ROWS, PSS = Cfg::PSS, DSS = Cfg::DSS, OPL = Cfg::OPL;
+  constexpr int UPB = Cfg::UPB, CWARPS = Cfg::CWARPS;
 
   extern __shared__ __align__(16) unsigned char smem[];
   T* raw = reinterpret_cast<T*>(smem);
-  float* Bs = reinterpret_cast<float*>(smem + Cfg::kRaw);
-  float* Cs = Bs + kChunk * NPAD;
-  float2* Ps = reinterpret_cast<float2*>(smem + Cfg::kRaw + Cfg::kBC);
-  float2* DS = reinterpret_cast<float2*>(smem + Cfg::kRaw + Cfg::kBC + Cfg::kP);
-  float4* red = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kBC + Cfg::kP + Cfg::kDS);
+  unsigned char* tab = smem + Cfg::kRaw;
+  float4* red = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kTab);
+  auto tabBs = [&](int s) { return reinterpret_cast<float*>(tab + s * Cfg::kTabStage); };
+  auto tabCs = [&](int s) { return reinterpret_cast<float*>(tab + s * Cfg::kTabStage) + kChunk * NPAD; };
+  auto tabPs = [&](int s) { return reinterpret_cast<float2*>(tab + s * Cfg::kTabStage + Cfg::kBCStage); };
+  auto tabDS = [&](int s) {
+    return reinterpret_cast<float2*>(tab + s * Cfg::kTabStage + Cfg::kBCStage + Cfg::kPStage);
+  };
 
   const int tid = threadIdx.x;
   const int nblk_d = (a.dim + CPB - 1) / CPB;
   const int b = blockIdx.x / nblk_d;
   const int d0 = (blockIdx.x % nblk_d) * CPB;
   const int warp = tid >> 5, lane = tid & 31;
+  const int L = a.seqlen, N = a.dstate;
+  const bool has_z = a.z != nullptr;
+  const int nchunks = (L + kChunk - 1) / kChunk;
+
+  if (warp >= CWARPS) {
+    // ================================ prep warps ================================
+    const int ptid = tid - 32 * CWARPS;
+    const int pw = warp - CWARPS;
+    const T* __restrict__ gu = static_cast<const T*>(a.u);
+    const T* __restrict__ gd = static_cast<const T*>(a.delta);
+    const T* __restrict__ gz = static_cast<const T*>(a.z);
+    const T* __restrict__ gB = static_cast<const T*>(a.B);
+    const T* __restrict__ gC = static_cast<const T*>(a.C);
+
+    auto row_src = [&](int r, bool& ok) -> const T* {
+      if (r < 3 * CPB) {
+        const int which = r / CPB, c = r % CPB;
+        const T* base = which == 0 ? gu : (which == 1 ? gd : gz);
+        ok = (d0 + c < a.dim) && (which < 2 || has_z);
+        return base + (size_t(b) * a.dim + (d0 + c)) * L;
+      }
+      const int rr = r - 3 * CPB;
+      const int which = rr / NPAD, n = rr % NPAD;
+      ok = n < N;
+      return (which == 0 ? gB : gC) + (size_t(b) * N + n) * L;
+    };
+    auto stage_load = [&](int stage, int t0) {
+      T* dst = raw + size_t(stage) * ROWS * RS;
+      if constexpr (VEC) {
+        for (int v = ptid; v < ROWS * VPR; v += PT) {
+          const int r = v / VPR, j = v % VPR;
+          if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;  // z rows are never read without a gate
+          bool ok;
+          const T* src = row_src(r, ok);
+          const int t = t0 + j * EPV;
+          int bytes = ok ? min(EPV, L - t) * int(sizeof(T)) : 0;
+          bytes = max(bytes, 0);
+          // a zero-byte copy only zero-fills, but its source must still be a valid aligned address
+          cp_async_16(dst + r * RS + j * EPV, bytes > 0 ? static_cast<const void*>(src + t) : gu, bytes);
+        }
+      } else {
+        for (int e = ptid; e < ROWS * kChunk; e += PT) {
+          const int r = e / kChunk, j = e % kChunk;
+          if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;
+          bool ok;
+          const T* src = row_src(r, ok);
+          const int t = t0 + j;
+          dst[r * RS + j] = (ok && t < L) ? src[t] : from_f32<T>(0.0f);
+        }
+      }
+    };
+
+    // prologue mapping: prep warp pw handles channels PCW*pw + (lane % PCW); the lanes lane/PCW +
+    // PPL*i walk the step pairs of the chunk (conflict-free reads of the staged rows)
+    constexpr int PCW = CPB / kPrepWarps;  // channels per prep warp (8)
+    constexpr int PPL = 32 / PCW;          // step-pair lanes per channel (4)
+    const int pcl = pw * PCW + (lane % PCW);
+    const bool pch_ok = d0 + pcl < a.dim;
+    const float p_bias = (pch_ok && a.dt_bias) ? a.dt_bias[d0 + pcl] : 0.0f;
+    const float p_D = (pch_ok && a.D) ? a.D[d0 + pcl] : 0.0f;
+
+    if (nchunks > 0) stage_load(0, 0);
+    cp_async_commit();
+    if (nchunks > 1) stage_load(1, kChunk);
+    cp_async_commit();
+
+    for (int k = 0; k < nchunks; ++k) {
+      const int s = k & 1;
+      const int t0 = k * kChunk;
+      cp_async_wait<1>();           // this thread's copies of chunk k have landed
+      bar_sync(kBarPrep, PT);       // ... and every prep thread's
+      if (k >= 2) bar_sync(kBarEmpty0 + s, NT);  // the recurrence warps are done with table stage s
+
+      const T* st = raw + size_t(s) * ROWS * RS;
+      const T* su = st;
+      const T* sd = st + CPB * RS;
+      const T* sz = st + 2 * CPB * RS;
+      const T* sB = st + 3 * CPB * RS;
+      const T* sC = sB + NPAD * RS;
+      float* Bs = tabBs(s);
+      float* Cs = tabCs(s);
+      float2* Ps = tabPs(s);
+      float2* DS = tabDS(s);
+
+      // B, C rows -> float32 [t][n] tables, two steps per item
+      for (int e = ptid; e < NPAD * kChunk; e += PT) {  // 2 tables x NPAD rows x CHUNK/2 step pairs
+        const int which = e / (NPAD * kChunk / 2), rem = e % (NPAD * kChunk / 2);
+        const int tp = rem / NPAD, n = rem % NPAD;
+        const float2 v = load2<T>((which == 0 ? sB : sC) + n * RS + 2 * tp);
+        float* dst = which == 0 ? Bs : Cs;
+        dst[(2 * tp) * NPAD + n] = v.x;
+        dst[(2 * tp + 1) * NPAD + n] = v.y;
+      }
+      // per-element work: Delta, Delta*u, D*u, silu(z), two steps per item
+      const bool full = t0 + kChunk <= L;
+#pragma unroll
+      for (int i = 0; i < kChunk / 2 / PPL; ++i) {
+        const int tp = lane / PCW + i * PPL;
+        const int t = 2 * tp;
+        const float2 dl_raw = load2<T>(sd + pcl * RS + t);
+        const float2 uu = load2<T>(su + pcl * RS + t);
+        float2 dl = __fadd2_rn(dl_raw, f2(p_bias, p_bias));
+        if (a.softplus) dl = softplus2(dl);
+        if (!full || !pch_ok) {
+          if (t0 + t >= L || !pch_ok) dl.x = 0.0f;
+          if (t0 + t + 1 >= L || !pch_ok) dl.y = 0.0f;
+        }
+        const float2 du = __fmul2_rn(dl, uu);
+        const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
+        float2 sg = f2(1.0f, 1.0f);
+        if (has_z) {
+          const float2 zz = load2<T>(sz + pcl * RS + t);
+          sg = f2(silu_f32(zz.x), silu_f32(zz.y));
+        }
+        Ps[t * PSS + pcl] = f2(dl.x, du.x);
+        Ps[(t + 1) * PSS + pcl] = f2(dl.y, du.y);
+        *reinterpret_cast<float4*>(DS + pcl * DSS + t) = make_float4(Du.x, sg.x, Du.y, sg.y);
+      }
+      bar_sync(kBarPrep, PT);            // every prep thread is done reading raw stage s
+      bar_arrive(kBarFull0 + s, NT);     // table stage s is ready
+      if (k + 2 < nchunks) stage_load(s, t0 + 2 * kChunk);
+      cp_async_commit();
+    }
+    cp_async_wait<0>();
+    // match the recurrence warps' last arrivals so that no barrier is left half-arrived
+    for (int k = max(0, nchunks - 2); k < nchunks; ++k) bar_sync(kBarEmpty0 + (k & 1), NT);
+    return;
+  }
+
+  // ============================== recurrence warps ==============================
   // n-group major: the lanes of a quarter-warp (R = 4) share one n-group, so their B and C loads
   // hit one address; the R lanes of channel cw are cw, cw + CPW, ...
   const int cw = lane % CPW, g = lane / CPW;
-  const int cl = warp * CPW + cw;  // this lane's channel within the CTA (recurrence mapping)
+  const int cl = warp * CPW + cw;  // this lane's channel within the CTA
   const int d = d0 + cl;
   const bool ch_ok = d < a.dim;
-  const int L = a.seqlen, N = a.dstate;
-  const bool has_z = a.z != nullptr;
 
-  const T* __restrict__ gu = static_cast<const T*>(a.u);
-  const T* __restrict__ gd = static_cast<const T*>(a.delta);
-  const T* __restrict__ gz = static_cast<const T*>(a.z);
-  const T* __restrict__ gB = static_cast<const T*>(a.B);
-  const T* __restrict__ gC = static_cast<const T*>(a.C);
-  T* __restrict__ gy = static_cast<T*>(a.y);
-
-  // Recurrence lane: states n = 4g .. 4g+3 of channel d, as two float2 pairs.
   float2 A01, A23, h01, h23;
   {
     float Av[4], hv[4];
@@ -184,112 +317,24 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
     A01 = f2(Av[0], Av[1]), A23 = f2(Av[2], Av[3]);
     h01 = f2(hv[0], hv[1]), h23 = f2(hv[2], hv[3]);
   }
-
-  // Prologue lane: channel pc of this warp (fixed, since 32 is a multiple of CPW), step pairs tp.
-  const int pc = lane % CPW;
-  const int pcl = warp * CPW + pc;
-  const bool pch_ok = d0 + pcl < a.dim;
-  const float p_bias = (pch_ok && a.dt_bias) ? a.dt_bias[d0 + pcl] : 0.0f;
-  const float p_D = (pch_ok && a.D) ? a.D[d0 + pcl] : 0.0f;
-
-  auto row_src = [&](int r, bool& ok) -> const T* {
-    if (r < 3 * CPB) {
-      const int which = r / CPB, c = r % CPB;
-      const T* base = which == 0 ? gu : (which == 1 ? gd : gz);
-      ok = (d0 + c < a.dim) && (which < 2 || has_z);
-      return base + (size_t(b) * a.dim + (d0 + c)) * L;
-    }
-    const int rr = r - 3 * CPB;
-    const int which = rr / NPAD, n = rr % NPAD;
-    ok = n < N;
-    return (which == 0 ? gB : gC) + (size_t(b) * N + n) * L;
-  };
-
-  auto stage_load = [&](int stage, int t0) {
-    T* dst = raw + size_t(stage) * ROWS * RS;
-    if constexpr (VEC) {
-      for (int v = tid; v < ROWS * VPR; v += NT) {
-        const int r = v / VPR, j = v % VPR;
-        if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;  // z rows are never read without a gate
-        bool ok;
-        const T* src = row_src(r, ok);
-        const int t = t0 + j * EPV;
-        int bytes = ok ? min(EPV, L - t) * int(sizeof(T)) : 0;
-        bytes = max(bytes, 0);
-        // a zero-byte copy only zero-fills, but its source must still be a valid aligned address
-        cp_async_16(dst + r * RS + j * EPV, bytes > 0 ? static_cast<const void*>(src + t) : gu, bytes);
-      }
-    } else {
-      for (int e = tid; e < ROWS * kChunk; e += NT) {
-        const int r = e / kChunk, j = e % kChunk;
-        if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;
-        bool ok;
-        const T* src = row_src(r, ok);
-        const int t = t0 + j;
-        dst[r * RS + j] = (ok && t < L) ? src[t] : from_f32<T>(0.0f);
-      }
-    }
-  };
-
-  const int nchunks = (L + kChunk - 1) / kChunk;
-  if (nchunks > 0) stage_load(0, 0);
-  cp_async_commit();
-  T* yrow = gy + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L;  // this lane's output row (finishing mapping)
+  T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L;
 
   for (int k = 0; k < nchunks; ++k) {
+    const int s = k & 1;
     const int t0 = k * kChunk;
-    if (k + 1 < nchunks) stage_load((k + 1) & 1, t0 + kChunk);
-    cp_async_commit();
-    cp_async_wait<1>();
-    __syncthreads();
+    bar_sync(kBarFull0 + s, NT);
+    const float* Bs = tabBs(s);
+    const float* Cs = tabCs(s);
+    const float2* Ps = tabPs(s);
+    const float2* DS = tabDS(s);
 
-    const T* st = raw + size_t(k & 1) * ROWS * RS;
-    const T* su = st;
-    const T* sd = st + CPB * RS;
-    const T* sz = st + 2 * CPB * RS;
-    const T* sB = st + 3 * CPB * RS;
-    const T* sC = sB + NPAD * RS;
-
-    // (a) B, C rows -> float32 [t][n] tables, two steps per thread and iteration.
-    for (int e = tid; e < NPAD * kChunk; e += NT) {  // 2 tables x NPAD rows x CHUNK/2 step pairs
-      const int which = e / (NPAD * kChunk / 2), rem = e % (NPAD * kChunk / 2);
-      const int tp = rem / NPAD, n = rem % NPAD;
-      const float2 v = load2<T>((which == 0 ? sB : sC) + n * RS + 2 * tp);
-      float* dst = which == 0 ? Bs : Cs;
-      dst[(2 * tp) * NPAD + n] = v.x;
-      dst[(2 * tp + 1) * NPAD + n] = v.y;
-    }
-    // (b) per-element prologue for this warp's channels, two steps at a time.
-#pragma unroll
-    for (int tp = lane / CPW; tp < kChunk / 2; tp += 32 / CPW) {
-      const int t = 2 * tp;
-      const float2 dl_raw = load2<T>(sd + pcl * RS + t);
-      const float2 uu = load2<T>(su + pcl * RS + t);
-      float2 dl = __fadd2_rn(dl_raw, f2(p_bias, p_bias));
-      if (a.softplus) dl = softplus2(dl);
-      if (t0 + t >= L || !pch_ok) dl.x = 0.0f;
-      if (t0 + t + 1 >= L || !pch_ok) dl.y = 0.0f;
-      const float2 du = __fmul2_rn(dl, uu);
-      const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
-      float2 sg = f2(1.0f, 1.0f);
-      if (has_z) {
-        const float2 zz = load2<T>(sz + pcl * RS + t);
-        sg = f2(silu_f32(zz.x), silu_f32(zz.y));
-      }
-      Ps[t * CPB + pcl] = f2(dl.x, du.x);
-      Ps[(t + 1) * CPB + pcl] = f2(dl.y, du.y);
-      *reinterpret_cast<float4*>(DS + pcl * DSS + t) = make_float4(Du.x, sg.x, Du.y, sg.y);
-    }
-    __syncthreads();
-
-    // (c) the recurrence over windows of kWin steps, then the readout sums and the epilogue.
 #pragma unroll 1
     for (int w = 0; w < kChunk; w += kWin) {
       float2 acc[kWin];
 #pragma unroll
       for (int j = 0; j < kWin; ++j) {
         const int t = w + j;
-        const float2 p = Ps[t * CPB + cl];
+        const float2 p = Ps[t * PSS + cl];
         const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
         const float4 cc = *reinterpret_cast<const float4*>(Cs + t * NPAD + 4 * g);
         const float2 dd = f2(p.x, p.x), uu = f2(p.y, p.y);
@@ -300,14 +345,13 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
         h23 = __ffma2_rn(a23, h23, __fmul2_rn(uu, f2(bb.z, bb.w)));
         acc[j] = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
       }
-      // sums over the R lanes of the channel and the pair halves; lane (cw, g) finishes the
-      // OPL steps w + g*OPL ... of channel cl
+      // sums over the R lanes of the channel and the pair halves; lane (g, cw) finishes the OPL
+      // steps w + g*OPL ... of channel cl
       float yv[OPL];
       if constexpr (R == 1) {
 #pragma unroll
         for (int j = 0; j < kWin; ++j) yv[j] = acc[j].x + acc[j].y;
       } else {
-        // this lane's partial for every step of the window, as 4 units of 4 steps
         float4* rb = red + size_t(warp) * 32 * UPB;
 #pragma unroll
         for (int i = 0; i < UPB; ++i)
@@ -315,7 +359,6 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
                                                         acc[4 * i + 2].x + acc[4 * i + 2].y,
                                                         acc[4 * i + 3].x + acc[4 * i + 3].y);
         __syncwarp();
-        // steps g*OPL .. g*OPL + OPL-1: units g*OPL/4 .. of every partner lane gp*CPW + cw
 #pragma unroll
         for (int u = 0; u < OPL / 4; ++u) {
           const int i = g * (OPL / 4) + u;
@@ -343,8 +386,8 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT) scan_fwd_kernel(const Sc
       const int tg = t0 + tb;  // first global step
       if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, L - tg);
     }
+    bar_arrive(kBarEmpty0 + s, NT);  // table stage s may be refilled
   }
-  cp_async_wait<0>();
 
   if (a.last_state && ch_ok) {
     const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
