@@ -72,6 +72,7 @@ struct ScanCfg {
   static constexpr size_t kRed = R > 1 ? size_t(32 * CWARPS) * UPB * 16 : 0;    // red [lanes][UPB] float4
   static constexpr size_t kSmem = kRaw + kTab + kRed;
   static_assert(kRawStage % 16 == 0 && kBCStage % 16 == 0 && kPStage % 16 == 0 && kDSStage % 16 == 0, "align");
+  static_assert(OPL % 4 == 0 && kChunk % kWin == 0, "each lane finishes whole 16-byte units of the window");
 };
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
@@ -251,14 +252,22 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
       float2* Ps = tabPs(s);
       float2* DS = tabDS(s);
 
-      // B, C rows -> float32 [t][n] tables, two steps per item
-      for (int e = ptid; e < NPAD * kChunk; e += PT) {  // 2 tables x NPAD rows x CHUNK/2 step pairs
-        const int which = e / (NPAD * kChunk / 2), rem = e % (NPAD * kChunk / 2);
-        const int tp = rem / NPAD, n = rem % NPAD;
-        const float2 v = load2<T>((which == 0 ? sB : sC) + n * RS + 2 * tp);
-        float* dst = which == 0 ? Bs : Cs;
-        dst[(2 * tp) * NPAD + n] = v.x;
-        dst[(2 * tp + 1) * NPAD + n] = v.y;
+      // B, C rows -> float32 [t][n] tables; one item = 8 steps of one row (a 16-byte staged read
+      // for bf16), consecutive threads take consecutive rows so the table writes are conflict-free
+      constexpr int SPI = 8;
+      for (int e = ptid; e < 2 * NPAD * (kChunk / SPI); e += PT) {
+        const int n = e % NPAD, rest = e / NPAD;
+        const int which = rest / (kChunk / SPI), q = rest % (kChunk / SPI);
+        const T* srow = (which == 0 ? sB : sC) + n * RS + q * SPI;
+        float v[SPI];
+#pragma unroll
+        for (int j = 0; j < SPI; j += 2) {
+          const float2 p2 = load2<T>(srow + j);
+          v[j] = p2.x, v[j + 1] = p2.y;
+        }
+        float* dst = (which == 0 ? Bs : Cs) + (q * SPI) * NPAD + n;
+#pragma unroll
+        for (int j = 0; j < SPI; ++j) dst[j * NPAD] = v[j];
       }
       // per-element work: Delta, Delta*u, D*u, silu(z), two steps per item
       const bool full = t0 + kChunk <= L;
