@@ -65,13 +65,21 @@ def measured_peaks():
 
 
 def committed_traffic(kernel: str):
-    """DRAM bytes per launch of `kernel` from the committed ncu summary (profiles/*.json), or None."""
+    """DRAM bytes per launch of `kernel` from the committed ncu capture (profiles/ncu_traffic.json),
+    or None when there is none or the kernel's sources changed since it was taken."""
+    import hashlib
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
         with open(path) as f:
-            data = json.load(f)
-        return data.get(kernel)
-    except (OSError, ValueError):
+            rec = json.load(f).get(kernel)
+        if rec is None:
+            return None
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        return int(rec["bytes"]) if h.hexdigest()[:16] == rec["source_sha256_16"] else None
+    except (OSError, ValueError, KeyError):
         return None
 
 
@@ -263,11 +271,18 @@ class _Null:
 
 
 def max_over_ranks(x: float, dist) -> float:
+    """The largest of the ranks' values (the job's time is its slowest rank's)."""
     if dist is None:
         return x
-    t = torch.tensor([x], dtype=torch.float64, device=torch.cuda.current_device())
+    dev = "cpu" if dist.get_backend() == "gloo" else torch.device("cuda", torch.cuda.current_device())
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(elements_per_rank: int, world: int, ms: float) -> float:
+    """Whole-job throughput: every rank processes its own replica of the workload."""
+    return elements_per_rank * world / (ms * 1e-3)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -413,6 +428,26 @@ def run_decode(device, steps_graph=3, warmup=1):
     }
 
 
+def profile_mode(which: str) -> int:
+    """A few launches of one kernel for an ncu capture: the mid-size scan (about 0.6 GB on the
+    device) or decode steps of the decode workload without a graph (about 0.2 GB)."""
+    from selective_state_space_155_b300 import build as _build
+    _build.build()
+    device = torch.device("cuda", 0)
+    if which == "scan":
+        run = ScanRun(wl.MID, device, copies=1)
+        fn = run.step
+    else:
+        import dataclasses
+        run = DecodeRun(dataclasses.replace(wl.DECODE, steps=5), device)
+        fn = run.step
+    for i in range(5):
+        fn(i)
+    torch.cuda.synchronize()
+    print(f"profile {which}: 5 launches done", flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -422,7 +457,12 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--profile", choices=["scan", "decode"], default=None,
+                    help="run 2 warm-up and 3 profiled launches of one kernel on its workload and exit "
+                         "(a small command for ncu; prints no JSON line)")
     args = ap.parse_args(argv)
+    if args.profile is not None:
+        return profile_mode(args.profile)
     if args.warmup < 3:
         args.warmup = 3
 
@@ -457,12 +497,12 @@ def main(argv=None):
     ms = timed(run.step, args.steps, args.warmup, dist, sampler)
     ms = max_over_ranks(ms, dist)
     elems = w.elements * world
-    value = elems / (ms * 1e-3)
+    value = weak_scaling_value(w.elements, world, ms)
     bytes_launch = w.algorithmic_bytes()
     hbm, src = measured_peaks()
     achieved = bytes_launch / (ms * 1e-3) / 1e9
     kernel = "scan_fwd_kernel"
-    traffic = committed_traffic(kernel)
+    traffic = committed_traffic(kernel)  # bytes per launch, or None
     del run
     torch.cuda.empty_cache()
 
