@@ -63,7 +63,8 @@ struct ScanCfg {
   static constexpr int UPB = kWin / 4;                // 16-byte units per lane block of readout partials
   // shared memory map (bytes)
   static constexpr size_t kRawStage = size_t(ROWS) * RS * sizeof(T);
-  static constexpr size_t kBCStage = size_t(2) * kChunk * NPAD * sizeof(float);  // Bs, Cs [CHUNK][NPAD]
+  static constexpr int kCOfs = kChunk * NPAD + 16;    // float offset of the C table after the B table
+  static constexpr size_t kBCStage = size_t(kCOfs + kChunk * NPAD) * sizeof(float);  // Bs, Cs [CHUNK][NPAD]
   static constexpr size_t kPStage = size_t(kChunk) * PSS * sizeof(float2);      // Ps [CHUNK][PSS]
   static constexpr size_t kDSStage = size_t(CPB) * DSS * sizeof(float2);        // DS [CPB][DSS]
   static constexpr size_t kTabStage = kBCStage + kPStage + kDSStage;
@@ -73,6 +74,7 @@ struct ScanCfg {
   static constexpr size_t kSmem = kRaw + kTab + kRed;
   static_assert(kRawStage % 16 == 0 && kBCStage % 16 == 0 && kPStage % 16 == 0 && kDSStage % 16 == 0, "align");
   static_assert(OPL % 4 == 0 && kChunk % kWin == 0, "each lane finishes whole 16-byte units of the window");
+  static_assert((RS * sizeof(T)) % 16 == 0 && kChunk % 8 == 0, "staged rows hold whole 16-byte vectors");
 };
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
@@ -111,6 +113,25 @@ __device__ __forceinline__ float2 load2<float>(const float* p) {
 template <>
 __device__ __forceinline__ float2 load2<__nv_bfloat16>(const __nv_bfloat16* p) {
   return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(p));
+}
+
+// Eight consecutive staged io elements (16-byte aligned) as float32, with 16-byte loads.
+template <typename T>
+__device__ __forceinline__ void load8(const T* p, float (&v)[8]);
+template <>
+__device__ __forceinline__ void load8<float>(const float* p, float (&v)[8]) {
+  const float4 lo = *reinterpret_cast<const float4*>(p), hi = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = lo.x, v[1] = lo.y, v[2] = lo.z, v[3] = lo.w, v[4] = hi.x, v[5] = hi.y, v[6] = hi.z, v[7] = hi.w;
+}
+template <>
+__device__ __forceinline__ void load8<__nv_bfloat16>(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 q = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+    v[2 * k] = f.x, v[2 * k + 1] = f.y;
+  }
 }
 
 // Store n consecutive outputs (n <= OPL valid ones of the OPL given) as io type.  With VEC the
@@ -157,7 +178,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   unsigned char* tab = smem + Cfg::kRaw;
   float4* red = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kTab);
   auto tabBs = [&](int s) { return reinterpret_cast<float*>(tab + s * Cfg::kTabStage); };
-  auto tabCs = [&](int s) { return reinterpret_cast<float*>(tab + s * Cfg::kTabStage) + kChunk * NPAD; };
+  auto tabCs = [&](int s) { return reinterpret_cast<float*>(tab + s * Cfg::kTabStage) + Cfg::kCOfs; };
   auto tabPs = [&](int s) { return reinterpret_cast<float2*>(tab + s * Cfg::kTabStage + Cfg::kBCStage); };
   auto tabDS = [&](int s) {
     return reinterpret_cast<float2*>(tab + s * Cfg::kTabStage + Cfg::kBCStage + Cfg::kPStage);
@@ -176,58 +197,104 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
     // ================================ prep warps ================================
     const int ptid = tid - 32 * CWARPS;
     const int pw = warp - CWARPS;
+    const int dim = a.dim;
+    const bool softplus = a.softplus != 0;
     const T* __restrict__ gu = static_cast<const T*>(a.u);
     const T* __restrict__ gd = static_cast<const T*>(a.delta);
     const T* __restrict__ gz = static_cast<const T*>(a.z);
     const T* __restrict__ gB = static_cast<const T*>(a.B);
     const T* __restrict__ gC = static_cast<const T*>(a.C);
 
-    auto row_src = [&](int r, bool& ok) -> const T* {
+    // Global start of staged row r (u, delta, z rows by channel, then B and C rows by state);
+    // ok = the row exists.  Rows of channels past dim and z rows without a gate are never used
+    // by another channel, so they are not copied; B and C rows past dstate are zero-filled
+    // (every channel reads them).
+    auto row_src = [&](int r, bool& ok, bool& fill) -> const T* {
       if (r < 3 * CPB) {
         const int which = r / CPB, c = r % CPB;
         const T* base = which == 0 ? gu : (which == 1 ? gd : gz);
-        ok = (d0 + c < a.dim) && (which < 2 || has_z);
-        return base + (size_t(b) * a.dim + (d0 + c)) * L;
+        ok = (d0 + c < dim) && (which < 2 || has_z);
+        fill = false;
+        return ok ? base + (size_t(b) * dim + (d0 + c)) * L : gu;
       }
       const int rr = r - 3 * CPB;
       const int which = rr / NPAD, n = rr % NPAD;
       ok = n < N;
-      return (which == 0 ? gB : gC) + (size_t(b) * N + n) * L;
+      fill = true;
+      return ok ? (which == 0 ? gB : gC) + (size_t(b) * N + n) * L : gu;
     };
+
+    // Each prep thread owns the same SLOTS 16-byte copy slots (row, column) in every chunk, so
+    // their addresses are worked out once.
+    constexpr int NV = ROWS * VPR;
+    constexpr int SLOTS = (NV + PT - 1) / PT;
+    const T* s_src[SLOTS];  // global address of the slot's first element in chunk 0
+    int s_dst[SLOTS];       // element offset within a raw stage, -1 = nothing to copy
+    int s_col[SLOTS];       // first step of the slot within a chunk
+    bool s_ok[SLOTS];
+    if constexpr (VEC) {
+#pragma unroll
+      for (int i = 0; i < SLOTS; ++i) {
+        const int v = ptid + i * PT;
+        const int r = v / VPR, j = v % VPR;
+        bool ok = false, fill = false;
+        const T* src = v < NV ? row_src(r, ok, fill) : gu;
+        s_src[i] = ok ? src + j * EPV : gu;
+        s_dst[i] = (v < NV && (ok || fill)) ? r * RS + j * EPV : -1;
+        s_col[i] = j * EPV;
+        s_ok[i] = ok;
+      }
+    }
     auto stage_load = [&](int stage, int t0) {
       T* dst = raw + size_t(stage) * ROWS * RS;
       if constexpr (VEC) {
-        for (int v = ptid; v < ROWS * VPR; v += PT) {
-          const int r = v / VPR, j = v % VPR;
-          if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;  // z rows are never read without a gate
-          bool ok;
-          const T* src = row_src(r, ok);
-          const int t = t0 + j * EPV;
-          int bytes = ok ? min(EPV, L - t) * int(sizeof(T)) : 0;
-          bytes = max(bytes, 0);
-          // a zero-byte copy only zero-fills, but its source must still be a valid aligned address
-          cp_async_16(dst + r * RS + j * EPV, bytes > 0 ? static_cast<const void*>(src + t) : gu, bytes);
+#pragma unroll
+        for (int i = 0; i < SLOTS; ++i) {
+          if (s_dst[i] < 0) continue;
+          // rows are 16-byte multiples, so a vector is wholly inside or wholly past the end;
+          // a zero-byte copy only zero-fills, but its source must still be a valid address
+          const bool in = s_ok[i] && t0 + s_col[i] < L;
+          cp_async_16(dst + s_dst[i], in ? static_cast<const void*>(s_src[i] + t0) : gu, in ? 16 : 0);
         }
       } else {
         for (int e = ptid; e < ROWS * kChunk; e += PT) {
           const int r = e / kChunk, j = e % kChunk;
-          if (!has_z && r >= 2 * CPB && r < 3 * CPB) continue;
-          bool ok;
-          const T* src = row_src(r, ok);
+          bool ok, fill;
+          const T* src = row_src(r, ok, fill);
+          if (!ok && !fill) continue;
           const int t = t0 + j;
           dst[r * RS + j] = (ok && t < L) ? src[t] : from_f32<T>(0.0f);
         }
       }
     };
 
+    // B, C conversion items: one item = 8 steps of one row.  Lanes 0..NPAD-1 of a group take the
+    // B rows and the next NPAD lanes the C rows of the same steps; the C table is offset by 16
+    // words so that both halves land in different banks.
+    constexpr int SPI = 8;
+    constexpr int NITEM = 2 * NPAD * (kChunk / SPI);
+    constexpr int IPT = (NITEM + PT - 1) / PT;
+    int c_src[IPT], c_dst[IPT];
+#pragma unroll
+    for (int m = 0; m < IPT; ++m) {
+      const int e = ptid + m * PT;
+      const int n = e % NPAD, which = (e / NPAD) % 2, q = e / (2 * NPAD);
+      c_src[m] = e < NITEM ? (3 * CPB + which * NPAD + n) * RS + q * SPI : -1;
+      c_dst[m] = which * Cfg::kCOfs + (q * SPI) * NPAD + n;
+    }
+
     // prologue mapping: prep warp pw handles channels PCW*pw + (lane % PCW); the lanes lane/PCW +
     // PPL*i walk the step pairs of the chunk (conflict-free reads of the staged rows)
     constexpr int PCW = CPB / kPrepWarps;  // channels per prep warp (8)
     constexpr int PPL = 32 / PCW;          // step-pair lanes per channel (4)
     const int pcl = pw * PCW + (lane % PCW);
-    const bool pch_ok = d0 + pcl < a.dim;
+    const int tq = lane / PCW;
+    const bool pch_ok = d0 + pcl < dim;
     const float p_bias = (pch_ok && a.dt_bias) ? a.dt_bias[d0 + pcl] : 0.0f;
     const float p_D = (pch_ok && a.D) ? a.D[d0 + pcl] : 0.0f;
+    const int r_ofs = pcl * RS + 2 * tq;     // element offset of this lane's first step pair in a row
+    const int ps_ofs = 2 * tq * PSS + pcl;   // float2 offset of its first (Delta, Delta*u) entry
+    const int ds_ofs = pcl * DSS + 2 * tq;   // float2 offset of its first (D*u, silu z) entry
 
     if (nchunks > 0) stage_load(0, 0);
     cp_async_commit();
@@ -242,58 +309,51 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
       if (k >= 2) bar_sync(kBarEmpty0 + s, NT);  // the recurrence warps are done with table stage s
 
       const T* st = raw + size_t(s) * ROWS * RS;
-      const T* su = st;
-      const T* sd = st + CPB * RS;
-      const T* sz = st + 2 * CPB * RS;
-      const T* sB = st + 3 * CPB * RS;
-      const T* sC = sB + NPAD * RS;
-      float* Bs = tabBs(s);
-      float* Cs = tabCs(s);
+      float* BCs = tabBs(s);
       float2* Ps = tabPs(s);
       float2* DS = tabDS(s);
 
-      // B, C rows -> float32 [t][n] tables; one item = 8 steps of one row (a 16-byte staged read
-      // for bf16), consecutive threads take consecutive rows so the table writes are conflict-free
-      constexpr int SPI = 8;
-      for (int e = ptid; e < 2 * NPAD * (kChunk / SPI); e += PT) {
-        const int n = e % NPAD, rest = e / NPAD;
-        const int which = rest / (kChunk / SPI), q = rest % (kChunk / SPI);
-        const T* srow = (which == 0 ? sB : sC) + n * RS + q * SPI;
-        float v[SPI];
 #pragma unroll
-        for (int j = 0; j < SPI; j += 2) {
-          const float2 p2 = load2<T>(srow + j);
-          v[j] = p2.x, v[j + 1] = p2.y;
-        }
-        float* dst = (which == 0 ? Bs : Cs) + (q * SPI) * NPAD + n;
+      for (int m = 0; m < IPT; ++m) {
+        if (c_src[m] < 0) continue;
+        float v[SPI];
+        load8<T>(st + c_src[m], v);
+        float* dst = BCs + c_dst[m];
 #pragma unroll
         for (int j = 0; j < SPI; ++j) dst[j * NPAD] = v[j];
       }
-      // per-element work: Delta, Delta*u, D*u, silu(z), two steps per item
-      const bool full = t0 + kChunk <= L;
+
+      // per-element work: Delta, Delta*u, D*u, silu(z), two steps per item.  Steps past the end
+      // (and channels past dim) get Delta = 0, which leaves the state unchanged.
+      const int lim = pch_ok ? L - t0 : 0;
+      auto items = [&](auto masked) {
 #pragma unroll
-      for (int i = 0; i < kChunk / 2 / PPL; ++i) {
-        const int tp = lane / PCW + i * PPL;
-        const int t = 2 * tp;
-        const float2 dl_raw = load2<T>(sd + pcl * RS + t);
-        const float2 uu = load2<T>(su + pcl * RS + t);
-        float2 dl = __fadd2_rn(dl_raw, f2(p_bias, p_bias));
-        if (a.softplus) dl = softplus2(dl);
-        if (!full || !pch_ok) {
-          if (t0 + t >= L || !pch_ok) dl.x = 0.0f;
-          if (t0 + t + 1 >= L || !pch_ok) dl.y = 0.0f;
+        for (int i = 0; i < kChunk / 2 / PPL; ++i) {
+          const int o = 2 * PPL * i;
+          const float2 uu = load2<T>(st + r_ofs + o);
+          const float2 dr = load2<T>(st + CPB * RS + r_ofs + o);
+          const float2 zz = load2<T>(st + 2 * CPB * RS + r_ofs + o);
+          const float2 dx = __fadd2_rn(dr, f2(p_bias, p_bias));
+          const float2 sp = softplus2(dx);
+          float2 dl = softplus ? sp : dx;
+          if constexpr (decltype(masked)::value) {
+            const int t = 2 * tq + o;
+            dl.x = t < lim ? dl.x : 0.0f;
+            dl.y = t + 1 < lim ? dl.y : 0.0f;
+          }
+          const float2 du = __fmul2_rn(dl, uu);
+          const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
+          const float2 sg = has_z ? f2(silu_f32(zz.x), silu_f32(zz.y)) : f2(1.0f, 1.0f);
+          Ps[ps_ofs + o * PSS] = f2(dl.x, du.x);
+          Ps[ps_ofs + (o + 1) * PSS] = f2(dl.y, du.y);
+          *reinterpret_cast<float4*>(DS + ds_ofs + o) = make_float4(Du.x, sg.x, Du.y, sg.y);
         }
-        const float2 du = __fmul2_rn(dl, uu);
-        const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
-        float2 sg = f2(1.0f, 1.0f);
-        if (has_z) {
-          const float2 zz = load2<T>(sz + pcl * RS + t);
-          sg = f2(silu_f32(zz.x), silu_f32(zz.y));
-        }
-        Ps[t * PSS + pcl] = f2(dl.x, du.x);
-        Ps[(t + 1) * PSS + pcl] = f2(dl.y, du.y);
-        *reinterpret_cast<float4*>(DS + pcl * DSS + t) = make_float4(Du.x, sg.x, Du.y, sg.y);
-      }
+      };
+      if (lim >= kChunk)
+        items(std::false_type{});
+      else
+        items(std::true_type{});
+
       bar_sync(kBarPrep, PT);            // every prep thread is done reading raw stage s
       bar_arrive(kBarFull0 + s, NT);     // table stage s is ready
       if (k + 2 < nchunks) stage_load(s, t0 + 2 * kChunk);
