@@ -42,6 +42,13 @@ constexpr int kChunk = 32;  // steps per chunk
 constexpr int kWin = 16;    // steps per recurrence window (readout partials held in registers)
 constexpr int kPrepWarps = 4;
 
+// Register split of the four-recurrence-warp layout (dstate 9..16): the kernel is launched with
+// kLaunchRegs per thread; the prep warpgroup gives registers back and the recurrence warpgroup,
+// whose unrolled window is the long pole, takes them.  The shares add up to the launch total.
+constexpr int kLaunchRegs = 80, kPrepRegs = 48, kRecRegs = 112;
+static_assert(4 * kPrepRegs + 4 * kRecRegs == 8 * kLaunchRegs && kPrepWarps == 4,
+              "setmaxnreg shares (one warpgroup each) must add up to the launch total");
+
 // named barrier ids (0 is __syncthreads)
 constexpr int kBarFull0 = 1, kBarEmpty0 = 3, kBarPrep = 5;
 
@@ -195,6 +202,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
 
   if (warp >= CWARPS) {
     // ================================ prep warps ================================
+    if constexpr (CWARPS == 4) asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kPrepRegs));
     const int ptid = tid - 32 * CWARPS;
     const int pw = warp - CWARPS;
     const int dim = a.dim;
@@ -366,6 +374,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   }
 
   // ============================== recurrence warps ==============================
+  if constexpr (CWARPS == 4) asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRecRegs));
   // n-group major: the lanes of a quarter-warp (R = 4) share one n-group, so their B and C loads
   // hit one address; the R lanes of channel cw are cw, cw + CPW, ...
   const int cw = lane % CPW, g = lane / CPW;
@@ -481,6 +490,14 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   if (!(configured.load(std::memory_order_acquire) & bit)) {
     err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(Cfg::kSmem));
     if (err != cudaSuccess) return err;
+    if constexpr (Cfg::CWARPS == 4) {
+      // the setmaxnreg split assumes the launch allocation it was sized for; a build whose
+      // register count differs would make the recurrence warps wait for registers forever
+      cudaFuncAttributes fa{};
+      err = cudaFuncGetAttributes(&fa, kernel);
+      if (err != cudaSuccess) return err;
+      if (fa.numRegs != kLaunchRegs) return cudaErrorInvalidDeviceFunction;
+    }
     configured.fetch_or(bit, std::memory_order_acq_rel);
   }
   const long long nblk = (long long)((a.dim + Cfg::CPB - 1) / Cfg::CPB) * a.batch;
