@@ -15,6 +15,9 @@ Parity status per function (what pins it, see tests/test_oracle_pins.py):
   scan            pinned: prefix-sum worked example, closed-form y2/y3 expansions,
                   brute-force convolution form, unrolled time-varying sum, Delta->0,
                   exact halving with Delta = ln 2, softplus/silu special values.
+  scan (zoh)      pinned: the exact solution of the continuous system under a held input
+                  (closed form, and scipy's matrix exponential of the augmented system),
+                  A = 0 equals the Delta*B form, decode steps equal the scan.
   state_update    pinned: equals the pinned scan step by step; exact halving case.
   assoc_scan      pinned: prefix-sum worked example; equals the closed-form products.
   scan_tree       pinned: equals the sequential scan (associativity).
@@ -64,9 +67,9 @@ def _load():
                 build()
             lib = ctypes.CDLL(_LIB)
             lib.oracle_scan_f64.restype = ctypes.c_int
-            lib.oracle_scan_f64.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP, _DP] + [ctypes.c_int] * 5
+            lib.oracle_scan_f64.argtypes = [_DP] * 8 + [ctypes.c_int, ctypes.c_int, _DP, _DP, _DP] + [ctypes.c_int] * 5
             lib.oracle_state_update_f64.restype = ctypes.c_int
-            lib.oracle_state_update_f64.argtypes = [_DP] * 9 + [ctypes.c_int, _DP] + [ctypes.c_int] * 4
+            lib.oracle_state_update_f64.argtypes = [_DP] * 9 + [ctypes.c_int, ctypes.c_int, _DP] + [ctypes.c_int] * 4
             lib.oracle_assoc_scan_pairs_f64.restype = ctypes.c_int
             lib.oracle_assoc_scan_pairs_f64.argtypes = [_DP] * 4 + [ctypes.c_int]
             lib.oracle_scan_tree_f64.restype = ctypes.c_int
@@ -92,8 +95,9 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(_DP)
 
 
-def scan(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, nthreads=0):
-    """Selective scan.  Returns (y [batch,dim,L], last_state [batch,dim,N])."""
+def scan(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, nthreads=0, zoh=False):
+    """Selective scan.  Returns (y [batch,dim,L], last_state [batch,dim,N]).  zoh selects the exact
+    zero-order-hold Bbar = (exp(Delta A) - 1) / A * B instead of Delta * B."""
     u = _f64(u)
     batch, dim, seqlen = u.shape
     A = _f64(A)
@@ -109,14 +113,14 @@ def scan(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, h
     y = np.zeros((batch, dim, seqlen), dtype=np.float64)
     last = np.zeros((batch, dim, dstate), dtype=np.float64)
     rc = _load().oracle_scan_f64(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(dt_bias),
-                                 int(bool(delta_softplus)), _ptr(h0), _ptr(y), _ptr(last),
+                                 int(bool(delta_softplus)), int(bool(zoh)), _ptr(h0), _ptr(y), _ptr(last),
                                  batch, dim, dstate, seqlen, int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_scan_f64 failed: {rc}")
     return y, last
 
 
-def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, nthreads=0):
+def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, nthreads=0, zoh=False):
     """One decode step.  Returns (new_state [batch,dim,N], out [batch,dim]); `state` is not modified."""
     s = np.array(state, dtype=np.float64, copy=True, order="C")
     batch, dim, dstate = s.shape
@@ -130,7 +134,8 @@ def state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplu
     dt_bias = _f64(dt_bias, (dim,))
     out = np.zeros((batch, dim), dtype=np.float64)
     rc = _load().oracle_state_update_f64(_ptr(s), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                                         _ptr(dt_bias), int(bool(dt_softplus)), _ptr(out), batch, dim, dstate,
+                                         _ptr(dt_bias), int(bool(dt_softplus)), int(bool(zoh)), _ptr(out), batch, dim,
+                                         dstate,
                                          int(nthreads))
     if rc != 0:
         raise RuntimeError(f"oracle_state_update_f64 failed: {rc}")

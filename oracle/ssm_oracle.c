@@ -18,6 +18,12 @@
  *                  A) and Bbar*x = Delta * B[n] * u: gsyq.cn page, sections
  *                  "连续到离散的转换" and "硬件优化并行扫描算法" (A_bar =
  *                  exp(Delta*A), B_bar = Delta*B); VMamba notes, "离散化SSM".
+ *                  With zoh set, Bbar is the exact zero-order hold instead:
+ *                  Bbar = (Delta A)^-1 (exp(Delta A) - I) Delta B, which for a
+ *                  diagonal A is (exp(Delta A[d,n]) - 1) / A[d,n] * B[n], and
+ *                  Delta * B[n] where A[d,n] = 0 (its limit): gsyq.cn page,
+ *                  "连续到离散的转换"; VMamba notes, section on the dimensions
+ *                  of A, B, C ("S4中三个矩阵的维度表示、维度变化").
  *   Recurrence     h_t = Abar_t * h_{t-1} + Bbar_t * x_t, h_{-1} = h0 (zero
  *                  when not given): gsyq.cn page, the sequential loop in
  *                  "计算复杂度分析"; VMamba notes, "循环结构表示以快速推理".
@@ -66,6 +72,13 @@ static double softplus_f64(double x) {
 /* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
 static double silu_f64(double z) { return z / (1.0 + exp(-z)); }
 
+/* The factor Bbar / B[n] of the discretisation: Delta (Delta*B form) or the exact
+ * zero-order-hold (exp(Delta*a) - 1) / a, whose limit at a = 0 is Delta. */
+static double bbar_factor(double dt, double a, int zoh) {
+  if (!zoh || a == 0.0) return dt;
+  return expm1(dt * a) / a;
+}
+
 static double step_size(double raw, const double* dt_bias, int d, int use_softplus) {
   double v = raw;
   if (dt_bias) v += dt_bias[d];
@@ -73,12 +86,13 @@ static double step_size(double raw, const double* dt_bias, int d, int use_softpl
   return v;
 }
 
-int oracle_abi_version(void) { return 1; }
+int oracle_abi_version(void) { return 2; }
 
 /* Selective scan over seqlen steps for every (batch, channel). */
 int oracle_scan_f64(const double* u, const double* delta, const double* A, const double* B, const double* C,
-                    const double* D, const double* z, const double* dt_bias, int delta_softplus, const double* h0,
-                    double* y, double* last_state, int batch, int dim, int dstate, int seqlen, int nthreads) {
+                    const double* D, const double* z, const double* dt_bias, int delta_softplus, int zoh,
+                    const double* h0, double* y, double* last_state, int batch, int dim, int dstate, int seqlen,
+                    int nthreads) {
   if (!u || !delta || !A || !B || !C || !y) return -1;
   if (batch < 0 || dim < 0 || dstate < 1 || seqlen < 0) return -2;
   long nch = (long)batch * dim;
@@ -99,8 +113,9 @@ int oracle_scan_f64(const double* u, const double* delta, const double* A, const
       double x = u_row[t];
       double acc = 0.0;
       for (int n = 0; n < dstate; ++n) {
-        double abar = exp(dt * A[(long)d * dstate + n]);
-        double bx = dt * B[((long)b * dstate + n) * seqlen + t] * x;
+        double a = A[(long)d * dstate + n];
+        double abar = exp(dt * a);
+        double bx = bbar_factor(dt, a, zoh) * B[((long)b * dstate + n) * seqlen + t] * x;
         h[n] = abar * h[n] + bx;
         acc += C[((long)b * dstate + n) * seqlen + t] * h[n];
       }
@@ -118,7 +133,7 @@ int oracle_scan_f64(const double* u, const double* delta, const double* A, const
 /* One decode step: state <- Abar*state + Bbar*x in place, out = (C.state + D x) * silu(z). */
 int oracle_state_update_f64(double* state, const double* x, const double* dt, const double* A, const double* B,
                             const double* C, const double* D, const double* z, const double* dt_bias,
-                            int dt_softplus, double* out, int batch, int dim, int dstate, int nthreads) {
+                            int dt_softplus, int zoh, double* out, int batch, int dim, int dstate, int nthreads) {
   if (!state || !x || !dt || !A || !B || !C || !out) return -1;
   if (batch < 0 || dim < 0 || dstate < 1) return -2;
   long nch = (long)batch * dim;
@@ -132,8 +147,9 @@ int oracle_state_update_f64(double* state, const double* x, const double* dt, co
     double acc = 0.0;
     for (int n = 0; n < dstate; ++n) {
       double* s = &state[ch * dstate + n];
-      double abar = exp(step * A[(long)d * dstate + n]);
-      *s = abar * *s + step * B[(long)b * dstate + n] * x[ch];
+      double a = A[(long)d * dstate + n];
+      double abar = exp(step * a);
+      *s = abar * *s + bbar_factor(step, a, zoh) * B[(long)b * dstate + n] * x[ch];
       acc += C[(long)b * dstate + n] * *s;
     }
     if (D) acc += D[d] * x[ch];

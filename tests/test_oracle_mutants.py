@@ -16,10 +16,9 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "ssm_oracle.c")
 
 MUTANTS = {
     "drop_D_skip": ("if (D) acc += D[d] * x;\n      if (z_row)", "if (z_row)"),
-    "A_sign": ("double abar = exp(dt * A[(long)d * dstate + n]);\n        double bx",
-               "double abar = exp(-dt * A[(long)d * dstate + n]);\n        double bx"),
-    "B_transposed": ("double bx = dt * B[((long)b * dstate + n) * seqlen + t] * x;",
-                     "double bx = dt * B[((long)b * seqlen + t) * dstate + n] * x;"),
+    "A_sign": ("double abar = exp(dt * a);\n        double bx", "double abar = exp(-dt * a);\n        double bx"),
+    "B_transposed": ("double bx = bbar_factor(dt, a, zoh) * B[((long)b * dstate + n) * seqlen + t] * x;",
+                     "double bx = bbar_factor(dt, a, zoh) * B[((long)b * seqlen + t) * dstate + n] * x;"),
     "C_from_B": ("acc += C[((long)b * dstate + n) * seqlen + t] * h[n];",
                  "acc += B[((long)b * dstate + n) * seqlen + t] * h[n];"),
     "readout_before_update": ("h[n] = abar * h[n] + bx;\n        acc += C[((long)b * dstate + n) * seqlen + t] * h[n];",
@@ -28,12 +27,15 @@ MUTANTS = {
                             "if (use_softplus) v = softplus_f64(v);\n  if (dt_bias) v += dt_bias[d];"),
     "softplus_wrong_branch": ("if (x > 0.0) return x + log1p(exp(-x));", "if (x > 0.0) return log1p(exp(-x));"),
     "silu_sign": ("return z / (1.0 + exp(-z));", "return z / (1.0 + exp(z));"),
-    "bbar_missing_delta": ("double bx = dt * B[((long)b * dstate + n) * seqlen + t] * x;",
-                           "double bx = B[((long)b * dstate + n) * seqlen + t] * x;"),
+    "bbar_missing_delta": ("if (!zoh || a == 0.0) return dt;", "if (!zoh || a == 0.0) return 1.0;"),
+    "zoh_exp_not_expm1": ("return expm1(dt * a) / a;", "return exp(dt * a) / a;"),
+    "zoh_missing_divide": ("return expm1(dt * a) / a;", "return expm1(dt * a);"),
+    "zoh_limit_at_zero": ("if (!zoh || a == 0.0) return dt;", "if (!zoh) return dt;\n  if (a == 0.0) return 0.0;"),
+    "zoh_ignored": ("if (!zoh || a == 0.0) return dt;\n  return", "if (1) return dt;\n  return"),
     "gate_additive": ("if (z_row) acc *= silu_f64(z_row[t]);", "if (z_row) acc += silu_f64(z_row[t]);"),
     "pair_combine_swapped": ("out_b[i] = ra * lb + rb;", "out_b[i] = la * rb + lb;"),
-    "decode_no_state_decay": ("*s = abar * *s + step * B[(long)b * dstate + n] * x[ch];",
-                              "*s = *s + step * B[(long)b * dstate + n] * x[ch];"),
+    "decode_no_state_decay": ("*s = abar * *s + bbar_factor(step, a, zoh) * B[(long)b * dstate + n] * x[ch];",
+                              "*s = *s + bbar_factor(step, a, zoh) * B[(long)b * dstate + n] * x[ch];"),
     "h0_ignored": ("h[n] = h0 ? h0[ch * dstate + n] : 0.0;", "h[n] = 0.0;"),
 }
 

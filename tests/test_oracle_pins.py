@@ -325,3 +325,88 @@ def test_empty_and_thread_count_independence():
     r4 = oracle.scan(u, delta, A, B, C, nthreads=4)
     np.testing.assert_array_equal(r1[0], r4[0])
     np.testing.assert_array_equal(r1[1], r4[1])
+
+
+# ---------------------------------------------------------------------------------------------
+# Exact zero-order hold: gsyq.cn page, section "连续到离散的转换", and the VMamba notes print
+# Bbar = (Delta A)^-1 (exp(Delta A) - I) Delta B.  Under a held input this is the exact
+# solution of the continuous system h' = A h + B x sampled every Delta.
+# ---------------------------------------------------------------------------------------------
+def test_zoh_equals_continuous_solution_under_constant_input():
+    """Constant Delta, B, C, u: h after k steps is (exp(A k Delta) - 1) / A * B u, the solution of
+    h' = A h + B u from h(0) = 0 at time k*Delta (closed form)."""
+    L, dt = 40, 0.37
+    A = np.array([[-0.7, -2.3, 0.4]])
+    Bv = np.array([1.5, -0.6, 0.9])
+    Cv = np.array([0.8, 1.1, -0.3])
+    u = np.full((1, 1, L), 0.75)
+    delta = np.full((1, 1, L), dt)
+    B = np.repeat(Bv[None, :, None], L, axis=2)
+    C = np.repeat(Cv[None, :, None], L, axis=2)
+    y, last = oracle.scan(u, delta, A, B, C, delta_softplus=False, zoh=True)
+    k = np.arange(1, L + 1)[:, None]
+    h = (np.exp(A[0][None, :] * k * dt) - 1.0) / A[0][None, :] * Bv[None, :] * 0.75
+    np.testing.assert_allclose(y.ravel(), h @ Cv, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(last.ravel(), h[-1], rtol=1e-12)
+
+
+def test_zoh_equals_matrix_exponential_of_augmented_system():
+    """Time-varying Delta, B, u held over each step: one step of the continuous system is the
+    matrix exponential of the augmented generator [[A, B u], [0, 0]] * Delta (scipy.linalg.expm),
+    applied to (h, 1).  Random signs, softplus step sizes, dt_bias, D and gate all on."""
+    from scipy.linalg import expm
+    rng = np.random.default_rng(31)
+    b_, d_, N, L = 1, 2, 3, 9
+    u = rng.standard_normal((b_, d_, L))
+    delta = rng.standard_normal((b_, d_, L))
+    A = -np.exp(rng.uniform(-1.0, 1.0, (d_, N)))
+    B = rng.standard_normal((b_, N, L))
+    C = rng.standard_normal((b_, N, L))
+    D = rng.standard_normal(d_)
+    z = rng.standard_normal((b_, d_, L))
+    bias = rng.uniform(-1.0, 0.5, d_)
+    y, last = oracle.scan(u, delta, A, B, C, D=D, z=z, dt_bias=bias, delta_softplus=True, zoh=True)
+    for d in range(d_):
+        h = np.zeros(N)
+        for t in range(L):
+            dt = math.log1p(math.exp(delta[0, d, t] + bias[d]))
+            for n in range(N):
+                G = np.array([[A[d, n], B[0, n, t] * u[0, d, t]], [0.0, 0.0]]) * dt
+                h[n] = (expm(G) @ np.array([h[n], 1.0]))[0]
+            ref = (C[0, :, t] @ h + D[d] * u[0, d, t]) * z[0, d, t] / (1.0 + math.exp(-z[0, d, t]))
+            assert abs(y[0, d, t] - ref) <= 1e-11 * (1.0 + abs(ref)), (d, t, y[0, d, t], ref)
+        np.testing.assert_allclose(last[0, d], h, rtol=1e-11, atol=1e-13)
+
+
+def test_zoh_with_A_zero_is_delta_B():
+    """A = 0: (exp(Delta A) - 1) / A tends to Delta, so the two discretisations coincide exactly."""
+    rng = np.random.default_rng(5)
+    u = rng.standard_normal((2, 3, 12))
+    delta = rng.standard_normal((2, 3, 12))
+    B = rng.standard_normal((2, 4, 12))
+    C = rng.standard_normal((2, 4, 12))
+    A = np.zeros((3, 4))
+    y0, s0 = oracle.scan(u, delta, A, B, C, delta_softplus=True)
+    y1, s1 = oracle.scan(u, delta, A, B, C, delta_softplus=True, zoh=True)
+    np.testing.assert_array_equal(y0, y1)
+    np.testing.assert_array_equal(s0, s1)
+
+
+def test_zoh_decode_steps_equal_scan():
+    rng = np.random.default_rng(8)
+    b_, d_, N, L = 2, 3, 4, 6
+    u = rng.standard_normal((b_, d_, L))
+    delta = rng.standard_normal((b_, d_, L))
+    A = -np.exp(rng.standard_normal((d_, N)))
+    B = rng.standard_normal((b_, N, L))
+    C = rng.standard_normal((b_, N, L))
+    D = rng.standard_normal(d_)
+    z = rng.standard_normal((b_, d_, L))
+    bias = rng.standard_normal(d_)
+    y, last = oracle.scan(u, delta, A, B, C, D=D, z=z, dt_bias=bias, zoh=True)
+    s = np.zeros((b_, d_, N))
+    for t in range(L):
+        s, out = oracle.state_update(s, u[:, :, t], delta[:, :, t], A, B[:, :, t], C[:, :, t], D=D, z=z[:, :, t],
+                                     dt_bias=bias, zoh=True)
+        np.testing.assert_array_equal(out, y[:, :, t])
+    np.testing.assert_array_equal(s, last)
