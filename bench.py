@@ -18,6 +18,7 @@ Extra objects on the line:
   cpu_baseline  the float64 oracle on the host cores (reported baseline, not a target);
   decode        the decode workload (batch 256, d_inner 5120, d_state 16): 1024 in-place steps
                 captured in one CUDA graph, and one step after an L2 flush;
+  zoh           the same scan workload with the exact zero-order-hold discretisation;
   clocks        SM clocks and throttle reasons sampled (NVML) during the timed region.
 
 Under torchrun each rank runs the same workload on its own GPU with no collective on the data
@@ -182,11 +183,12 @@ def l2_flush_buffer(device):
 class ScanRun:
     """The scan workload resident in HBM, with rotating input copies and preallocated outputs."""
 
-    def __init__(self, w: wl.ScanWorkload, device, copies: int = ROTATING_COPIES):
+    def __init__(self, w: wl.ScanWorkload, device, copies: int = ROTATING_COPIES, discretization: str = "delta_b"):
         import selective_state_space_155_b300 as ssm
         self.ssm = ssm
         self.w = w
         self.device = device
+        self.discretization = discretization
         base = wl.scan_inputs(w, device=device)
         self.sets = [base] + [{k: (v.clone() if v is not None else None) for k, v in base.items()}
                               for _ in range(copies - 1)]
@@ -198,7 +200,8 @@ class ScanRun:
         k = i % len(self.sets)
         s = self.sets[k]
         self.ssm.ssm_scan_fwd(s["u"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"], s["dt_bias"],
-                              delta_softplus=True, y=self.y[k], last_state=self.last[k])
+                              delta_softplus=True, y=self.y[k], last_state=self.last[k],
+                              discretization=self.discretization)
 
 
 class DecodeRun:
@@ -395,6 +398,18 @@ def run_e2e(w, device, steps, warmup, dist):
     return ms, h2d, d2h
 
 
+def run_zoh(w: wl.ScanWorkload, device, steps=200, warmup=5):
+    """The same scan workload with the exact zero-order-hold discretisation (same bytes moved)."""
+    run = ScanRun(w, device, discretization="zoh")
+    ms = timed(run.step, steps, warmup)
+    del run
+    torch.cuda.empty_cache()
+    hbm, _ = measured_peaks()
+    gbs = w.algorithmic_bytes() / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "discretization": "zoh", "us_per_step": ms * 1e3,
+            "elements_per_s": w.elements / (ms * 1e-3), "hbm_gbs": gbs, "frac_of_hbm": gbs / hbm, "steps": steps}
+
+
 def run_decode(device, steps_graph=3, warmup=1):
     w = wl.DECODE
     run = DecodeRun(w, device)
@@ -457,6 +472,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--profile", choices=["scan", "decode"], default=None,
                     help="run 2 warm-up and 3 profiled launches of one kernel on its workload and exit "
                          "(a small command for ncu; prints no JSON line)")
@@ -524,6 +540,8 @@ def main(argv=None):
                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
     if rank == 0 and not args.no_decode:
         res["decode"] = run_decode(device)
+    if rank == 0 and not args.no_zoh:
+        res["zoh"] = run_zoh(w, device)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w)
     if dist is not None:

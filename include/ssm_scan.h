@@ -60,10 +60,23 @@ typedef enum {
   SSM_ERR_ALIGN = -4,       /* a pointer is not aligned to its element size */
   SSM_ERR_UNSUPPORTED = -5, /* dstate > 16, or a grid dimension would overflow */
   SSM_ERR_LAUNCH = -6,      /* the CUDA launch failed (no device, bad stream, ...) */
-  SSM_ERR_TIMEOUT = -7      /* reserved: a bounded in-kernel wait gave up */
+  SSM_ERR_TIMEOUT = -7,     /* reserved: a bounded in-kernel wait gave up */
+  SSM_ERR_ARG = -8          /* an enumerated argument (discretization) is out of range */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
+
+/*
+ * How B is discretised (A is always Abar = exp(Delta A)).
+ *  SSM_DISC_DELTA_B : Bbar = Delta * B, the form the scan pseudo-code uses (gsyq.cn page,
+ *                     "硬件优化并行扫描算法": B_bar = Δ*B).  The default of every entry point
+ *                     without a discretization argument.
+ *  SSM_DISC_ZOH     : the exact zero-order hold Bbar = (Delta A)^-1 (exp(Delta A) - I) Delta B
+ *                     (gsyq.cn page, "连续到离散的转换"; VMamba notes, section on the dimensions
+ *                     of A, B, C), i.e. (exp(Delta A[d,n]) - 1) / A[d,n] * B[n] for the diagonal
+ *                     A, with its limit Delta * B[n] where A[d,n] = 0.
+ */
+typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization;
 
 /* Version of this ABI (bumped when a signature changes). */
 int ssm_abi_version(void);
@@ -97,6 +110,15 @@ int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void
                     float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, void* stream);
 
 /*
+ * ssm_scan_fwd_h0 with a choice of discretization (an ssm_discretization value; anything
+ * else returns SSM_ERR_ARG).  With SSM_DISC_DELTA_B it is exactly ssm_scan_fwd_h0.
+ */
+int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
+                    void* stream);
+
+/*
  * Single-token decode step, state updated in place.
  *   state          : [batch][dim][dstate] float32, read and written.
  *   x, dt, z, out  : [batch][dim], io dtype.  dt is the raw step size.
@@ -110,6 +132,14 @@ int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void
 int ssm_state_update(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
                      const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
                      int dim, int dstate, int io_dtype, void* stream);
+
+/*
+ * ssm_state_update with a choice of discretization (as ssm_scan_fwd_ex), so that a decode
+ * continues a scan made with the same Bbar.  With SSM_DISC_DELTA_B it is exactly ssm_state_update.
+ */
+int ssm_state_update_ex(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
+                        int dim, int dstate, int io_dtype, int discretization, void* stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_status_string(int status);

@@ -18,6 +18,13 @@ from ._native import SsmError, lib, status_string  # noqa: F401
 __all__ = ["ssm_scan_fwd", "ssm_state_update", "SsmError", "lib", "status_string", "io_dtype_code"]
 
 _IO = {torch.float32: _native.SSM_F32, torch.bfloat16: _native.SSM_BF16}
+_DISC = {"delta_b": _native.SSM_DISC_DELTA_B, "zoh": _native.SSM_DISC_ZOH}
+
+
+def _disc(discretization: str) -> int:
+    if discretization not in _DISC:
+        raise ValueError(f"discretization must be one of {sorted(_DISC)}, got {discretization!r}")
+    return _DISC[discretization]
 
 
 def io_dtype_code(dtype: torch.dtype) -> int:
@@ -47,13 +54,15 @@ def _stream(stream) -> int | None:
 
 
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, y=None, last_state=None,
-                 h0=None, return_last_state=True, stream=None):
-    """Selective scan forward (``ssm_scan_fwd`` / ``ssm_scan_fwd_h0`` of the C-ABI).
+                 h0=None, return_last_state=True, stream=None, discretization="delta_b"):
+    """Selective scan forward (``ssm_scan_fwd`` / ``ssm_scan_fwd_h0`` / ``ssm_scan_fwd_ex`` of the C-ABI).
 
     u, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (float32 or bfloat16, all the same);
     A: [dim, dstate], D, dt_bias: [dim], h0: [batch, dim, dstate] (float32).
+    discretization: "delta_b" (Bbar = Delta B) or "zoh" (exact zero-order hold).
     Returns (y, last_state); y has u's dtype, last_state is float32 (None if not requested).
     """
+    disc = _disc(discretization)
     batch, dim, L = u.shape
     dstate = A.shape[1]
     io = io_dtype_code(u.dtype)
@@ -77,25 +86,31 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus
         _ptr(last_state, torch.float32, (batch, dim, dstate), "last_state"),
         batch, dim, dstate, L, io, _stream(stream),
     ]
-    if h0 is None:
+    h0p = _ptr(h0, torch.float32, (batch, dim, dstate), "h0")
+    if disc != _native.SSM_DISC_DELTA_B:
+        _native.check("ssm_scan_fwd_ex", lib().ssm_scan_fwd_ex(*args, h0p, *tail[:-1], disc, tail[-1]))
+    elif h0 is None:
         _native.check("ssm_scan_fwd", lib().ssm_scan_fwd(*args, *tail))
     else:
-        h0p = _ptr(h0, torch.float32, (batch, dim, dstate), "h0")
         _native.check("ssm_scan_fwd_h0", lib().ssm_scan_fwd_h0(*args, h0p, *tail))
     return y, last_state
 
 
-def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, out=None, stream=None):
-    """One decode step (``ssm_state_update`` of the C-ABI); `state` is updated in place.
+def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, out=None, stream=None,
+                     discretization="delta_b"):
+    """One decode step (``ssm_state_update`` / ``ssm_state_update_ex`` of the C-ABI); `state` is
+    updated in place.
 
     state: [batch, dim, dstate] float32; x, dt, z: [batch, dim]; B, C: [batch, dstate]
-    (float32 or bfloat16); A: [dim, dstate], D, dt_bias: [dim] float32.  Returns out [batch, dim].
+    (float32 or bfloat16); A: [dim, dstate], D, dt_bias: [dim] float32.
+    discretization: "delta_b" or "zoh", as for ssm_scan_fwd.  Returns out [batch, dim].
     """
+    disc = _disc(discretization)
     batch, dim, dstate = state.shape
     io = io_dtype_code(x.dtype)
     if out is None:
         out = torch.empty_like(x)
-    st = lib().ssm_state_update(
+    args = [
         _ptr(state, torch.float32, (batch, dim, dstate), "state"),
         _ptr(x, x.dtype, (batch, dim), "x"),
         _ptr(dt, x.dtype, (batch, dim), "dt"),
@@ -107,7 +122,10 @@ def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_sof
         _ptr(dt_bias, torch.float32, (dim,), "dt_bias"),
         int(bool(dt_softplus)),
         _ptr(out, x.dtype, (batch, dim), "out"),
-        batch, dim, dstate, io, _stream(stream),
-    )
-    _native.check("ssm_state_update", st)
+        batch, dim, dstate, io,
+    ]
+    if disc != _native.SSM_DISC_DELTA_B:
+        _native.check("ssm_state_update_ex", lib().ssm_state_update_ex(*args, disc, _stream(stream)))
+    else:
+        _native.check("ssm_state_update", lib().ssm_state_update(*args, _stream(stream)))
     return out

@@ -19,9 +19,13 @@ SSM_ERR_ALIGN = -4
 SSM_ERR_UNSUPPORTED = -5
 SSM_ERR_LAUNCH = -6
 SSM_ERR_TIMEOUT = -7
+SSM_ERR_ARG = -8
 
 SSM_F32 = 0
 SSM_BF16 = 1
+
+SSM_DISC_DELTA_B = 0
+SSM_DISC_ZOH = 1
 
 # Every symbol the header declares, with its ctypes signature.
 _vp, _fp, _i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
@@ -30,7 +34,9 @@ SIGNATURES = {
     "ssm_status_string": (ctypes.c_char_p, [_i]),
     "ssm_scan_fwd": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _vp, _fp, _i, _i, _i, _i, _i, _vp]),
     "ssm_scan_fwd_h0": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _fp, _i, _i, _i, _i, _i, _vp]),
+    "ssm_scan_fwd_ex": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
     "ssm_state_update": (_i, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _vp, _i, _i, _i, _i, _vp]),
+    "ssm_state_update_ex": (_i, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _vp, _i, _i, _i, _i, _i, _vp]),
 }
 
 _lock = threading.Lock()

@@ -16,7 +16,7 @@ size_t io_size(int io) { return io == SSM_F32 ? 4 : 2; }
 
 extern "C" {
 
-int ssm_abi_version(void) { return 1; }
+int ssm_abi_version(void) { return 2; }
 
 const char* ssm_status_string(int status) {
   switch (status) {
@@ -28,15 +28,18 @@ const char* ssm_status_string(int status) {
     case SSM_ERR_UNSUPPORTED: return "unsupported size (dstate > 16 or grid overflow)";
     case SSM_ERR_LAUNCH: return "the CUDA kernel launch failed";
     case SSM_ERR_TIMEOUT: return "a bounded in-kernel wait gave up";
+    case SSM_ERR_ARG: return "discretization is not an ssm_discretization value";
     default: return "unknown status";
   }
 }
 
-int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
                     const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
-                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, void* stream) {
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
+                    void* stream) {
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
   if (dstate > 16) return SSM_ERR_UNSUPPORTED;
   if (batch == 0 || dim == 0) return SSM_OK;
   if (!A) return SSM_ERR_NULL;
@@ -57,8 +60,16 @@ int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void
   a.batch = batch, a.dim = dim, a.dstate = dstate, a.seqlen = seqlen;
   a.softplus = delta_softplus ? 1 : 0;
   a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  a.zoh = discretization == SSM_DISC_ZOH ? 1 : 0;
   const cudaError_t err = ssm::launch_scan_fwd(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, void* stream) {
+  return ssm_scan_fwd_ex(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, batch, dim, dstate,
+                         seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
 }
 
 int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -68,11 +79,12 @@ int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B
                          seqlen, io_dtype, stream);
 }
 
-int ssm_state_update(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
-                     const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
-                     int dim, int dstate, int io_dtype, void* stream) {
+int ssm_state_update_ex(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
+                        int dim, int dstate, int io_dtype, int discretization, void* stream) {
   if (batch < 0 || dim < 0 || dstate < 1) return SSM_ERR_SHAPE;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
   if (dstate > 16) return SSM_ERR_UNSUPPORTED;
   if (batch == 0 || dim == 0) return SSM_OK;
   if (!state || !x || !dt || !A || !B || !C || !out) return SSM_ERR_NULL;
@@ -91,8 +103,16 @@ int ssm_state_update(float* state, const void* x, const void* dt, const float* A
   a.batch = batch, a.dim = dim, a.dstate = dstate;
   a.softplus = dt_softplus ? 1 : 0;
   a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  a.zoh = discretization == SSM_DISC_ZOH ? 1 : 0;
   const cudaError_t err = ssm::launch_state_update(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_state_update(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
+                     const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
+                     int dim, int dstate, int io_dtype, void* stream) {
+  return ssm_state_update_ex(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, out, batch, dim, dstate, io_dtype,
+                             SSM_DISC_DELTA_B, stream);
 }
 
 }  // extern "C"

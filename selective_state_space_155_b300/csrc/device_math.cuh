@@ -53,6 +53,37 @@ __device__ __forceinline__ float softplus_f32(float x) {
 
 __device__ __forceinline__ float silu_f32(float z) { return z * rcp_approx(1.0f + ex2_approx(-z * kLog2e)); }
 
+// Exact zero-order hold: Bbar = (exp(Delta a) - 1) / a * B for a diagonal A.  This returns the
+// factor Bbar / B from x = Delta*a, abar = exp(x) (already computed by the caller), Delta and
+// inv_a = 1/a.  For |x| >= 1/8 it is (abar - 1) * inv_a, which loses at most a few units in
+// the sixth digit to the rounding of abar.  Below that, abar - 1 would cancel, so it is
+// Delta * (e^x - 1)/x from the Taylor series 1 + x/2 + x^2/6 + ... + x^5/720, whose first
+// omitted term is under 1e-9 relative there; this branch also covers a = 0, where the factor
+// is its limit Delta and inv_a is never used.
+__device__ __forceinline__ float zoh_factor(float x, float abar, float delta, float inv_a) {
+  float p = fmaf(x, 1.0f / 720.0f, 1.0f / 120.0f);
+  p = fmaf(x, p, 1.0f / 24.0f);
+  p = fmaf(x, p, 1.0f / 6.0f);
+  p = fmaf(x, p, 0.5f);
+  p = fmaf(x, p, 1.0f);
+  return fabsf(x) < 0.125f ? delta * p : (abar - 1.0f) * inv_a;
+}
+
+// zoh_factor on a pair of states with packed arithmetic.
+__device__ __forceinline__ float2 zoh_factor2(float2 x, float2 abar, float2 delta, float2 inv_a) {
+  float2 p = __ffma2_rn(x, make_float2(1.0f / 720.0f, 1.0f / 720.0f), make_float2(1.0f / 120.0f, 1.0f / 120.0f));
+  p = __ffma2_rn(x, p, make_float2(1.0f / 24.0f, 1.0f / 24.0f));
+  p = __ffma2_rn(x, p, make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+  p = __ffma2_rn(x, p, make_float2(0.5f, 0.5f));
+  p = __ffma2_rn(x, p, make_float2(1.0f, 1.0f));
+  p = __fmul2_rn(p, delta);
+  const float2 q = __fmul2_rn(__fadd2_rn(abar, make_float2(-1.0f, -1.0f)), inv_a);
+  return make_float2(fabsf(x.x) < 0.125f ? p.x : q.x, fabsf(x.y) < 0.125f ? p.y : q.y);
+}
+
+// 1/a for the zero-order-hold factor (0 where a = 0: that state always takes the series branch).
+__device__ __forceinline__ float zoh_inv(float a) { return a != 0.0f ? 1.0f / a : 0.0f; }
+
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
 template <>

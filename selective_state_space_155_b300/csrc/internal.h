@@ -23,6 +23,7 @@ struct ScanArgs {
   int batch, dim, dstate, seqlen;
   int softplus;
   int io;
+  int zoh;  // exact zero-order-hold Bbar instead of Delta * B
 };
 
 // Arguments of one decode step; pointer and layout meaning as in ssm_scan.h.
@@ -40,11 +41,13 @@ struct UpdateArgs {
   int batch, dim, dstate;
   int softplus;
   int io;
+  int zoh;  // exact zero-order-hold Bbar instead of Delta * B
 };
 
 // Enqueue the scan on `stream`.  Arguments are already validated.  Picks the lane-per-channel
 // form when there are enough channels to give every SM eight or more of its warps, otherwise the
-// four-lanes-per-channel form; SSM_SCAN_VARIANT=lane|quad in the environment forces one.
+// four-lanes-per-channel form; SSM_SCAN_VARIANT=lane|quad in the environment forces one.  The
+// zero-order-hold discretization always runs the four-lanes-per-channel form.
 cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream);
 
 // The four-lanes-per-channel form (scan_fwd.cu).

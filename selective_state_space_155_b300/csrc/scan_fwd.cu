@@ -3,6 +3,7 @@
 // What it computes (per batch row b, channel d, state n; sources cited in ssm_scan.h):
 //   Delta_t = softplus(delta_t + dt_bias[d]);  Abar = exp(Delta_t A[d,n]);  h_t = Abar h_{t-1} + Delta_t B_t[n] u_t
 //   y_t = sum_n C_t[n] h_t[n] + D[d] u_t;  out_t = y_t * silu(z_t);  last_state = h_{L-1}
+// or, with the exact zero-order hold (ZOH), Delta_t B_t[n] replaced by (Abar - 1) / A[d,n] B_t[n].
 //
 // Why it looks like this.  On B300 the scan is not HBM-bound in practice: per element it needs 16
 // MUFU ex2, ~64 FP32 lane-operations and a cross-lane readout, and a straightforward kernel spends
@@ -173,7 +174,7 @@ __device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) 
   }
 }
 
-template <typename T, int NPAD, bool VEC>
+template <typename T, int NPAD, bool VEC, bool ZOH>
 __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const ScanArgs a) {
   using Cfg = ScanCfg<T, NPAD>;
   constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, RS = Cfg::RS, VPR = Cfg::VPR;
@@ -349,7 +350,9 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
             dl.x = t < lim ? dl.x : 0.0f;
             dl.y = t + 1 < lim ? dl.y : 0.0f;
           }
-          const float2 du = __fmul2_rn(dl, uu);
+          // the recurrence's input factor: Delta*u, or u alone for the zero-order hold (whose
+          // Bbar factor needs Delta and A together and is formed in the recurrence)
+          const float2 du = ZOH ? uu : __fmul2_rn(dl, uu);
           const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
           const float2 sg = has_z ? f2(silu_f32(zz.x), silu_f32(zz.y)) : f2(1.0f, 1.0f);
           Ps[ps_ofs + o * PSS] = f2(dl.x, du.x);
@@ -382,17 +385,20 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   const int d = d0 + cl;
   const bool ch_ok = d < a.dim;
 
-  float2 A01, A23, h01, h23;
+  float2 A01, A23, h01, h23, iA01, iA23;
   {
-    float Av[4], hv[4];
+    float Av[4], hv[4], iv[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int n = 4 * g + i;
       const bool ok = ch_ok && n < N;
-      Av[i] = ok ? a.A[size_t(d) * N + n] * kLog2e : 0.0f;
+      const float av = ok ? a.A[size_t(d) * N + n] : 0.0f;
+      Av[i] = av * kLog2e;
+      iv[i] = zoh_inv(av);
       hv[i] = (ok && a.h0) ? a.h0[(size_t(b) * a.dim + d) * N + n] : 0.0f;
     }
     A01 = f2(Av[0], Av[1]), A23 = f2(Av[2], Av[3]);
+    iA01 = f2(iv[0], iv[1]), iA23 = f2(iv[2], iv[3]);
     h01 = f2(hv[0], hv[1]), h23 = f2(hv[2], hv[3]);
   }
   T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L;
@@ -419,8 +425,17 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
         const float2 g01 = __fmul2_rn(dd, A01), g23 = __fmul2_rn(dd, A23);
         const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y));
         const float2 a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
-        h01 = __ffma2_rn(a01, h01, __fmul2_rn(uu, f2(bb.x, bb.y)));
-        h23 = __ffma2_rn(a23, h23, __fmul2_rn(uu, f2(bb.z, bb.w)));
+        if constexpr (ZOH) {
+          // p.y is u here; Bbar*u = zoh_factor(Delta*A) * u * B
+          const float2 ln2 = f2(kLn2, kLn2);
+          const float2 c01 = zoh_factor2(__fmul2_rn(g01, ln2), a01, dd, iA01);
+          const float2 c23 = zoh_factor2(__fmul2_rn(g23, ln2), a23, dd, iA23);
+          h01 = __ffma2_rn(a01, h01, __fmul2_rn(c01, __fmul2_rn(uu, f2(bb.x, bb.y))));
+          h23 = __ffma2_rn(a23, h23, __fmul2_rn(c23, __fmul2_rn(uu, f2(bb.z, bb.w))));
+        } else {
+          h01 = __ffma2_rn(a01, h01, __fmul2_rn(uu, f2(bb.x, bb.y)));
+          h23 = __ffma2_rn(a23, h23, __fmul2_rn(uu, f2(bb.z, bb.w)));
+        }
         acc[j] = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
       }
       // sums over the R lanes of the channel and the pair halves; lane (g, cw) finishes the OPL
@@ -477,10 +492,10 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   }
 }
 
-template <typename T, int NPAD, bool VEC>
+template <typename T, int NPAD, bool VEC, bool ZOH>
 cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   using Cfg = ScanCfg<T, NPAD>;
-  auto kernel = scan_fwd_kernel<T, NPAD, VEC>;
+  auto kernel = scan_fwd_kernel<T, NPAD, VEC, ZOH>;
   // The dynamic shared-memory opt-in is a per-device function attribute; set it once per device.
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -509,11 +524,16 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
                           Cfg::kSmem, stream);
 }
 
-template <typename T, bool VEC>
+template <typename T, bool VEC, bool ZOH>
 cudaError_t dispatch_npad(const ScanArgs& a, cudaStream_t stream) {
-  if (a.dstate <= 4) return launch_cfg<T, 4, VEC>(a, stream);
-  if (a.dstate <= 8) return launch_cfg<T, 8, VEC>(a, stream);
-  return launch_cfg<T, 16, VEC>(a, stream);
+  if (a.dstate <= 4) return launch_cfg<T, 4, VEC, ZOH>(a, stream);
+  if (a.dstate <= 8) return launch_cfg<T, 8, VEC, ZOH>(a, stream);
+  return launch_cfg<T, 16, VEC, ZOH>(a, stream);
+}
+
+template <typename T, bool VEC>
+cudaError_t dispatch_disc(const ScanArgs& a, cudaStream_t stream) {
+  return a.zoh ? dispatch_npad<T, VEC, true>(a, stream) : dispatch_npad<T, VEC, false>(a, stream);
 }
 
 template <typename T>
@@ -539,8 +559,8 @@ int sm_count() {
 
 cudaError_t launch_scan_fwd_quad(const ScanArgs& a, bool vec, cudaStream_t stream) {
   if (a.io == kF32)
-    return vec ? dispatch_npad<float, true>(a, stream) : dispatch_npad<float, false>(a, stream);
-  return vec ? dispatch_npad<__nv_bfloat16, true>(a, stream) : dispatch_npad<__nv_bfloat16, false>(a, stream);
+    return vec ? dispatch_disc<float, true>(a, stream) : dispatch_disc<float, false>(a, stream);
+  return vec ? dispatch_disc<__nv_bfloat16, true>(a, stream) : dispatch_disc<__nv_bfloat16, false>(a, stream);
 }
 
 cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
@@ -557,7 +577,7 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
     const long long warps = ((long long)a.batch * a.dim + 31) / 32;
     lane = warps >= 8LL * sm_count();
   }
-  return lane ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);
+  return (lane && !a.zoh) ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);
 }
 
 }  // namespace ssm

@@ -2,6 +2,7 @@
 //
 // One step of the recurrence on a stored float32 state, in place:
 //   Delta = softplus(dt + dt_bias[d]);  s[n] <- exp(Delta A[d,n]) s[n] + Delta B[n] x
+//   (or, with the exact zero-order hold, (exp(Delta A[d,n]) - 1) / A[d,n] B[n] x in place of Delta B[n] x)
 //   y = sum_n C[n] s[n] + D[d] x;  out = y * silu(z)
 // (constant-memory inference from the previous state and the current input only).
 //
@@ -96,13 +97,27 @@ __global__ void __launch_bounds__(kBlock) state_update_kernel(const UpdateArgs a
   const float step = a.softplus ? softplus_f32(r) : r;
   const float2 dd = f2(step * kLog2e, step * kLog2e), dx = f2(step * x, step * x);
   float2 acc = f2(0.0f, 0.0f);
+  if (a.zoh) {
+    const float2 sd = f2(step, step), xx = f2(x, x);
 #pragma unroll
-  for (int i = 0; i < NPAD; i += 2) {
-    const float2 g = __fmul2_rn(dd, f2(Av[i], Av[i + 1]));
-    const float2 ab = f2(ex2_approx(g.x), ex2_approx(g.y));
-    const float2 sn = __ffma2_rn(ab, f2(s[i], s[i + 1]), __fmul2_rn(dx, f2(Bv[i], Bv[i + 1])));
-    s[i] = sn.x, s[i + 1] = sn.y;
-    acc = __ffma2_rn(f2(Cv[i], Cv[i + 1]), sn, acc);
+    for (int i = 0; i < NPAD; i += 2) {
+      const float2 Ai = f2(Av[i], Av[i + 1]);
+      const float2 g = __fmul2_rn(dd, Ai);
+      const float2 ab = f2(ex2_approx(g.x), ex2_approx(g.y));
+      const float2 c = zoh_factor2(__fmul2_rn(sd, Ai), ab, sd, f2(zoh_inv(Ai.x), zoh_inv(Ai.y)));
+      const float2 sn = __ffma2_rn(ab, f2(s[i], s[i + 1]), __fmul2_rn(c, __fmul2_rn(xx, f2(Bv[i], Bv[i + 1]))));
+      s[i] = sn.x, s[i + 1] = sn.y;
+      acc = __ffma2_rn(f2(Cv[i], Cv[i + 1]), sn, acc);
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < NPAD; i += 2) {
+      const float2 g = __fmul2_rn(dd, f2(Av[i], Av[i + 1]));
+      const float2 ab = f2(ex2_approx(g.x), ex2_approx(g.y));
+      const float2 sn = __ffma2_rn(ab, f2(s[i], s[i + 1]), __fmul2_rn(dx, f2(Bv[i], Bv[i + 1])));
+      s[i] = sn.x, s[i + 1] = sn.y;
+      acc = __ffma2_rn(f2(Cv[i], Cv[i + 1]), sn, acc);
+    }
   }
   float y = fmaf(Dd, x, acc.x + acc.y);
   if (a.z) y *= silu_f32(zz);

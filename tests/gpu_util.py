@@ -28,10 +28,10 @@ def assert_close(got, ref, tol, what):
     return err
 
 
-def oracle_scan(inp, softplus=True, h0=None):
+def oracle_scan(inp, softplus=True, h0=None, zoh=False):
     f = wl.to_f64
     return oracle.scan(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), f(inp.get("D")),
-                       f(inp.get("z")), f(inp.get("dt_bias")), delta_softplus=softplus, h0=f(h0))
+                       f(inp.get("z")), f(inp.get("dt_bias")), delta_softplus=softplus, h0=f(h0), zoh=zoh)
 
 
 def to_device(inp, dev):

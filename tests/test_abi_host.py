@@ -30,7 +30,8 @@ def declared_functions():
 
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
-        ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_state_update", "ssm_status_string"])
+        ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_scan_fwd_ex", "ssm_state_update",
+         "ssm_state_update_ex", "ssm_status_string"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -40,8 +41,8 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.ssm_abi_version() == 1
-    for code in range(-7, 1):
+    assert lib.ssm_abi_version() == 2
+    for code in range(-8, 1):
         s = lib.ssm_status_string(code).decode()
         assert s and s != "unknown status"
     assert lib.ssm_status_string(42).decode() == "unknown status"
@@ -91,6 +92,22 @@ def test_scan_h0_validation(lib):
     assert lib.ssm_scan_fwd_h0(*h0_args) == _native.SSM_ERR_NULL
 
 
+@pytest.mark.parametrize("disc,expected", [(0, _native.SSM_OK), (1, _native.SSM_OK), (2, _native.SSM_ERR_ARG),
+                                            (-1, _native.SSM_ERR_ARG)])
+def test_scan_ex_discretization_validation(lib, disc, expected):
+    # batch 0 makes a valid call return before any launch
+    args = scan_args(batch=0)
+    ex_args = args[:9] + [None] + args[9:16] + [disc] + args[16:]
+    assert lib.ssm_scan_fwd_ex(*ex_args) == expected
+
+
+def test_scan_ex_validates_like_h0(lib):
+    args = scan_args(u=None)
+    assert lib.ssm_scan_fwd_ex(*(args[:9] + [None] + args[9:16] + [1] + args[16:])) == _native.SSM_ERR_NULL
+    args = scan_args()
+    assert lib.ssm_scan_fwd_ex(*(args[:9] + [P + 2] + args[9:16] + [1] + args[16:])) == _native.SSM_ERR_ALIGN
+
+
 def update_args(**over):
     a = dict(state=P, x=P, dt=P, A=P, B=P, C=P, D=P, z=P, dt_bias=P, softplus=1, out=P, batch=2, dim=3, dstate=16,
              io=_native.SSM_BF16, stream=None)
@@ -115,6 +132,14 @@ def update_args(**over):
 ])
 def test_update_validation(lib, over, expected):
     assert lib.ssm_state_update(*update_args(**over)) == expected
+    args = update_args(**over)
+    assert lib.ssm_state_update_ex(*(args[:-1] + [1] + args[-1:])) == expected
+
+
+@pytest.mark.parametrize("disc,expected", [(0, _native.SSM_OK), (1, _native.SSM_OK), (5, _native.SSM_ERR_ARG)])
+def test_update_ex_discretization_validation(lib, disc, expected):
+    args = update_args(batch=0)
+    assert lib.ssm_state_update_ex(*(args[:-1] + [disc] + args[-1:])) == expected
 
 
 def test_binding_rejects_cpu_tensors():
