@@ -21,6 +21,9 @@ Parity status per function (what pins it, see tests/test_oracle_pins.py):
   state_update    pinned: equals the pinned scan step by step; exact halving case.
   assoc_scan      pinned: prefix-sum worked example; equals the closed-form products.
   scan_tree       pinned: equals the sequential scan (associativity).
+  causal_conv1d   pinned: numpy's full convolution (first L outputs), torch's grouped Conv1d with
+                  padding W-1 as the gsyq.cn sketch writes it, streaming in two pieces, impulse
+                  response, silu special values.
 """
 from __future__ import annotations
 
@@ -74,6 +77,8 @@ def _load():
             lib.oracle_assoc_scan_pairs_f64.argtypes = [_DP] * 4 + [ctypes.c_int]
             lib.oracle_scan_tree_f64.restype = ctypes.c_int
             lib.oracle_scan_tree_f64.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP] + [ctypes.c_int] * 4
+            lib.oracle_causal_conv1d_f64.restype = ctypes.c_int
+            lib.oracle_causal_conv1d_f64.argtypes = [_DP] * 6 + [ctypes.c_int] * 5
             lib.oracle_softplus_f64.restype = ctypes.c_double
             lib.oracle_softplus_f64.argtypes = [ctypes.c_double]
             lib.oracle_silu_f64.restype = ctypes.c_double
@@ -175,6 +180,26 @@ def scan_tree(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=Tr
     if rc != 0:
         raise RuntimeError(f"oracle_scan_tree_f64 failed: {rc}")
     return y, last
+
+
+def causal_conv1d(x, weight, bias=None, state_in=None, silu=True):
+    """Causal depthwise conv1d.  x [batch,dim,L], weight [dim,W], bias [dim], state_in
+    [batch,dim,W-1] (the inputs before t = 0, oldest first).  Returns (out [batch,dim,L],
+    state_out [batch,dim,W-1])."""
+    x = _f64(x)
+    batch, dim, seqlen = x.shape
+    weight = _f64(weight)
+    width = weight.shape[1]
+    weight = _f64(weight, (dim, width))
+    bias = _f64(bias, (dim,))
+    state_in = _f64(state_in, (batch, dim, width - 1))
+    out = np.zeros((batch, dim, seqlen), dtype=np.float64)
+    st = np.zeros((batch, dim, width - 1), dtype=np.float64)
+    rc = _load().oracle_causal_conv1d_f64(_ptr(x), _ptr(weight), _ptr(bias), _ptr(state_in), _ptr(out), _ptr(st),
+                                          batch, dim, seqlen, width, int(bool(silu)))
+    if rc != 0:
+        raise RuntimeError(f"oracle_causal_conv1d_f64 failed: {rc}")
+    return out, st
 
 
 def softplus(x: float) -> float:

@@ -40,6 +40,16 @@
  *   Decode step    the same single recurrence step applied to a stored state
  *                  (constant-memory inference: gsyq.cn page, complexity table
  *                  row "推理内存 O(d) 状态向量").
+ *   Causal conv    depthwise causal convolution of width W over time, one
+ *                  filter per channel, before the scan:
+ *                    out_t = act(bias[d] + sum_k w[d,k] * x_{t-(W-1)+k}),
+ *                  inputs before t = 0 taken from a carried state of the W-1
+ *                  previous inputs (zeros when not given), act = silu or none.
+ *                  gsyq.cn page, SelectiveSSM sketch ("卷积预处理":
+ *                  Conv1d(d_model, d_model, d_conv, padding=d_conv-1,
+ *                  groups=d_model), whose first L outputs are the causal
+ *                  ones); datacamp tutorial, install notes (the causal-conv1d
+ *                  layer used inside the Mamba block).
  *   Associative    the pair operator (a1,b1) o (a2,b2) = (a1*a2, a2*b1 + b2)
  *   scan           evaluated in tree order (53ai.com Mamba article, section
  *                  3.3 "Parallel Associative Scan": grouping does not change a
@@ -223,6 +233,39 @@ int oracle_scan_tree_f64(const double* u, const double* delta, const double* A, 
   free(bx);
   free(pa);
   free(h);
+  return 0;
+}
+
+/*
+ * Causal depthwise conv1d of width W over [batch][dim][seqlen] inputs.  state_in holds, per
+ * (batch, channel), the W-1 inputs that precede t = 0 (oldest first; NULL = zeros);
+ * state_out receives the W-1 last inputs of concat(state_in, x) (NULL = not written).
+ * weight [dim][W], bias [dim] (NULL = 0); silu non-zero applies silu to each output.
+ */
+int oracle_causal_conv1d_f64(const double* x, const double* weight, const double* bias, const double* state_in,
+                             double* out, double* state_out, int batch, int dim, int seqlen, int width, int silu) {
+  if (!x || !weight || !out) return -1;
+  if (batch < 0 || dim < 0 || seqlen < 0 || width < 1) return -2;
+  int hw = width - 1;
+  for (long ch = 0; ch < (long)batch * dim; ++ch) {
+    int d = (int)(ch % dim);
+    const double* xr = x + ch * seqlen;
+    const double* sr = state_in ? state_in + ch * hw : NULL;
+    for (int t = 0; t < seqlen; ++t) {
+      double acc = bias ? bias[d] : 0.0;
+      for (int k = 0; k < width; ++k) {
+        int s = t - hw + k; /* input time index */
+        double v = s >= 0 ? xr[s] : (sr ? sr[hw + s] : 0.0);
+        acc += weight[(long)d * width + k] * v;
+      }
+      out[ch * seqlen + t] = silu ? silu_f64(acc) : acc;
+    }
+    if (state_out)
+      for (int j = 0; j < hw; ++j) {
+        int s = seqlen - hw + j; /* time index of state slot j */
+        state_out[ch * hw + j] = s >= 0 ? xr[s] : (sr ? sr[hw + s] : 0.0);
+      }
+  }
   return 0;
 }
 

@@ -36,6 +36,10 @@ MUTANTS = {
     "pair_combine_swapped": ("out_b[i] = ra * lb + rb;", "out_b[i] = la * rb + lb;"),
     "decode_no_state_decay": ("*s = abar * *s + bbar_factor(step, a, zoh) * B[(long)b * dstate + n] * x[ch];",
                               "*s = *s + bbar_factor(step, a, zoh) * B[(long)b * dstate + n] * x[ch];"),
+    "conv_taps_reversed": ("acc += weight[(long)d * width + k] * v;", "acc += weight[(long)d * width + (width - 1 - k)] * v;"),
+    "conv_off_by_one": ("int s = t - hw + k; /* input time index */", "int s = t - hw + k - 1; /* input time index */"),
+    "conv_state_ignored": ("double v = s >= 0 ? xr[s] : (sr ? sr[hw + s] : 0.0);", "double v = s >= 0 ? xr[s] : 0.0;"),
+    "conv_no_bias": ("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
     "h0_ignored": ("h[n] = h0 ? h0[ch * dstate + n] : 0.0;", "h[n] = 0.0;"),
 }
 

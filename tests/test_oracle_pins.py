@@ -410,3 +410,64 @@ def test_zoh_decode_steps_equal_scan():
                                      dt_bias=bias, zoh=True)
         np.testing.assert_array_equal(out, y[:, :, t])
     np.testing.assert_array_equal(s, last)
+
+
+# ---------------------------------------------------------------------------------------------
+# Causal depthwise conv1d before the scan: gsyq.cn page, SelectiveSSM sketch ("卷积预处理",
+# Conv1d(d_model, d_model, d_conv, padding=d_conv-1, groups=d_model)); datacamp tutorial,
+# install notes (the causal-conv1d layer inside the Mamba block).
+# ---------------------------------------------------------------------------------------------
+def _conv_case(seed, batch=2, dim=5, L=23, W=4):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((batch, dim, L)), rng.standard_normal((dim, W)), rng.standard_normal(dim))
+
+
+def test_conv_equals_numpy_full_convolution():
+    """Each output is numpy's full convolution of the row with the channel's filter (flipped,
+    since np.convolve flips its second argument), first L outputs, plus the bias."""
+    x, w, bias = _conv_case(1)
+    out, _ = oracle.causal_conv1d(x, w, bias, silu=False)
+    for b in range(x.shape[0]):
+        for d in range(x.shape[1]):
+            ref = np.convolve(x[b, d], w[d][::-1])[: x.shape[2]] + bias[d]
+            np.testing.assert_allclose(out[b, d], ref, rtol=1e-13, atol=1e-13)
+
+
+def test_conv_equals_torch_grouped_conv1d_as_the_sketch_writes_it():
+    """torch.nn.functional.conv1d with groups = channels and padding W-1 (the sketch's layer);
+    its first L outputs are the causal ones.  Then silu."""
+    import torch
+    x, w, bias = _conv_case(2, batch=3, dim=6, L=31, W=4)
+    out, _ = oracle.causal_conv1d(x, w, bias, silu=True)
+    xt = torch.from_numpy(x)
+    ref = torch.nn.functional.conv1d(xt, torch.from_numpy(w)[:, None, :], torch.from_numpy(bias), padding=3,
+                                     groups=6)[..., :31]
+    ref = torch.nn.functional.silu(ref).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-12, atol=1e-13)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3, 4])
+def test_conv_streaming_in_two_pieces(W):
+    """conv(L1) then conv(L2) carrying the W-1 last inputs equals conv(L1 + L2); the carried
+    state is the last W-1 inputs."""
+    x, w, bias = _conv_case(3, L=40, W=W)
+    full, st_full = oracle.causal_conv1d(x, w, bias)
+    o1, s1 = oracle.causal_conv1d(x[..., :17], w, bias)
+    o2, s2 = oracle.causal_conv1d(x[..., 17:], w, bias, state_in=s1)
+    np.testing.assert_array_equal(np.concatenate([o1, o2], axis=-1), full)
+    np.testing.assert_array_equal(s2, st_full)
+    np.testing.assert_array_equal(st_full, x[..., 40 - (W - 1):])
+
+
+def test_conv_impulse_response_and_short_rows():
+    """A unit impulse at t = 0 returns the filter taps in reverse order of k (out_t = w[W-1-t]);
+    with a row shorter than W-1 the carried state mixes the old state and the row."""
+    w = np.array([[0.5, -1.0, 2.0, 3.0]])
+    x = np.zeros((1, 1, 6))
+    x[0, 0, 0] = 1.0
+    out, _ = oracle.causal_conv1d(x, w, None, silu=False)
+    np.testing.assert_array_equal(out.ravel(), [3.0, 2.0, -1.0, 0.5, 0.0, 0.0])
+    st_in = np.array([[[7.0, 8.0, 9.0]]])
+    out, st = oracle.causal_conv1d(np.array([[[1.0]]]), w, None, state_in=st_in, silu=False)
+    assert out.ravel()[0] == 0.5 * 7.0 - 1.0 * 8.0 + 2.0 * 9.0 + 3.0 * 1.0
+    np.testing.assert_array_equal(st.ravel(), [8.0, 9.0, 1.0])
