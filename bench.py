@@ -19,6 +19,7 @@ Extra objects on the line:
   decode        the decode workload (batch 256, d_inner 5120, d_state 16): 1024 in-place steps
                 captured in one CUDA graph, and one step after an L2 flush;
   zoh           the same scan workload with the exact zero-order-hold discretisation;
+  conv1d        the causal conv1d (width 4, silu) that produces u, on the same activation shape;
   clocks        SM clocks and throttle reasons sampled (NVML) during the timed region.
 
 Under torchrun each rank runs the same workload on its own GPU with no collective on the data
@@ -410,6 +411,31 @@ def run_zoh(w: wl.ScanWorkload, device, steps=200, warmup=5):
             "elements_per_s": w.elements / (ms * 1e-3), "hbm_gbs": gbs, "frac_of_hbm": gbs / hbm, "steps": steps}
 
 
+def run_conv(w: wl.ScanWorkload, device, steps=300, warmup=5, copies=ROTATING_COPIES):
+    """The causal conv1d (width 4, silu) that produces the scan's u, on the scan workload's
+    activation shape; rotating copies keep each launch reading from HBM."""
+    import selective_state_space_155_b300 as ssm
+    width = 4
+    base = wl.conv_inputs(w.batch, w.dim, w.seqlen, width, w.io, seed=w.seed)
+    sets = [{k: (v.to(device) if v is not None else None) for k, v in base.items()} for _ in range(copies)]
+    outs = [torch.empty_like(sets[0]["x"]) for _ in range(copies)]
+
+    def step(i):
+        k = i % copies
+        ssm.causal_conv1d_fwd(sets[k]["x"], sets[k]["weight"], sets[k]["bias"], silu=True, out=outs[k])
+
+    ms = timed(step, steps, warmup)
+    hbm, _ = measured_peaks()
+    es = sets[0]["x"].element_size()
+    nbytes = 2 * w.elements * es + w.dim * (width + 1) * 4  # x read, out written, weight + bias
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    del sets, outs
+    torch.cuda.empty_cache()
+    return {"workload": f"conv1d_{w.io}_b{w.batch}_d{w.dim}_l{w.seqlen}_w{width}_silu", "us_per_step": ms * 1e3,
+            "elements_per_s": w.elements / (ms * 1e-3), "algorithmic_bytes_per_launch": nbytes, "hbm_gbs": gbs,
+            "frac_of_hbm": gbs / hbm, "steps": steps, "kernel": "conv_vec_kernel"}
+
+
 def run_decode(device, steps_graph=3, warmup=1):
     w = wl.DECODE
     run = DecodeRun(w, device)
@@ -444,14 +470,25 @@ def run_decode(device, steps_graph=3, warmup=1):
 
 
 def profile_mode(which: str) -> int:
-    """A few launches of one kernel for an ncu capture: the mid-size scan (about 0.6 GB on the
-    device) or decode steps of the decode workload without a graph (about 0.2 GB)."""
+    """A few launches of one kernel for an ncu capture: the mid-size scan with either
+    discretisation (about 0.6 GB on the device), the causal conv1d on the same activation shape
+    (about 0.1 GB), or decode steps of the decode workload without a graph (about 0.2 GB)."""
     from selective_state_space_155_b300 import build as _build
     _build.build()
     device = torch.device("cuda", 0)
     if which == "scan":
         run = ScanRun(wl.MID, device, copies=1)
         fn = run.step
+    elif which == "zoh":
+        run = ScanRun(wl.MID, device, copies=1, discretization="zoh")
+        fn = run.step
+    elif which == "conv":
+        import selective_state_space_155_b300 as ssm
+        w = wl.MID
+        c = {k: (v.to(device) if v is not None else None)
+             for k, v in wl.conv_inputs(w.batch, w.dim, w.seqlen, 4, w.io, seed=w.seed).items()}
+        out = torch.empty_like(c["x"])
+        fn = lambda i: ssm.causal_conv1d_fwd(c["x"], c["weight"], c["bias"], silu=True, out=out)
     else:
         import dataclasses
         run = DecodeRun(dataclasses.replace(wl.DECODE, steps=5), device)
@@ -473,7 +510,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-zoh", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "decode"], default=None,
+    ap.add_argument("--no-conv", action="store_true")
+    ap.add_argument("--profile", choices=["scan", "zoh", "conv", "decode"], default=None,
                     help="run 2 warm-up and 3 profiled launches of one kernel on its workload and exit "
                          "(a small command for ncu; prints no JSON line)")
     args = ap.parse_args(argv)
@@ -542,6 +580,8 @@ def main(argv=None):
         res["decode"] = run_decode(device)
     if rank == 0 and not args.no_zoh:
         res["zoh"] = run_zoh(w, device)
+    if rank == 0 and not args.no_conv:
+        res["conv1d"] = run_conv(w, device)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w)
     if dist is not None:

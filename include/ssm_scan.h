@@ -25,6 +25,10 @@
  *                    row "推理内存 O(d) 状态向量"; 53ai.com Mamba article, §1 on
  *                    RNN-style inference from the previous hidden state only).
  *
+ *  ssm_causal_conv1d_fwd / ssm_causal_conv1d_update
+ *                    The depthwise causal convolution that produces the scan's
+ *                    input, over whole rows and as a decode step.
+ *
  * Conventions shared by every entry point
  *  - Every pointer is a DEVICE pointer owned by the caller.  The library never
  *    allocates, never frees and keeps no global state between calls.
@@ -61,7 +65,7 @@ typedef enum {
   SSM_ERR_UNSUPPORTED = -5, /* dstate > 16, or a grid dimension would overflow */
   SSM_ERR_LAUNCH = -6,      /* the CUDA launch failed (no device, bad stream, ...) */
   SSM_ERR_TIMEOUT = -7,     /* reserved: a bounded in-kernel wait gave up */
-  SSM_ERR_ARG = -8          /* an enumerated argument (discretization) is out of range */
+  SSM_ERR_ARG = -8          /* an enumerated argument is out of range, or buffers alias that must not */
 } ssm_status;
 
 typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
@@ -140,6 +144,38 @@ int ssm_state_update(float* state, const void* x, const void* dt, const float* A
 int ssm_state_update_ex(float* state, const void* x, const void* dt, const float* A, const void* B, const void* C,
                         const float* D, const void* z, const float* dt_bias, int dt_softplus, void* out, int batch,
                         int dim, int dstate, int io_dtype, int discretization, void* stream);
+
+/*
+ * Causal depthwise conv1d, the step of the Mamba block that produces the scan's input u
+ * (gsyq.cn page, SelectiveSSM sketch "卷积预处理": Conv1d(d_model, d_model, d_conv,
+ * padding=d_conv-1, groups=d_model), of which the first L outputs are the causal ones;
+ * datacamp tutorial, the causal-conv1d layer used inside the Mamba block).  For every
+ * batch row b, channel d and step t, with W = width:
+ *     out_t = act(bias[d] + sum_{k<W} weight[d,k] * x_{t-(W-1)+k}),  act = silu or identity
+ * where the inputs before t = 0 are state_in (zeros when NULL).
+ *   x, out             : [batch][dim][seqlen], io dtype (out must not alias x).
+ *   weight             : [dim][width] float32.  bias : [dim] float32 (nullable).
+ *   state_in           : [batch][dim][width-1], io dtype, the width-1 inputs before t = 0,
+ *                        oldest first (nullable = zeros).
+ *   state_out          : [batch][dim][width-1], io dtype, receives the width-1 last inputs of
+ *                        concat(state_in, x) (nullable = not written; must not alias state_in).
+ *                        Two calls carrying it equal one call over the concatenated rows.
+ *   width              : 1..4 (SSM_ERR_UNSUPPORTED otherwise).  silu : non-zero applies silu.
+ * Aliasing out/x or state_out/state_in returns SSM_ERR_ARG.  Returns an ssm_status.
+ */
+int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias, const void* state_in, void* out,
+                          void* state_out, int batch, int dim, int seqlen, int width, int silu, int io_dtype,
+                          void* stream);
+
+/*
+ * One decode step of the causal conv1d: out = act(bias + sum_{k<W-1} weight[d,k] state[k]
+ * + weight[d,W-1] x), then state <- (state[1..W-2], x), in place.
+ *   state : [batch][dim][width-1], io dtype (may be NULL when width == 1).
+ *   x, out: [batch][dim], io dtype.  weight, bias: as ssm_causal_conv1d_fwd.
+ * Returns an ssm_status.
+ */
+int ssm_causal_conv1d_update(void* state, const void* x, const float* weight, const float* bias, void* out,
+                             int batch, int dim, int width, int silu, int io_dtype, void* stream);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_status_string(int status);

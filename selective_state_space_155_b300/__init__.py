@@ -5,8 +5,10 @@ torch CUDA tensors into device pointers and the current stream, then call the li
 (``libssm_scan.so``), which runs every step of the path in its own kernels.  PyTorch
 provides device memory and streams; nothing is computed in Python.
 
+    u, conv_state = causal_conv1d_fwd(x, conv_weight, conv_bias, silu=True, return_state=True)
     y, last_state = ssm_scan_fwd(u, delta, A, B, C, D, z, dt_bias, delta_softplus=True)
-    out = ssm_state_update(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus=True)
+    u_t = causal_conv1d_update(conv_state, x_t, conv_weight, conv_bias)
+    out = ssm_state_update(state, u_t, dt, A, B, C, D, z, dt_bias, dt_softplus=True)
 """
 from __future__ import annotations
 
@@ -15,7 +17,8 @@ import torch
 from . import _native
 from ._native import SsmError, lib, status_string  # noqa: F401
 
-__all__ = ["ssm_scan_fwd", "ssm_state_update", "SsmError", "lib", "status_string", "io_dtype_code"]
+__all__ = ["ssm_scan_fwd", "ssm_state_update", "causal_conv1d_fwd", "causal_conv1d_update", "SsmError", "lib",
+           "status_string", "io_dtype_code"]
 
 _IO = {torch.float32: _native.SSM_F32, torch.bfloat16: _native.SSM_BF16}
 _DISC = {"delta_b": _native.SSM_DISC_DELTA_B, "zoh": _native.SSM_DISC_ZOH}
@@ -128,4 +131,52 @@ def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_sof
         _native.check("ssm_state_update_ex", lib().ssm_state_update_ex(*args, disc, _stream(stream)))
     else:
         _native.check("ssm_state_update", lib().ssm_state_update(*args, _stream(stream)))
+    return out
+
+
+def causal_conv1d_fwd(x, weight, bias=None, state_in=None, silu=True, out=None, state_out=None, return_state=False,
+                      stream=None):
+    """Causal depthwise conv1d (``ssm_causal_conv1d_fwd`` of the C-ABI).
+
+    x: [batch, dim, L] (float32 or bfloat16); weight: [dim, W] float32 (W <= 4); bias: [dim]
+    float32; state_in: [batch, dim, W-1] (x's dtype), the inputs before t = 0.  Returns out, or
+    (out, state_out) with return_state (state_out: the W-1 last inputs, for the next piece).
+    """
+    batch, dim, L = x.shape
+    width = weight.shape[1]
+    io = io_dtype_code(x.dtype)
+    if out is None:
+        out = torch.empty_like(x)
+    if state_out is None and return_state:
+        state_out = torch.empty((batch, dim, width - 1), dtype=x.dtype, device=x.device)
+    st = lib().ssm_causal_conv1d_fwd(
+        _ptr(x, x.dtype, (batch, dim, L), "x"),
+        _ptr(weight, torch.float32, (dim, width), "weight"),
+        _ptr(bias, torch.float32, (dim,), "bias"),
+        _ptr(state_in, x.dtype, (batch, dim, width - 1), "state_in"),
+        _ptr(out, x.dtype, (batch, dim, L), "out"),
+        _ptr(state_out, x.dtype, (batch, dim, width - 1), "state_out"),
+        batch, dim, L, width, int(bool(silu)), io, _stream(stream),
+    )
+    _native.check("ssm_causal_conv1d_fwd", st)
+    return (out, state_out) if return_state else out
+
+
+def causal_conv1d_update(state, x, weight, bias=None, silu=True, out=None, stream=None):
+    """One decode step of the causal conv1d (``ssm_causal_conv1d_update``); `state` [batch, dim,
+    W-1] is shifted in place.  x: [batch, dim].  Returns out [batch, dim]."""
+    batch, dim = x.shape
+    width = weight.shape[1]
+    io = io_dtype_code(x.dtype)
+    if out is None:
+        out = torch.empty_like(x)
+    st = lib().ssm_causal_conv1d_update(
+        _ptr(state, x.dtype, (batch, dim, width - 1), "state") if width > 1 else None,
+        _ptr(x, x.dtype, (batch, dim), "x"),
+        _ptr(weight, torch.float32, (dim, width), "weight"),
+        _ptr(bias, torch.float32, (dim,), "bias"),
+        _ptr(out, x.dtype, (batch, dim), "out"),
+        batch, dim, width, int(bool(silu)), io, _stream(stream),
+    )
+    _native.check("ssm_causal_conv1d_update", st)
     return out

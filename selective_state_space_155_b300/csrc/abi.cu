@@ -28,7 +28,7 @@ const char* ssm_status_string(int status) {
     case SSM_ERR_UNSUPPORTED: return "unsupported size (dstate > 16 or grid overflow)";
     case SSM_ERR_LAUNCH: return "the CUDA kernel launch failed";
     case SSM_ERR_TIMEOUT: return "a bounded in-kernel wait gave up";
-    case SSM_ERR_ARG: return "discretization is not an ssm_discretization value";
+    case SSM_ERR_ARG: return "an enumerated argument is out of range, or buffers alias that must not";
     default: return "unknown status";
   }
 }
@@ -113,6 +113,58 @@ int ssm_state_update(float* state, const void* x, const void* dt, const float* A
                      int dim, int dstate, int io_dtype, void* stream) {
   return ssm_state_update_ex(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, out, batch, dim, dstate, io_dtype,
                              SSM_DISC_DELTA_B, stream);
+}
+
+int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias, const void* state_in, void* out,
+                          void* state_out, int batch, int dim, int seqlen, int width, int silu, int io_dtype,
+                          void* stream) {
+  if (batch < 0 || dim < 0 || seqlen < 0 || width < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (width > 4) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0) return SSM_OK;
+  if (!weight) return SSM_ERR_NULL;
+  if (seqlen > 0 && (!x || !out)) return SSM_ERR_NULL;
+  if (seqlen == 0 && (!state_out || width == 1)) return SSM_OK;
+  if (x && x == out) return SSM_ERR_ARG;
+  if (state_in && state_in == state_out) return SSM_ERR_ARG;
+  const size_t es = io_size(io_dtype);
+  const void* io_ptrs[] = {x, out, state_in, state_out};
+  for (const void* p : io_ptrs)
+    if (!aligned(p, es)) return SSM_ERR_ALIGN;
+  if (!aligned(weight, 4) || !aligned(bias, 4)) return SSM_ERR_ALIGN;
+  if ((long long)batch * dim * ((long long)seqlen + width) / 256 + 1 > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+
+  ssm::ConvArgs a{};
+  a.x = x, a.weight = weight, a.bias = bias, a.state_in = state_in, a.out = out, a.state_out = state_out;
+  a.batch = batch, a.dim = dim, a.seqlen = seqlen, a.width = width;
+  a.silu = silu ? 1 : 0;
+  a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  const cudaError_t err = ssm::launch_causal_conv1d(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_causal_conv1d_update(void* state, const void* x, const float* weight, const float* bias, void* out,
+                             int batch, int dim, int width, int silu, int io_dtype, void* stream) {
+  if (batch < 0 || dim < 0 || width < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (width > 4) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0) return SSM_OK;
+  if (!x || !weight || !out || (width > 1 && !state)) return SSM_ERR_NULL;
+  if (x == out) return SSM_ERR_ARG;
+  const size_t es = io_size(io_dtype);
+  const void* io_ptrs[] = {state, x, out};
+  for (const void* p : io_ptrs)
+    if (!aligned(p, es)) return SSM_ERR_ALIGN;
+  if (!aligned(weight, 4) || !aligned(bias, 4)) return SSM_ERR_ALIGN;
+  if ((long long)batch * dim / 256 + 1 > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+
+  ssm::ConvUpdateArgs a{};
+  a.state = state, a.x = x, a.weight = weight, a.bias = bias, a.out = out;
+  a.batch = batch, a.dim = dim, a.width = width;
+  a.silu = silu ? 1 : 0;
+  a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  const cudaError_t err = ssm::launch_causal_conv1d_update(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
 }  // extern "C"

@@ -1,0 +1,228 @@
+// Causal depthwise conv1d (width W <= 4) with bias and optional silu: the step of the Mamba block
+// that produces the scan's input u.  For every (batch b, channel d, step t):
+//   out_t = act(bias[d] + sum_k w[d,k] * x_{t-(W-1)+k}),   x_{-1}, x_{-2}, ... from state_in
+// and state_out = the W-1 last inputs of concat(state_in, x), so that a long row can be streamed
+// in pieces.  The decode form applies the same filter to one new input and shifts the state.
+//
+// The op moves 2 x io bytes per element and does W multiply-adds: it is bound by HBM.  The
+// sequence layout is [batch][dim][seqlen] (time innermost), so one thread takes 16 contiguous
+// bytes of one row (8 bf16 or 4 float32 steps), loads them with one 16-byte load, gets the W-1
+// inputs before them from the previous lane by a shuffle (the first vector of a row takes them
+// from state_in, the first lane of a warp from global memory, where its neighbour's load has
+// just put them in L1), and writes its 16 bytes of output with one store.  Rows whose length
+// or base is not 16-byte aligned take a one-element-per-thread form of the same arithmetic.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <type_traits>
+
+#include "device_math.cuh"
+#include "internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kThreads = 256;
+
+template <typename T>
+struct Vec16;  // 16 bytes of io elements as float32
+template <>
+struct Vec16<float> {
+  static constexpr int N = 4;
+  static __device__ __forceinline__ void load(const float* p, float (&v)[4]) {
+    const float4 q = *reinterpret_cast<const float4*>(p);
+    v[0] = q.x, v[1] = q.y, v[2] = q.z, v[3] = q.w;
+  }
+  static __device__ __forceinline__ void store(float* p, const float (&v)[4]) {
+    *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  }
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+  static constexpr int N = 8;
+  static __device__ __forceinline__ void load(const __nv_bfloat16* p, float (&v)[8]) {
+    const uint4 q = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[k]));
+      v[2 * k] = f.x, v[2 * k + 1] = f.y;
+    }
+  }
+  static __device__ __forceinline__ void store(__nv_bfloat16* p, const float (&v)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * k], v[2 * k + 1]);
+      w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+__device__ __forceinline__ float act(float v, bool silu) { return silu ? silu_f32(v) : v; }
+
+// One thread per 16 bytes of a row; every row is 16-byte aligned and a whole number of vectors.
+template <typename T, int W>
+__global__ void __launch_bounds__(kThreads) conv_vec_kernel(const ConvArgs a) {
+  constexpr int E = Vec16<T>::N, H = W - 1;
+  const long long vpr = a.seqlen / E;
+  const long long nvec = (long long)a.batch * a.dim * vpr;
+  const long long v = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const bool active = v < nvec;
+  const int lane = threadIdx.x & 31;
+  const long long row = active ? v / vpr : 0;
+  const long long j = active ? v % vpr : 0;
+  const T* x = static_cast<const T*>(a.x);
+
+  float xv[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) xv[e] = 0.0f;
+  if (active) Vec16<T>::load(x + row * a.seqlen + j * E, xv);
+  // the H inputs before xv[0]: the previous lane's last ones, unless this vector starts a row
+  // (state_in) or a warp (global memory)
+  float hl[H > 0 ? H : 1];
+#pragma unroll
+  for (int i = 0; i < H; ++i) hl[i] = __shfl_up_sync(0xffffffffu, xv[E - H + i], 1);
+  if (active) {
+    if (j == 0) {
+      const T* si = static_cast<const T*>(a.state_in);
+#pragma unroll
+      for (int i = 0; i < H; ++i) hl[i] = si ? to_f32<T>(si[row * H + i]) : 0.0f;
+    } else if (lane == 0) {
+#pragma unroll
+      for (int i = 0; i < H; ++i) hl[i] = to_f32<T>(x[row * a.seqlen + j * E - H + i]);
+    }
+    const int d = int(row % a.dim);
+    float w[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k) w[k] = __ldg(a.weight + (size_t)d * W + k);
+    const float bias = a.bias ? __ldg(a.bias + d) : 0.0f;
+    float ov[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float acc = bias;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const int s = e - H + k;  // position relative to xv[0]
+        acc = fmaf(w[k], s >= 0 ? xv[s] : hl[H + s], acc);
+      }
+      ov[e] = act(acc, a.silu != 0);
+    }
+    Vec16<T>::store(static_cast<T*>(a.out) + row * a.seqlen + j * E, ov);
+    if (a.state_out && j == vpr - 1) {
+      T* so = static_cast<T*>(a.state_out);
+#pragma unroll
+      for (int i = 0; i < H; ++i) so[row * H + i] = from_f32<T>(xv[E - H + i]);
+    }
+  }
+}
+
+// One thread per output element, then one per state slot (rows x H items after the outputs).
+template <typename T, int W>
+__global__ void __launch_bounds__(kThreads) conv_scalar_kernel(const ConvArgs a) {
+  constexpr int H = W - 1;
+  const long long rows = (long long)a.batch * a.dim;
+  const long long nout = rows * a.seqlen;
+  const long long e = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const T* x = static_cast<const T*>(a.x);
+  const T* si = static_cast<const T*>(a.state_in);
+  // input at time s (< seqlen) of row r: the row itself, or the carried state before t = 0
+  auto in = [&](long long r, long long s) -> float {
+    if (s >= 0) return to_f32<T>(x[r * a.seqlen + s]);
+    return si ? to_f32<T>(si[r * H + H + s]) : 0.0f;
+  };
+  if (e < nout) {
+    const long long r = e / a.seqlen, t = e % a.seqlen;
+    const int d = int(r % a.dim);
+    float acc = a.bias ? __ldg(a.bias + d) : 0.0f;
+#pragma unroll
+    for (int k = 0; k < W; ++k) acc = fmaf(__ldg(a.weight + (size_t)d * W + k), in(r, t - H + k), acc);
+    static_cast<T*>(a.out)[e] = from_f32<T>(act(acc, a.silu != 0));
+  } else if (H > 0 && a.state_out && e < nout + rows * H) {
+    const long long q = e - nout, r = q / (H > 0 ? H : 1), i = q % (H > 0 ? H : 1);
+    static_cast<T*>(a.state_out)[r * H + i] = from_f32<T>(in(r, a.seqlen - H + i));
+  }
+}
+
+// Decode step: out = act(bias + sum_{k<H} w[k] state[k] + w[H] x); state <- (state[1..], x).
+template <typename T, int W>
+__global__ void __launch_bounds__(kThreads) conv_update_kernel(const ConvUpdateArgs a) {
+  constexpr int H = W - 1;
+  const long long ch = (long long)blockIdx.x * kThreads + threadIdx.x;
+  if (ch >= (long long)a.batch * a.dim) return;
+  const int d = int(ch % a.dim);
+  T* st = static_cast<T*>(a.state);
+  float s[H > 0 ? H : 1];
+#pragma unroll
+  for (int i = 0; i < H; ++i) s[i] = to_f32<T>(st[ch * H + i]);
+  const float xv = to_f32<T>(static_cast<const T*>(a.x)[ch]);
+  float acc = a.bias ? __ldg(a.bias + d) : 0.0f;
+#pragma unroll
+  for (int k = 0; k < H; ++k) acc = fmaf(__ldg(a.weight + (size_t)d * W + k), s[k], acc);
+  acc = fmaf(__ldg(a.weight + (size_t)d * W + H), xv, acc);
+  static_cast<T*>(a.out)[ch] = from_f32<T>(act(acc, a.silu != 0));
+#pragma unroll
+  for (int i = 0; i < H; ++i) st[ch * H + i] = from_f32<T>(i + 1 < H ? s[i + 1] : xv);
+}
+
+template <typename T, int W>
+cudaError_t launch_fwd(const ConvArgs& a, bool vec, cudaStream_t stream) {
+  const long long rows = (long long)a.batch * a.dim;
+  constexpr int E = 16 / sizeof(T);
+  const long long items = vec ? rows * (a.seqlen / E) : rows * a.seqlen + (a.state_out ? rows * (W - 1) : 0);
+  if (items <= 0) return cudaSuccess;
+  const long long nblk = (items + kThreads - 1) / kThreads;
+  if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  ConvArgs args = a;
+  void* params[] = {&args};
+  const void* fn = vec ? reinterpret_cast<const void*>(conv_vec_kernel<T, W>)
+                       : reinterpret_cast<const void*>(conv_scalar_kernel<T, W>);
+  return cudaLaunchKernel(fn, dim3(unsigned(nblk)), dim3(kThreads), params, 0, stream);
+}
+
+template <typename T>
+cudaError_t dispatch_fwd(const ConvArgs& a, cudaStream_t stream) {
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  const bool vec = a.seqlen > 0 && (size_t(a.seqlen) * sizeof(T)) % 16 == 0 && al(a.x) && al(a.out);
+  switch (a.width) {
+    case 1: return launch_fwd<T, 1>(a, vec, stream);
+    case 2: return launch_fwd<T, 2>(a, vec, stream);
+    case 3: return launch_fwd<T, 3>(a, vec, stream);
+    default: return launch_fwd<T, 4>(a, vec, stream);
+  }
+}
+
+template <typename T, int W>
+cudaError_t launch_update(const ConvUpdateArgs& a, cudaStream_t stream) {
+  const long long nblk = ((long long)a.batch * a.dim + kThreads - 1) / kThreads;
+  if (nblk <= 0) return cudaSuccess;
+  if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  ConvUpdateArgs args = a;
+  void* params[] = {&args};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(conv_update_kernel<T, W>), dim3(unsigned(nblk)),
+                          dim3(kThreads), params, 0, stream);
+}
+
+template <typename T>
+cudaError_t dispatch_update(const ConvUpdateArgs& a, cudaStream_t stream) {
+  switch (a.width) {
+    case 1: return launch_update<T, 1>(a, stream);
+    case 2: return launch_update<T, 2>(a, stream);
+    case 3: return launch_update<T, 3>(a, stream);
+    default: return launch_update<T, 4>(a, stream);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_causal_conv1d(const ConvArgs& a, cudaStream_t stream) {
+  return a.io == kF32 ? dispatch_fwd<float>(a, stream) : dispatch_fwd<__nv_bfloat16>(a, stream);
+}
+
+cudaError_t launch_causal_conv1d_update(const ConvUpdateArgs& a, cudaStream_t stream) {
+  return a.io == kF32 ? dispatch_update<float>(a, stream) : dispatch_update<__nv_bfloat16>(a, stream);
+}
+
+}  // namespace ssm

@@ -44,6 +44,31 @@ struct UpdateArgs {
   int zoh;  // exact zero-order-hold Bbar instead of Delta * B
 };
 
+// Arguments of one causal conv1d over whole rows; meaning as in ssm_scan.h.
+struct ConvArgs {
+  const void* x;
+  const float* weight;
+  const float* bias;
+  const void* state_in;
+  void* out;
+  void* state_out;
+  int batch, dim, seqlen, width;
+  int silu;
+  int io;
+};
+
+// Arguments of one causal conv1d decode step; meaning as in ssm_scan.h.
+struct ConvUpdateArgs {
+  void* state;
+  const void* x;
+  const float* weight;
+  const float* bias;
+  void* out;
+  int batch, dim, width;
+  int silu;
+  int io;
+};
+
 // Enqueue the scan on `stream`.  Arguments are already validated.  Picks the lane-per-channel
 // form when there are enough channels to give every SM eight or more of its warps, otherwise the
 // four-lanes-per-channel form; SSM_SCAN_VARIANT=lane|quad in the environment forces one.  The
@@ -58,5 +83,10 @@ cudaError_t launch_scan_fwd_lane(const ScanArgs& a, bool vec, cudaStream_t strea
 
 // Enqueue one decode step on `stream`.  Arguments are already validated.
 cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);
+
+// Enqueue the causal conv1d / its decode step on `stream` (causal_conv1d.cu).  Arguments are
+// already validated (width 1..4).
+cudaError_t launch_causal_conv1d(const ConvArgs& a, cudaStream_t stream);
+cudaError_t launch_causal_conv1d_update(const ConvUpdateArgs& a, cudaStream_t stream);
 
 }  // namespace ssm

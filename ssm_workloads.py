@@ -19,6 +19,9 @@ Recipe (one per workload, all seeded):
   * device generator: torch's CUDA Philox generator seeded with ``seed``; used for
     the 65536-long scan and the 1024-step decode loop, whose parity tests sample
     channels and copy those inputs back to the host.
+  * causal conv1d (the layer in front of the scan): x ~ N(0, 1) in the scan's io dtype and
+    shape, weight[d, k] and bias[d] ~ U(-1/sqrt(W), 1/sqrt(W)) (the default init bound of a
+    depthwise Conv1d, fan-in W), float32; width W = 4 (d_conv of the pages' usage example).
 """
 from __future__ import annotations
 
@@ -203,6 +206,18 @@ def random_scan_case(batch, dim, dstate, seqlen, io="f32", seed=0, gate=True, us
     D = torch.from_numpy(rng.standard_normal(dim).astype(np.float32)) if use_D else None
     h0t = torch.from_numpy(rng.standard_normal((batch, dim, dstate)).astype(np.float32)) if h0 else None
     return dict(u=u, delta=delta, z=z, B=B, C=C, A=A, D=D, dt_bias=dt_bias, h0=h0t, softplus=softplus)
+
+
+def conv_inputs(batch, dim, seqlen, width=4, io="bf16", seed=0, bias=True, state=False):
+    """Seeded inputs of the causal conv1d (host generator): x [batch, dim, seqlen], weight
+    [dim, width], bias [dim], and optionally a carried state [batch, dim, width-1]."""
+    rng = np.random.default_rng(seed)
+    bound = 1.0 / math.sqrt(width)
+    x = _round_io(rng.standard_normal((batch, dim, seqlen)), io)
+    weight = torch.from_numpy(rng.uniform(-bound, bound, (dim, width)).astype(np.float32))
+    b = torch.from_numpy(rng.uniform(-bound, bound, dim).astype(np.float32)) if bias else None
+    st = _round_io(rng.standard_normal((batch, dim, width - 1)), io) if state else None
+    return dict(x=x, weight=weight, bias=b, state=st)
 
 
 def to_f64(t):

@@ -31,7 +31,7 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_scan_fwd_ex", "ssm_state_update",
-         "ssm_state_update_ex", "ssm_status_string"])
+         "ssm_state_update_ex", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -148,3 +148,48 @@ def test_binding_rejects_cpu_tensors():
     u = torch.zeros(1, 2, 3)
     with pytest.raises(ValueError, match="CUDA"):
         ssm.ssm_scan_fwd(u, u, torch.zeros(2, 4), torch.zeros(1, 4, 3), torch.zeros(1, 4, 3))
+
+
+def conv_args(**over):
+    a = dict(x=P, weight=P, bias=P, state_in=P + 0x1000, out=P + 0x2000, state_out=P + 0x3000, batch=2, dim=3,
+             seqlen=8, width=4, silu=1, io=_native.SSM_BF16, stream=None)
+    a.update(over)
+    return [a[k] for k in ("x", "weight", "bias", "state_in", "out", "state_out", "batch", "dim", "seqlen", "width",
+                           "silu", "io", "stream")]
+
+
+@pytest.mark.parametrize("over,expected", [
+    (dict(x=None), _native.SSM_ERR_NULL),
+    (dict(out=None), _native.SSM_ERR_NULL),
+    (dict(weight=None), _native.SSM_ERR_NULL),
+    (dict(width=0), _native.SSM_ERR_SHAPE),
+    (dict(width=5), _native.SSM_ERR_UNSUPPORTED),
+    (dict(seqlen=-1), _native.SSM_ERR_SHAPE),
+    (dict(io=3), _native.SSM_ERR_DTYPE),
+    (dict(out=P), _native.SSM_ERR_ARG),
+    (dict(state_out=P + 0x1000), _native.SSM_ERR_ARG),
+    (dict(x=P + 1), _native.SSM_ERR_ALIGN),
+    (dict(weight=P + 2), _native.SSM_ERR_ALIGN),
+    (dict(batch=0), _native.SSM_OK),
+    (dict(seqlen=0, x=None, out=None, state_out=None), _native.SSM_OK),
+])
+def test_conv_validation(lib, over, expected):
+    assert lib.ssm_causal_conv1d_fwd(*conv_args(**over)) == expected
+
+
+@pytest.mark.parametrize("over,expected", [
+    (dict(state=None), _native.SSM_ERR_NULL),
+    (dict(state=None, width=1), _native.SSM_OK),
+    (dict(x=None), _native.SSM_ERR_NULL),
+    (dict(width=9), _native.SSM_ERR_UNSUPPORTED),
+    (dict(out=P + 0x1000), _native.SSM_ERR_ARG),
+    (dict(state=P + 1), _native.SSM_ERR_ALIGN),
+])
+def test_conv_update_validation(lib, over, expected):
+    a = dict(state=P, x=P + 0x1000, weight=P, bias=None, out=P + 0x2000, batch=2, dim=3, width=4, silu=1,
+             io=_native.SSM_BF16, stream=None)
+    a.update(over)
+    if expected == _native.SSM_OK:
+        a["batch"] = 0  # a valid call that launches nothing
+    args = [a[k] for k in ("state", "x", "weight", "bias", "out", "batch", "dim", "width", "silu", "io", "stream")]
+    assert lib.ssm_causal_conv1d_update(*args) == expected
