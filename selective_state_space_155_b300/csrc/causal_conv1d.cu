@@ -6,11 +6,12 @@
 //
 // The op moves 2 x io bytes per element and does W multiply-adds: it is bound by HBM.  The
 // sequence layout is [batch][dim][seqlen] (time innermost), so one thread takes 16 contiguous
-// bytes of one row (8 bf16 or 4 float32 steps), loads them with one 16-byte load, gets the W-1
-// inputs before them from the previous lane by a shuffle (the first vector of a row takes them
-// from state_in, the first lane of a warp from global memory, where its neighbour's load has
-// just put them in L1), and writes its 16 bytes of output with one store.  Rows whose length
-// or base is not 16-byte aligned take a one-element-per-thread form of the same arithmetic.
+// bytes of one row (8 bf16 or 4 float32 steps) at a time, loads them with one 16-byte load, gets
+// the W-1 inputs before them from the previous lane by a shuffle (the first vector of a row takes
+// them from state_in, the first lane of a warp from global memory, where its neighbour's load has
+// just put them in L1), and writes its 16 bytes of output with one store; two such vectors per
+// thread, loads first.  Rows whose length or base is not 16-byte aligned take a
+// one-element-per-thread form of the same arithmetic.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -63,38 +64,62 @@ struct Vec16<__nv_bfloat16> {
 
 __device__ __forceinline__ float act(float v, bool silu) { return silu ? silu_f32(v) : v; }
 
-// One thread per 16 bytes of a row; every row is 16-byte aligned and a whole number of vectors.
+// q = n / f.d and r = n % f.d: the multiply-shift division while n fits in 32 bits (every tensor
+// below 2^32 work items), a 64-bit division beyond.
+__device__ __forceinline__ void divmod(long long n, const FastDiv& f, long long& q, long long& r) {
+  if (n < (1LL << 32)) {
+    q = fast_div(uint32_t(n), f);
+  } else {
+    q = n / (long long)f.d;
+  }
+  r = n - q * (long long)f.d;
+}
+
+// Each thread takes K vectors of 16 bytes, kThreads apart, so that consecutive lanes hold
+// consecutive vectors; all K loads are issued before any arithmetic to keep enough bytes in
+// flight.  Every row is 16-byte aligned and a whole number of vectors, so vector v starts at
+// element v*E of the flattened [batch*dim][seqlen] tensor.
+constexpr int kVecPerThread = 2;
+
 template <typename T, int W>
 __global__ void __launch_bounds__(kThreads) conv_vec_kernel(const ConvArgs a) {
-  constexpr int E = Vec16<T>::N, H = W - 1;
+  constexpr int E = Vec16<T>::N, H = W - 1, K = kVecPerThread;
   const long long vpr = a.seqlen / E;
   const long long nvec = (long long)a.batch * a.dim * vpr;
-  const long long v = (long long)blockIdx.x * kThreads + threadIdx.x;
-  const bool active = v < nvec;
+  const long long base = (long long)blockIdx.x * kThreads * K + threadIdx.x;
   const int lane = threadIdx.x & 31;
-  const long long row = active ? v / vpr : 0;
-  const long long j = active ? v % vpr : 0;
   const T* x = static_cast<const T*>(a.x);
 
-  float xv[E];
+  float xv[K][E];
 #pragma unroll
-  for (int e = 0; e < E; ++e) xv[e] = 0.0f;
-  if (active) Vec16<T>::load(x + row * a.seqlen + j * E, xv);
-  // the H inputs before xv[0]: the previous lane's last ones, unless this vector starts a row
-  // (state_in) or a warp (global memory)
-  float hl[H > 0 ? H : 1];
+  for (int i = 0; i < K; ++i) {
+    const long long v = base + (long long)i * kThreads;
 #pragma unroll
-  for (int i = 0; i < H; ++i) hl[i] = __shfl_up_sync(0xffffffffu, xv[E - H + i], 1);
-  if (active) {
+    for (int e = 0; e < E; ++e) xv[i][e] = 0.0f;
+    if (v < nvec) Vec16<T>::load(x + v * E, xv[i]);
+  }
+#pragma unroll
+  for (int i = 0; i < K; ++i) {
+    const long long v = base + (long long)i * kThreads;
+    const bool active = v < nvec;
+    // the H inputs before xv[i][0]: the previous lane's last ones, unless this vector starts a
+    // row (state_in) or a warp (global memory)
+    float hl[H > 0 ? H : 1];
+#pragma unroll
+    for (int h = 0; h < H; ++h) hl[h] = __shfl_up_sync(0xffffffffu, xv[i][E - H + h], 1);
+    if (!active) continue;
+    long long row, j, dq, dr;
+    divmod(v, a.div_row, row, j);
     if (j == 0) {
       const T* si = static_cast<const T*>(a.state_in);
 #pragma unroll
-      for (int i = 0; i < H; ++i) hl[i] = si ? to_f32<T>(si[row * H + i]) : 0.0f;
+      for (int h = 0; h < H; ++h) hl[h] = si ? to_f32<T>(si[row * H + h]) : 0.0f;
     } else if (lane == 0) {
 #pragma unroll
-      for (int i = 0; i < H; ++i) hl[i] = to_f32<T>(x[row * a.seqlen + j * E - H + i]);
+      for (int h = 0; h < H; ++h) hl[h] = to_f32<T>(x[v * E - H + h]);
     }
-    const int d = int(row % a.dim);
+    divmod(row, a.div_dim, dq, dr);
+    const int d = int(dr);
     float w[W];
 #pragma unroll
     for (int k = 0; k < W; ++k) w[k] = __ldg(a.weight + (size_t)d * W + k);
@@ -105,16 +130,16 @@ __global__ void __launch_bounds__(kThreads) conv_vec_kernel(const ConvArgs a) {
       float acc = bias;
 #pragma unroll
       for (int k = 0; k < W; ++k) {
-        const int s = e - H + k;  // position relative to xv[0]
-        acc = fmaf(w[k], s >= 0 ? xv[s] : hl[H + s], acc);
+        const int s = e - H + k;  // position relative to xv[i][0]
+        acc = fmaf(w[k], s >= 0 ? xv[i][s] : hl[H + s], acc);
       }
       ov[e] = act(acc, a.silu != 0);
     }
-    Vec16<T>::store(static_cast<T*>(a.out) + row * a.seqlen + j * E, ov);
+    Vec16<T>::store(static_cast<T*>(a.out) + v * E, ov);
     if (a.state_out && j == vpr - 1) {
       T* so = static_cast<T*>(a.state_out);
 #pragma unroll
-      for (int i = 0; i < H; ++i) so[row * H + i] = from_f32<T>(xv[E - H + i]);
+      for (int h = 0; h < H; ++h) so[row * H + h] = from_f32<T>(xv[i][E - H + h]);
     }
   }
 }
@@ -134,8 +159,10 @@ __global__ void __launch_bounds__(kThreads) conv_scalar_kernel(const ConvArgs a)
     return si ? to_f32<T>(si[r * H + H + s]) : 0.0f;
   };
   if (e < nout) {
-    const long long r = e / a.seqlen, t = e % a.seqlen;
-    const int d = int(r % a.dim);
+    long long r, t, dq, dr;
+    divmod(e, a.div_row, r, t);
+    divmod(r, a.div_dim, dq, dr);
+    const int d = int(dr);
     float acc = a.bias ? __ldg(a.bias + d) : 0.0f;
 #pragma unroll
     for (int k = 0; k < W; ++k) acc = fmaf(__ldg(a.weight + (size_t)d * W + k), in(r, t - H + k), acc);
@@ -152,7 +179,9 @@ __global__ void __launch_bounds__(kThreads) conv_update_kernel(const ConvUpdateA
   constexpr int H = W - 1;
   const long long ch = (long long)blockIdx.x * kThreads + threadIdx.x;
   if (ch >= (long long)a.batch * a.dim) return;
-  const int d = int(ch % a.dim);
+  long long bq, dr;
+  divmod(ch, a.div_dim, bq, dr);
+  const int d = int(dr);
   T* st = static_cast<T*>(a.state);
   float s[H > 0 ? H : 1];
 #pragma unroll
@@ -173,9 +202,12 @@ cudaError_t launch_fwd(const ConvArgs& a, bool vec, cudaStream_t stream) {
   constexpr int E = 16 / sizeof(T);
   const long long items = vec ? rows * (a.seqlen / E) : rows * a.seqlen + (a.state_out ? rows * (W - 1) : 0);
   if (items <= 0) return cudaSuccess;
-  const long long nblk = (items + kThreads - 1) / kThreads;
+  const long long per_block = vec ? (long long)kThreads * kVecPerThread : kThreads;
+  const long long nblk = (items + per_block - 1) / per_block;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   ConvArgs args = a;
+  args.div_row = make_fastdiv(uint32_t(vec ? a.seqlen / E : (a.seqlen > 0 ? a.seqlen : 1)));
+  args.div_dim = make_fastdiv(uint32_t(a.dim));
   void* params[] = {&args};
   const void* fn = vec ? reinterpret_cast<const void*>(conv_vec_kernel<T, W>)
                        : reinterpret_cast<const void*>(conv_scalar_kernel<T, W>);
@@ -200,6 +232,7 @@ cudaError_t launch_update(const ConvUpdateArgs& a, cudaStream_t stream) {
   if (nblk <= 0) return cudaSuccess;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   ConvUpdateArgs args = a;
+  args.div_dim = make_fastdiv(uint32_t(a.dim));
   void* params[] = {&args};
   return cudaLaunchKernel(reinterpret_cast<const void*>(conv_update_kernel<T, W>), dim3(unsigned(nblk)),
                           dim3(kThreads), params, 0, stream);

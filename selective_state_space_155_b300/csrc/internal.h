@@ -2,8 +2,30 @@
 #pragma once
 
 #include <cuda_runtime.h>
+#include <stdint.h>
 
 namespace ssm {
+
+// Unsigned 32-bit division by a run-time constant d >= 1 with one multiply-high, an add and a
+// shift (the round-up multiply-shift method of Granlund and Montgomery, "Division by invariant
+// integers using multiplication"): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// n / d = (umulhi(n, m) + n) >> l for every 32-bit n (the sum is formed in 64 bits).
+struct FastDiv {
+  uint32_t d, m, l;
+};
+
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while (l < 32 && (uint64_t(1) << l) < d) ++l;
+  const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << l) - d)) / d + 1;
+  return FastDiv{d, uint32_t(m), l};
+}
+
+#ifdef __CUDACC__
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  return uint32_t((uint64_t(__umulhi(n, f.m)) + n) >> f.l);
+}
+#endif
 
 enum Io { kF32 = 0, kBF16 = 1 };
 
@@ -41,7 +63,8 @@ struct UpdateArgs {
   int batch, dim, dstate;
   int softplus;
   int io;
-  int zoh;  // exact zero-order-hold Bbar instead of Delta * B
+  int zoh;          // exact zero-order-hold Bbar instead of Delta * B
+  FastDiv div_dim;  // filled at launch
 };
 
 // Arguments of one causal conv1d over whole rows; meaning as in ssm_scan.h.
@@ -55,6 +78,8 @@ struct ConvArgs {
   int batch, dim, seqlen, width;
   int silu;
   int io;
+  FastDiv div_row;  // by the work items of one row (vectors or elements), filled at launch
+  FastDiv div_dim;  // by dim, filled at launch
 };
 
 // Arguments of one causal conv1d decode step; meaning as in ssm_scan.h.
@@ -67,6 +92,7 @@ struct ConvUpdateArgs {
   int batch, dim, width;
   int silu;
   int io;
+  FastDiv div_dim;  // filled at launch
 };
 
 // Enqueue the scan on `stream`.  Arguments are already validated.  Picks the lane-per-channel

@@ -60,7 +60,9 @@ template <typename T, int NPAD, bool VEC>
 __global__ void __launch_bounds__(kBlock) state_update_kernel(const UpdateArgs a) {
   const long long ch = (long long)blockIdx.x * kBlock + threadIdx.x;
   if (ch >= (long long)a.batch * a.dim) return;
-  const int b = int(ch / a.dim), d = int(ch % a.dim);
+  // (b, d) = divmod(ch, dim): the multiply-shift division below 2^32 channels
+  const long long bq = ch < (1LL << 32) ? (long long)fast_div(uint32_t(ch), a.div_dim) : ch / a.dim;
+  const int b = int(bq), d = int(ch - bq * a.dim);
   const int N = a.dstate;
   float* srow = a.state + ch * N;
   const float* Arow = a.A + size_t(d) * N;
@@ -149,6 +151,7 @@ cudaError_t launch_npad(const UpdateArgs& a, cudaStream_t stream) {
                                                   (reinterpret_cast<uintptr_t>(a.C) & 7u) == 0));
   const bool vec = a.dstate == NPAD && al(a.state) && al(a.A) && bc_ok;
   UpdateArgs args = a;
+  args.div_dim = make_fastdiv(uint32_t(a.dim));
   void* params[] = {&args};
   const void* fn = vec ? reinterpret_cast<const void*>(state_update_kernel<T, NPAD, true>)
                        : reinterpret_cast<const void*>(state_update_kernel<T, NPAD, false>);
