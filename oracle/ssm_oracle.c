@@ -40,6 +40,15 @@
  *   Decode step    the same single recurrence step applied to a stored state
  *                  (constant-memory inference: gsyq.cn page, complexity table
  *                  row "推理内存 O(d) 状态向量").
+ *   Backward       reverse-mode gradients of the scan (Delta*B form) for a
+ *                  loss whose gradient with respect to the outputs is dout:
+ *                  the same recurrence run backwards with the adjoint state
+ *                  lambda_t = dy_t C_t + Abar_{t+1} lambda_{t+1} (chain rule
+ *                  through h_t = Abar_t h_{t-1} + Delta_t B_t u_t).  Training
+ *                  is where the pages' speed claims are made (53ai.com
+ *                  article, sections on the hardware-aware algorithm and the
+ *                  training speed-up); the steps follow from the forward
+ *                  definitions above and nothing else.
  *   Causal conv    depthwise causal convolution of width W over time, one
  *                  filter per channel, before the scan:
  *                    out_t = act(bias[d] + sum_k w[d,k] * x_{t-(W-1)+k}),
@@ -166,6 +175,97 @@ int oracle_state_update_f64(double* state, const double* x, const double* dt, co
     if (z) acc *= silu_f64(z[ch]);
     out[ch] = acc;
   }
+  return 0;
+}
+
+/* d silu / dz = sigmoid(z) * (1 + z * (1 - sigmoid(z))). */
+static double dsilu_f64(double z) {
+  double sg = 1.0 / (1.0 + exp(-z));
+  return sg * (1.0 + z * (1.0 - sg));
+}
+
+/*
+ * Gradients of the scan (Delta*B discretisation) given dout = dLoss/dout, same layouts as the
+ * forward.  Outputs (all overwritten, summed over what the parameter is shared by):
+ *   du, ddelta, dz        [batch][dim][seqlen]   (dz only when z is given; NULL skips it)
+ *   dA                    [dim][dstate]          (summed over batch)
+ *   dB, dC                [batch][dstate][seqlen] (summed over channels)
+ *   dD, ddt_bias          [dim]                  (summed over batch and time; NULL skips)
+ *   dh0                   [batch][dim][dstate]   (gradient of the initial state; NULL skips)
+ * ddelta is with respect to the raw delta (before dt_bias and softplus).
+ */
+int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, const double* B, const double* C,
+                        const double* D, const double* z, const double* dt_bias, int delta_softplus,
+                        const double* h0, const double* dout, double* du, double* ddelta, double* dA, double* dB,
+                        double* dC, double* dD, double* dz, double* ddt_bias, double* dh0, int batch, int dim,
+                        int dstate, int seqlen) {
+  if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC) return -1;
+  if (batch < 0 || dim < 0 || dstate < 1 || seqlen < 0) return -2;
+  long N = dstate, L = seqlen;
+  for (long i = 0; i < (long)dim * N; ++i) dA[i] = 0.0;
+  for (long i = 0; i < (long)batch * N * L; ++i) dB[i] = dC[i] = 0.0;
+  if (dD) for (int i = 0; i < dim; ++i) dD[i] = 0.0;
+  if (ddt_bias) for (int i = 0; i < dim; ++i) ddt_bias[i] = 0.0;
+  double* hs = (double*)malloc(sizeof(double) * (size_t)((L + 1) * N + 1)); /* hs[(t+1)*N + n] = h_t */
+  double* carry = (double*)malloc(sizeof(double) * (size_t)N);
+  double* ys = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+  double* dts = (double*)malloc(sizeof(double) * (size_t)(L + 1));
+  for (long ch = 0; ch < (long)batch * dim; ++ch) {
+    int b = (int)(ch / dim), d = (int)(ch % dim);
+    const double* ur = u + ch * L;
+    const double* dr = delta + ch * L;
+    const double* zr = z ? z + ch * L : NULL;
+    const double* gr = dout + ch * L;
+    /* forward, keeping every state */
+    for (long n = 0; n < N; ++n) hs[n] = h0 ? h0[ch * N + n] : 0.0;
+    for (long t = 0; t < L; ++t) {
+      double dt = step_size(dr[t], dt_bias, d, delta_softplus);
+      dts[t] = dt;
+      double acc = 0.0;
+      for (long n = 0; n < N; ++n) {
+        double a = exp(dt * A[(long)d * N + n]);
+        double h = a * hs[t * N + n] + dt * B[((long)b * N + n) * L + t] * ur[t];
+        hs[(t + 1) * N + n] = h;
+        acc += C[((long)b * N + n) * L + t] * h;
+      }
+      if (D) acc += D[d] * ur[t];
+      ys[t] = acc; /* before the gate */
+    }
+    /* backward */
+    for (long n = 0; n < N; ++n) carry[n] = 0.0;
+    for (long t = L - 1; t >= 0; --t) {
+      double dt = dts[t];
+      double dy = zr ? gr[t] * silu_f64(zr[t]) : gr[t];
+      if (zr && dz) dz[ch * L + t] = gr[t] * ys[t] * dsilu_f64(zr[t]);
+      if (D && dD) dD[d] += dy * ur[t];
+      double dut = D ? dy * D[d] : 0.0;
+      double ddt = 0.0;
+      for (long n = 0; n < N; ++n) {
+        double an = A[(long)d * N + n];
+        double a = exp(dt * an);
+        double bn = B[((long)b * N + n) * L + t];
+        double hp = hs[t * N + n];        /* h_{t-1} */
+        double lam = dy * C[((long)b * N + n) * L + t] + carry[n];
+        dC[((long)b * N + n) * L + t] += dy * hs[(t + 1) * N + n];
+        dB[((long)b * N + n) * L + t] += lam * dt * ur[t];
+        dut += lam * dt * bn;
+        ddt += lam * (an * a * hp + bn * ur[t]);
+        dA[(long)d * N + n] += lam * dt * a * hp;
+        carry[n] = lam * a;
+      }
+      du[ch * L + t] = dut;
+      double raw = dr[t] + (dt_bias ? dt_bias[d] : 0.0);
+      double dd = delta_softplus ? ddt / (1.0 + exp(-raw)) : ddt; /* softplus' = sigmoid */
+      ddelta[ch * L + t] = dd;
+      if (ddt_bias && dt_bias) ddt_bias[d] += dd;
+    }
+    if (dh0)
+      for (long n = 0; n < N; ++n) dh0[ch * N + n] = carry[n];
+  }
+  free(hs);
+  free(carry);
+  free(ys);
+  free(dts);
   return 0;
 }
 

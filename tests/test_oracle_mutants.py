@@ -40,22 +40,38 @@ MUTANTS = {
     "conv_off_by_one": ("int s = t - hw + k; /* input time index */", "int s = t - hw + k - 1; /* input time index */"),
     "conv_state_ignored": ("double v = s >= 0 ? xr[s] : (sr ? sr[hw + s] : 0.0);", "double v = s >= 0 ? xr[s] : 0.0;"),
     "conv_no_bias": ("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
+    "bwd_no_carry": ("double lam = dy * C[((long)b * N + n) * L + t] + carry[n];",
+                     "double lam = dy * C[((long)b * N + n) * L + t];"),
+    "bwd_carry_without_decay": ("carry[n] = lam * a;", "carry[n] = lam;"),
+    "bwd_dA_missing_state": ("dA[(long)d * N + n] += lam * dt * a * hp;", "dA[(long)d * N + n] += lam * dt * a;"),
+    "bwd_dC_previous_state": ("dC[((long)b * N + n) * L + t] += dy * hs[(t + 1) * N + n];",
+                              "dC[((long)b * N + n) * L + t] += dy * hs[t * N + n];"),
+    "bwd_softplus_grad": ("double dd = delta_softplus ? ddt / (1.0 + exp(-raw)) : ddt;",
+                          "double dd = delta_softplus ? ddt / (1.0 + exp(raw)) : ddt;"),
+    "bwd_dsilu": ("return sg * (1.0 + z * (1.0 - sg));", "return sg * (1.0 - sg);"),
     "h0_ignored": ("h[n] = h0 ? h0[ch * dstate + n] : 0.0;", "h[n] = 0.0;"),
 }
 
 PIN_TESTS = [getattr(pins, n) for n in dir(pins) if n.startswith("test_")]
 
 
+def _arglists(fn):
+    """Every keyword-argument combination of a test's parametrize marks (their product)."""
+    arglists = [{}]
+    for m in getattr(fn, "pytestmark", []):
+        if m.name != "parametrize":
+            continue
+        names, values = m.args
+        names = [n.strip() for n in names.split(",")] if isinstance(names, str) else list(names)
+        combos = [dict(zip(names, v if len(names) > 1 else (v,))) for v in values]
+        arglists = [{**a, **c} for a in arglists for c in combos]
+    return arglists
+
+
 def _run_pins():
     failures = 0
     for fn in PIN_TESTS:
-        params = getattr(fn, "pytestmark", [])
-        arglists = [{}]
-        for m in params:
-            if m.name == "parametrize":
-                name, values = m.args
-                arglists = [{name: v} for v in values]
-        for kw in arglists:
+        for kw in _arglists(fn):
             try:
                 fn(**kw)
             except Exception:  # an assertion or a numerical error both count as a rejection
