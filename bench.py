@@ -20,6 +20,7 @@ Extra objects on the line:
                 captured in one CUDA graph, and one step after an L2 flush;
   zoh           the same scan workload with the exact zero-order-hold discretisation;
   conv1d        the causal conv1d (width 4, silu) that produces u, on the same activation shape;
+  train         the training pair on the same workload: forward with state checkpoints, backward;
   clocks        SM clocks and throttle reasons sampled (NVML) during the timed region.
 
 Under torchrun each rank runs the same workload on its own GPU with no collective on the data
@@ -411,6 +412,40 @@ def run_zoh(w: wl.ScanWorkload, device, steps=200, warmup=5):
             "elements_per_s": w.elements / (ms * 1e-3), "hbm_gbs": gbs, "frac_of_hbm": gbs / hbm, "steps": steps}
 
 
+def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_COPIES):
+    """The training pair on the scan workload: the forward that keeps chunk checkpoints, then the
+    backward pass from them and a synthetic dout (rotating input copies, as for the forward)."""
+    import selective_state_space_155_b300 as ssm
+    run = ScanRun(w, device, copies=copies)
+    nck = ssm.scan_num_checkpoints(w.seqlen)
+    cks = [torch.empty((w.batch, nck, w.dim, w.dstate), dtype=torch.float32, device=device) for _ in range(copies)]
+    gen = torch.Generator(device=device).manual_seed(w.seed)
+    douts = [torch.randn((w.batch, w.dim, w.seqlen), generator=gen, device=device).to(run.sets[0]["u"].dtype)
+             for _ in range(copies)]
+
+    def fwd(i):
+        k = i % copies
+        s = run.sets[k]
+        ssm.ssm_scan_fwd(s["u"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"], s["dt_bias"],
+                         y=run.y[k], last_state=run.last[k], checkpoints=cks[k])
+
+    def bwd(i):
+        k = i % copies
+        s = run.sets[k]
+        ssm.ssm_scan_bwd(s["u"], s["delta"], s["A"], s["B"], s["C"], cks[k], douts[k], D=s["D"], z=s["z"],
+                         dt_bias=s["dt_bias"])
+
+    for i in range(copies):
+        fwd(i)
+    ms_f = timed(fwd, steps, warmup)
+    ms_b = timed(bwd, steps, warmup)
+    del run, cks, douts
+    torch.cuda.empty_cache()
+    return {"workload": w.name, "fwd_train_us": ms_f * 1e3, "bwd_us": ms_b * 1e3, "step_us": (ms_f + ms_b) * 1e3,
+            "elements_per_s": w.elements / ((ms_f + ms_b) * 1e-3), "steps": steps,
+            "note": "backward allocates its gradient tensors each call (torch caching allocator)"}
+
+
 def run_conv(w: wl.ScanWorkload, device, steps=300, warmup=5, copies=ROTATING_COPIES):
     """The causal conv1d (width 4, silu) that produces the scan's u, on the scan workload's
     activation shape; rotating copies keep each launch reading from HBM."""
@@ -482,6 +517,17 @@ def profile_mode(which: str) -> int:
     elif which == "zoh":
         run = ScanRun(wl.MID, device, copies=1, discretization="zoh")
         fn = run.step
+    elif which == "bwd":
+        import selective_state_space_155_b300 as ssm
+        run = ScanRun(wl.MID, device, copies=1)
+        s0 = run.sets[0]
+        ck = torch.empty((wl.MID.batch, ssm.scan_num_checkpoints(wl.MID.seqlen), wl.MID.dim, wl.MID.dstate),
+                         dtype=torch.float32, device=device)
+        ssm.ssm_scan_fwd(s0["u"], s0["delta"], s0["A"], s0["B"], s0["C"], s0["D"], s0["z"], s0["dt_bias"],
+                         checkpoints=ck)
+        dout = torch.randn_like(s0["u"], dtype=torch.float32).to(s0["u"].dtype)
+        fn = lambda i: ssm.ssm_scan_bwd(s0["u"], s0["delta"], s0["A"], s0["B"], s0["C"], ck, dout, D=s0["D"],
+                                        z=s0["z"], dt_bias=s0["dt_bias"])
     elif which == "conv":
         import selective_state_space_155_b300 as ssm
         w = wl.MID
@@ -511,7 +557,8 @@ def main(argv=None):
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "zoh", "conv", "decode"], default=None,
+    ap.add_argument("--no-train", action="store_true")
+    ap.add_argument("--profile", choices=["scan", "zoh", "bwd", "conv", "decode"], default=None,
                     help="run 2 warm-up and 3 profiled launches of one kernel on its workload and exit "
                          "(a small command for ncu; prints no JSON line)")
     args = ap.parse_args(argv)
@@ -582,6 +629,8 @@ def main(argv=None):
         res["zoh"] = run_zoh(w, device)
     if rank == 0 and not args.no_conv:
         res["conv1d"] = run_conv(w, device)
+    if rank == 0 and not args.no_train:
+        res["train"] = run_train(w, device)
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w)
     if dist is not None:

@@ -25,6 +25,10 @@
  *                    row "推理内存 O(d) 状态向量"; 53ai.com Mamba article, §1 on
  *                    RNN-style inference from the previous hidden state only).
  *
+ *  ssm_scan_fwd_train / ssm_scan_bwd
+ *                    The training pair: a forward that keeps chunk checkpoints of
+ *                    the state, and the backward pass from them.
+ *
  *  ssm_causal_conv1d_fwd / ssm_causal_conv1d_update
  *                    The depthwise causal convolution that produces the scan's
  *                    input, over whole rows and as a decode step.
@@ -121,6 +125,45 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void
                     const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
                     float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
                     void* stream);
+
+/*
+ * Training forward: ssm_scan_fwd_h0 (Delta*B discretization) that also stores, for the backward
+ * pass, the state at the start of every chunk of SSM_SCAN_CHECKPOINT_STEPS steps:
+ *   checkpoints : [batch][nchunks][dim][dstate] float32, nchunks = ssm_scan_num_checkpoints(seqlen);
+ *                 chunk c holds h_{c*SSM_SCAN_CHECKPOINT_STEPS - 1} (h0, or zero, for c = 0).
+ * Required: checkpoints, plus what ssm_scan_fwd_h0 requires.  The lane-per-channel form is not
+ * used for this call.  Returns an ssm_status.
+ */
+#define SSM_SCAN_CHECKPOINT_STEPS 32
+int ssm_scan_num_checkpoints(int seqlen);
+int ssm_scan_fwd_train(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                       const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,
+                       void* y, float* last_state, float* checkpoints, int batch, int dim, int dstate, int seqlen,
+                       int io_dtype, void* stream);
+
+/*
+ * Backward pass of the scan (Delta*B discretization): the gradients of a loss given
+ * dout = dLoss/dout ([batch][dim][seqlen], io dtype), from the same inputs as the forward and the
+ * forward's checkpoints (ssm_scan_fwd_train).  Reverse-mode differentiation of the recurrence
+ * with the adjoint state lambda_t = dy_t C_t + Abar_{t+1} lambda_{t+1}; the pages state the
+ * speed-up of this layer for training (53ai.com article, sections on the hardware-aware
+ * algorithm and its training speed), the steps follow from the forward definitions.
+ *   du, ddelta, dz : [batch][dim][seqlen], io dtype; ddelta is with respect to the raw delta.
+ *                    dz is written only when z is given (nullable).
+ *   dA             : [dim][dstate] float32, summed over the batch.
+ *   dB, dC         : [batch][dstate][seqlen] float32, summed over the channels.
+ *   dD, ddt_bias   : [dim] float32 (written only when D / dt_bias are given; nullable).
+ *   dh0            : [batch][dim][dstate] float32, the gradient of the initial state (nullable).
+ * The accumulated outputs (dA, dB, dC, dD, ddt_bias) are overwritten, not added to; atomics
+ * make their last bits depend on the order of the additions.  No output may alias an input.
+ * Required: u, delta, A, B, C, checkpoints, dout, du, ddelta, dA, dB, dC.
+ * Returns an ssm_status.
+ */
+int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* dt_bias, int delta_softplus, const float* checkpoints,
+                 const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                 float* ddt_bias, float* dh0, int batch, int dim, int dstate, int seqlen, int io_dtype,
+                 void* stream);
 
 /*
  * Single-token decode step, state updated in place.

@@ -17,8 +17,8 @@ import torch
 from . import _native
 from ._native import SsmError, lib, status_string  # noqa: F401
 
-__all__ = ["ssm_scan_fwd", "ssm_state_update", "causal_conv1d_fwd", "causal_conv1d_update", "SsmError", "lib",
-           "status_string", "io_dtype_code"]
+__all__ = ["ssm_scan_fwd", "ssm_scan_bwd", "scan_num_checkpoints", "ssm_state_update", "causal_conv1d_fwd",
+           "causal_conv1d_update", "SsmError", "lib", "status_string", "io_dtype_code"]
 
 _IO = {torch.float32: _native.SSM_F32, torch.bfloat16: _native.SSM_BF16}
 _DISC = {"delta_b": _native.SSM_DISC_DELTA_B, "zoh": _native.SSM_DISC_ZOH}
@@ -56,13 +56,20 @@ def _stream(stream) -> int | None:
     return getattr(stream, "cuda_stream", stream) or None
 
 
+def scan_num_checkpoints(seqlen: int) -> int:
+    """Number of state checkpoints the training forward stores for a sequence of `seqlen` steps."""
+    return lib().ssm_scan_num_checkpoints(int(seqlen))
+
+
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, y=None, last_state=None,
-                 h0=None, return_last_state=True, stream=None, discretization="delta_b"):
-    """Selective scan forward (``ssm_scan_fwd`` / ``ssm_scan_fwd_h0`` / ``ssm_scan_fwd_ex`` of the C-ABI).
+                 h0=None, return_last_state=True, stream=None, discretization="delta_b", checkpoints=None):
+    """Selective scan forward (``ssm_scan_fwd`` / ``_h0`` / ``_ex`` / ``_train`` of the C-ABI).
 
     u, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (float32 or bfloat16, all the same);
     A: [dim, dstate], D, dt_bias: [dim], h0: [batch, dim, dstate] (float32).
     discretization: "delta_b" (Bbar = Delta B) or "zoh" (exact zero-order hold).
+    checkpoints: a float32 [batch, scan_num_checkpoints(L), dim, dstate] tensor to receive the
+    chunk-start states for ssm_scan_bwd (training forward; "delta_b" only).
     Returns (y, last_state); y has u's dtype, last_state is float32 (None if not requested).
     """
     disc = _disc(discretization)
@@ -90,13 +97,58 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus
         batch, dim, dstate, L, io, _stream(stream),
     ]
     h0p = _ptr(h0, torch.float32, (batch, dim, dstate), "h0")
-    if disc != _native.SSM_DISC_DELTA_B:
+    if checkpoints is not None:
+        if disc != _native.SSM_DISC_DELTA_B:
+            raise ValueError("the training forward (checkpoints) uses the delta_b discretization")
+        ck = _ptr(checkpoints, torch.float32, (batch, scan_num_checkpoints(L), dim, dstate), "checkpoints")
+        _native.check("ssm_scan_fwd_train", lib().ssm_scan_fwd_train(*args, h0p, tail[0], tail[1], ck, *tail[2:]))
+    elif disc != _native.SSM_DISC_DELTA_B:
         _native.check("ssm_scan_fwd_ex", lib().ssm_scan_fwd_ex(*args, h0p, *tail[:-1], disc, tail[-1]))
     elif h0 is None:
         _native.check("ssm_scan_fwd", lib().ssm_scan_fwd(*args, *tail))
     else:
         _native.check("ssm_scan_fwd_h0", lib().ssm_scan_fwd_h0(*args, h0p, *tail))
     return y, last_state
+
+
+def ssm_scan_bwd(u, delta, A, B, C, checkpoints, dout, D=None, z=None, dt_bias=None, delta_softplus=True,
+                 need_dh0=False, stream=None):
+    """Backward pass of the scan (``ssm_scan_bwd`` of the C-ABI) from the training forward's
+    checkpoints and dout = dLoss/dout [batch, dim, L].  Returns a dict of gradients: du, ddelta
+    (and dz when z is given) in u's dtype; dA, dB, dC (and dD, ddt_bias, dh0 when D, dt_bias are
+    given / need_dh0) in float32."""
+    batch, dim, L = u.shape
+    dstate = A.shape[1]
+    io = io_dtype_code(u.dtype)
+    f32 = dict(dtype=torch.float32, device=u.device)
+    g = {"du": torch.empty_like(u), "ddelta": torch.empty_like(u), "dA": torch.empty((dim, dstate), **f32),
+         "dB": torch.empty((batch, dstate, L), **f32), "dC": torch.empty((batch, dstate, L), **f32)}
+    if D is not None:
+        g["dD"] = torch.empty((dim,), **f32)
+    if z is not None:
+        g["dz"] = torch.empty_like(u)
+    if dt_bias is not None:
+        g["ddt_bias"] = torch.empty((dim,), **f32)
+    if need_dh0:
+        g["dh0"] = torch.empty((batch, dim, dstate), **f32)
+    st = lib().ssm_scan_bwd(
+        _ptr(u, u.dtype, (batch, dim, L), "u"),
+        _ptr(delta, u.dtype, (batch, dim, L), "delta"),
+        _ptr(A, torch.float32, (dim, dstate), "A"),
+        _ptr(B, u.dtype, (batch, dstate, L), "B"),
+        _ptr(C, u.dtype, (batch, dstate, L), "C"),
+        _ptr(D, torch.float32, (dim,), "D"),
+        _ptr(z, u.dtype, (batch, dim, L), "z"),
+        _ptr(dt_bias, torch.float32, (dim,), "dt_bias"),
+        int(bool(delta_softplus)),
+        _ptr(checkpoints, torch.float32, (batch, scan_num_checkpoints(L), dim, dstate), "checkpoints"),
+        _ptr(dout, u.dtype, (batch, dim, L), "dout"),
+        _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
+        _ptr(g.get("dz")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0")),
+        batch, dim, dstate, L, io, _stream(stream),
+    )
+    _native.check("ssm_scan_bwd", st)
+    return g
 
 
 def ssm_state_update(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, out=None, stream=None,

@@ -37,6 +37,11 @@ SIGNATURES = {
     "ssm_scan_fwd_ex": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
     "ssm_state_update": (_i, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _vp, _i, _i, _i, _i, _vp]),
     "ssm_state_update_ex": (_i, [_fp, _vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _vp, _i, _i, _i, _i, _i, _vp]),
+    "ssm_scan_num_checkpoints": (_i, [_i]),
+    "ssm_scan_fwd_train": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _fp, _fp, _i, _i, _i, _i, _i,
+                                _vp]),
+    "ssm_scan_bwd": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp, _fp,
+                          _fp, _i, _i, _i, _i, _i, _vp]),
     "ssm_causal_conv1d_fwd": (_i, [_vp, _fp, _fp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "ssm_causal_conv1d_update": (_i, [_vp, _vp, _fp, _fp, _vp, _i, _i, _i, _i, _i, _vp]),
 }

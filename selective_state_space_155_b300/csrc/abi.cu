@@ -33,10 +33,14 @@ const char* ssm_status_string(int status) {
   }
 }
 
-int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+}  // extern "C"
+
+namespace {
+
+int scan_fwd_common(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
                     const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
-                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
-                    void* stream) {
+                    float* last_state, float* ckpt, int batch, int dim, int dstate, int seqlen, int io_dtype,
+                    int discretization, void* stream) {
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
   if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
@@ -61,8 +65,43 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void
   a.softplus = delta_softplus ? 1 : 0;
   a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
   a.zoh = discretization == SSM_DISC_ZOH ? 1 : 0;
+  a.ckpt = ckpt;
   const cudaError_t err = ssm::launch_scan_fwd(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+}  // namespace
+
+extern "C" {
+
+int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
+                    void* stream) {
+  return scan_fwd_common(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, nullptr, batch, dim,
+                         dstate, seqlen, io_dtype, discretization, stream);
+}
+
+int ssm_scan_num_checkpoints(int seqlen) {
+  return seqlen > 0 ? (seqlen + SSM_SCAN_CHECKPOINT_STEPS - 1) / SSM_SCAN_CHECKPOINT_STEPS : 0;
+}
+
+int ssm_scan_fwd_train(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                       const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,
+                       void* y, float* last_state, float* checkpoints, int batch, int dim, int dstate, int seqlen,
+                       int io_dtype, void* stream) {
+  static_assert(SSM_SCAN_CHECKPOINT_STEPS == ssm::kScanChunk, "checkpoint interval");
+  if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (dstate > 16) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0 || seqlen == 0) {
+    return ssm_scan_fwd_ex(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, batch, dim, dstate,
+                           seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
+  }
+  if (!checkpoints) return SSM_ERR_NULL;
+  if (!aligned(checkpoints, 4)) return SSM_ERR_ALIGN;
+  return scan_fwd_common(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, checkpoints, batch,
+                         dim, dstate, seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
 }
 
 int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -113,6 +152,39 @@ int ssm_state_update(float* state, const void* x, const void* dt, const float* A
                      int dim, int dstate, int io_dtype, void* stream) {
   return ssm_state_update_ex(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, out, batch, dim, dstate, io_dtype,
                              SSM_DISC_DELTA_B, stream);
+}
+
+int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* dt_bias, int delta_softplus, const float* checkpoints,
+                 const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                 float* ddt_bias, float* dh0, int batch, int dim, int dstate, int seqlen, int io_dtype,
+                 void* stream) {
+  if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (dstate > 16) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0) return SSM_OK;
+  if (!A || !dA) return SSM_ERR_NULL;
+  if (seqlen > 0 && (!u || !delta || !B || !C || !checkpoints || !dout || !du || !ddelta || !dB || !dC))
+    return SSM_ERR_NULL;
+  const size_t es = io_size(io_dtype);
+  const void* io_ptrs[] = {u, delta, B, C, z, dout, du, ddelta, dz};
+  for (const void* p : io_ptrs)
+    if (!aligned(p, es)) return SSM_ERR_ALIGN;
+  const void* f_ptrs[] = {A, D, dt_bias, checkpoints, dA, dB, dC, dD, ddt_bias, dh0};
+  for (const void* p : f_ptrs)
+    if (!aligned(p, 4)) return SSM_ERR_ALIGN;
+  if ((long long)((dim + 31) / 32) * batch > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+
+  ssm::ScanBwdArgs a{};
+  a.u = u, a.delta = delta, a.A = A, a.B = B, a.C = C, a.D = D, a.z = z, a.dt_bias = dt_bias;
+  a.ckpt = checkpoints, a.dout = dout;
+  a.du = du, a.ddelta = ddelta, a.dA = dA, a.dB = dB, a.dC = dC, a.dD = dD, a.dz = dz, a.ddt_bias = ddt_bias;
+  a.dh0 = dh0;
+  a.batch = batch, a.dim = dim, a.dstate = dstate, a.seqlen = seqlen;
+  a.softplus = delta_softplus ? 1 : 0;
+  a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  const cudaError_t err = ssm::launch_scan_bwd(a, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
 int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias, const void* state_in, void* out,

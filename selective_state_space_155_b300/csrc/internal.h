@@ -45,7 +45,37 @@ struct ScanArgs {
   int batch, dim, dstate, seqlen;
   int softplus;
   int io;
-  int zoh;  // exact zero-order-hold Bbar instead of Delta * B
+  int zoh;      // exact zero-order-hold Bbar instead of Delta * B
+  float* ckpt;  // nullable: the state at the start of every kScanChunk-step chunk, for the backward
+};
+
+// Steps per chunk of the scan kernels; the forward's checkpoints are kScanChunk steps apart.
+constexpr int kScanChunk = 32;
+
+// Arguments of one backward pass of the scan; meaning as in ssm_scan.h.
+struct ScanBwdArgs {
+  const void* u;
+  const void* delta;
+  const float* A;
+  const void* B;
+  const void* C;
+  const float* D;
+  const void* z;
+  const float* dt_bias;
+  const float* ckpt;
+  const void* dout;
+  void* du;
+  void* ddelta;
+  float* dA;
+  float* dB;
+  float* dC;
+  float* dD;
+  void* dz;
+  float* ddt_bias;
+  float* dh0;
+  int batch, dim, dstate, seqlen;
+  int softplus;
+  int io;
 };
 
 // Arguments of one decode step; pointer and layout meaning as in ssm_scan.h.
@@ -109,6 +139,10 @@ cudaError_t launch_scan_fwd_lane(const ScanArgs& a, bool vec, cudaStream_t strea
 
 // Enqueue one decode step on `stream`.  Arguments are already validated.
 cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);
+
+// Enqueue the backward pass of the scan on `stream` (scan_bwd.cu): zero the accumulated
+// gradients, then one launch.  Arguments are already validated.
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);
 
 // Enqueue the causal conv1d / its decode step on `stream` (causal_conv1d.cu).  Arguments are
 // already validated (width 1..4).

@@ -1,0 +1,336 @@
+// Backward pass of the selective scan (Delta*B discretisation) for sm_103a.
+//
+// Forward, per batch row b, channel d, state n (see scan_fwd.cu):
+//   Delta_t = softplus(delta_t + dt_bias[d]),  a_t = exp(Delta_t A[d,n]),  h_t = a_t h_{t-1} + Delta_t B_t u_t
+//   y_t = sum_n C_t h_t + D u_t,  out_t = y_t silu(z_t)
+// Backward, for dout_t = dLoss/dout_t, with dy_t = dout_t silu(z_t) and the adjoint state
+//   lambda_t = dy_t C_t + a_{t+1} lambda_{t+1}      (run from t = L-1 down to 0):
+//   du_t     = dy_t D + Delta_t sum_n lambda_t B_t
+//   dDelta_t = sum_n lambda_t (A a_t h_{t-1} + B_t u_t),   ddelta_t = dDelta_t sigmoid(delta_t + dt_bias)
+//   dA       = sum_{b,t} lambda_t Delta_t a_t h_{t-1},     dB_t = sum_d lambda_t Delta_t u_t
+//   dC_t     = sum_d dy_t h_t,   dD = sum_{b,t} dy_t u_t,   dz_t = dout_t y_t silu'(z_t)
+//   ddt_bias = sum_{b,t} ddelta_t,   dh0 = a_0 lambda_0
+//
+// Layout of the work.  A CTA owns 32 channels of one batch row; lane (g, cw) of warp w holds
+// states 4g .. 4g+3 of channel 8w + cw (the forward's four-lanes-per-channel layout).  Chunks of
+// 32 steps are processed last to first.  For each chunk all 128 threads stage the per-(channel,
+// step) values (Delta, u, dy, the softplus and silu derivatives) and B, C into shared memory;
+// then every lane recomputes the chunk forward from the state the forward pass checkpointed at
+// its start, keeping the state at the start of each 8-step sub-chunk, and walks the sub-chunks
+// last to first: it recomputes the sub-chunk's 8 states and decay factors into registers and
+// runs the adjoint recurrence backwards over them.  Sums over a channel's 4 lanes (du, dDelta,
+// y) take two shuffles; dB and dC, shared by all channels, are reduce-scattered over the 8
+// channels of a warp by shuffles and added across the warps in shared memory, then added to the
+// float32 outputs with one atomic per (state, step) and CTA.  dA, dD and ddt_bias are added
+// across CTAs the same way; the launcher zeroes these accumulated outputs first.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "device_math.cuh"
+#include "internal.h"
+
+namespace ssm {
+namespace {
+
+constexpr int kK = kScanChunk;  // steps per chunk (the forward's checkpoint interval)
+constexpr int kS = 8;           // steps per register sub-chunk
+constexpr int kSub = kK / kS;
+constexpr int kCPB = 32;        // channels per CTA
+constexpr int kThr = 128;       // four warps; four lanes per channel, four states per lane
+constexpr int kTS = kK + 1;     // padded row stride of the per-(channel, step) tables
+static_assert(kK % kS == 0 && kK == 32, "chunk layout");
+
+struct __align__(16) BwdSmem {
+  float Bs[kK][16];
+  float Cs[kK][16];
+  float acc[kK][2][16];  // dB, dC of the chunk, summed over the CTA's channels
+  float dl[kCPB][kTS];   // Delta
+  float uu[kCPB][kTS];   // u
+  float dy[kCPB][kTS];   // dout * silu(z)  (dout without a gate)
+  float sg[kCPB][kTS];   // dDelta/ddelta: sigmoid(delta + dt_bias) with softplus, else 1
+  float qz[kCPB][kTS];   // dout * silu'(z)
+  float yv[kCPB][kTS];   // y before the gate, recomputed
+  float gu[kCPB][kTS];   // sum_n lambda B
+  float gd[kCPB][kTS];   // dDelta
+};
+
+template <typename T>
+__global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
+  __shared__ BwdSmem sm;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int dim = a.dim, N = a.dstate, L = a.seqlen;
+  const int nblk_d = (dim + kCPB - 1) / kCPB;
+  const int b = blockIdx.x / nblk_d;
+  const int d0 = (blockIdx.x % nblk_d) * kCPB;
+  const int nck = (L + kK - 1) / kK;
+  const T* gu_ = static_cast<const T*>(a.u);
+  const T* gdl = static_cast<const T*>(a.delta);
+  const T* gz = static_cast<const T*>(a.z);
+  const T* gdo = static_cast<const T*>(a.dout);
+  const T* gB = static_cast<const T*>(a.B);
+  const T* gC = static_cast<const T*>(a.C);
+
+  // recurrence role
+  const int cw = lane & 7, g = lane >> 3;
+  const int cl = warp * 8 + cw, d = d0 + cl;
+  const bool ch_ok = d < dim;
+  float An[4], An2[4], carry[4], dA[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int n = 4 * g + i;
+    An[i] = (ch_ok && n < N) ? a.A[size_t(d) * N + n] : 0.0f;
+    An2[i] = An[i] * kLog2e;
+    carry[i] = 0.0f;
+    dA[i] = 0.0f;
+  }
+  // epilogue role: channel tid / 4, steps (tid % 4) + 4j
+  const int ec = tid >> 2, eq = tid & 3;
+  const int ed = d0 + ec;
+  const bool e_ok = ed < dim;
+  const float eD = (e_ok && a.D) ? a.D[ed] : 0.0f;
+  float accD = 0.0f, accBias = 0.0f;
+  const bool has_z = gz != nullptr;
+
+  for (int k = nck - 1; k >= 0; --k) {
+    const int t0 = k * kK;
+    __syncthreads();  // the previous chunk is finished with every table
+    // ---- stage the chunk ----
+    for (int e = tid; e < kCPB * kK; e += kThr) {
+      const int c = e / kK, t = e % kK;
+      const int dd = d0 + c, tg = t0 + t;
+      float dl = 0.0f, u = 0.0f, dyv = 0.0f, sgv = 0.0f, qzv = 0.0f;
+      if (dd < dim && tg < L) {
+        const size_t off = (size_t(b) * dim + dd) * L + tg;
+        u = to_f32<T>(gu_[off]);
+        const float raw = to_f32<T>(gdl[off]) + (a.dt_bias ? a.dt_bias[dd] : 0.0f);
+        if (a.softplus) {
+          dl = softplus_f32(raw);
+          sgv = rcp_approx(1.0f + ex2_approx(-raw * kLog2e));
+        } else {
+          dl = raw;
+          sgv = 1.0f;
+        }
+        const float go = to_f32<T>(gdo[off]);
+        if (has_z) {
+          const float zz = to_f32<T>(gz[off]);
+          const float s = rcp_approx(1.0f + ex2_approx(-zz * kLog2e));
+          dyv = go * (zz * s);
+          qzv = go * (s * (1.0f + zz * (1.0f - s)));
+        } else {
+          dyv = go;
+        }
+      }
+      sm.dl[c][t] = dl, sm.uu[c][t] = u, sm.dy[c][t] = dyv, sm.sg[c][t] = sgv, sm.qz[c][t] = qzv;
+    }
+    for (int e = tid; e < 2 * 16 * kK; e += kThr) {
+      const int which = e / (16 * kK), r = e % (16 * kK), n = r / kK, t = r % kK;
+      const int tg = t0 + t;
+      const T* src = which ? gC : gB;
+      const float v = (n < N && tg < L) ? to_f32<T>(src[(size_t(b) * N + n) * L + tg]) : 0.0f;
+      (which ? sm.Cs : sm.Bs)[t][n] = v;
+    }
+    for (int e = tid; e < kK * 2 * 16; e += kThr) (&sm.acc[0][0][0])[e] = 0.0f;
+    __syncthreads();
+
+    // ---- recurrence role: forward recompute of the chunk, keeping each sub-chunk's start ----
+    float hs[kSub][4];
+    {
+      float h[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = 4 * g + i;
+        h[i] = (ch_ok && n < N) ? a.ckpt[((size_t(b) * nck + k) * dim + d) * N + n] : 0.0f;
+      }
+#pragma unroll
+      for (int sb = 0; sb < kSub; ++sb) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) hs[sb][i] = h[i];
+#pragma unroll
+        for (int j = 0; j < kS; ++j) {
+          const int t = sb * kS + j;
+          const float dl = sm.dl[cl][t], du = dl * sm.uu[cl][t];
+          const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
+          const float4 cc = *reinterpret_cast<const float4*>(&sm.Cs[t][4 * g]);
+          const float bv[4] = {bb.x, bb.y, bb.z, bb.w}, cv[4] = {cc.x, cc.y, cc.z, cc.w};
+          float yp = 0.0f;
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            h[i] = fmaf(ex2_approx(dl * An2[i]), h[i], du * bv[i]);
+            yp = fmaf(cv[i], h[i], yp);
+          }
+          if (has_z) {
+            yp += __shfl_xor_sync(0xffffffffu, yp, 8);
+            yp += __shfl_xor_sync(0xffffffffu, yp, 16);
+            if (g == 0) sm.yv[cl][t] = yp;
+          }
+        }
+      }
+    }
+
+    // ---- recurrence role: sub-chunks last to first, adjoint recurrence backwards ----
+    const int k1 = (cw >> 2) & 1, k2 = (cw >> 1) & 1, k3 = cw & 1;
+#pragma unroll
+    for (int sb = kSub - 1; sb >= 0; --sb) {
+      float ht[kS][4], at[kS][4];
+      {
+        float h[4] = {hs[sb][0], hs[sb][1], hs[sb][2], hs[sb][3]};
+#pragma unroll
+        for (int j = 0; j < kS; ++j) {
+          const int t = sb * kS + j;
+          const float dl = sm.dl[cl][t], du = dl * sm.uu[cl][t];
+          const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
+          const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            at[j][i] = ex2_approx(dl * An2[i]);
+            h[i] = fmaf(at[j][i], h[i], du * bv[i]);
+            ht[j][i] = h[i];
+          }
+        }
+      }
+#pragma unroll
+      for (int j = kS - 1; j >= 0; --j) {
+        const int t = sb * kS + j;
+        const float dl = sm.dl[cl][t], u = sm.uu[cl][t], dyv = sm.dy[cl][t];
+        const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
+        const float4 cc = *reinterpret_cast<const float4*>(&sm.Cs[t][4 * g]);
+        const float bv[4] = {bb.x, bb.y, bb.z, bb.w}, cv[4] = {cc.x, cc.y, cc.z, cc.w};
+        const float du = dl * u;
+        float gup = 0.0f, gdp = 0.0f, v[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float hp = j > 0 ? ht[j - 1][i] : hs[sb][i];  // h_{t-1}
+          const float lam = fmaf(dyv, cv[i], carry[i]);
+          const float ahp = at[j][i] * hp;
+          v[4 + i] = dyv * ht[j][i];  // dC
+          v[i] = lam * du;            // dB
+          gup = fmaf(lam, bv[i], gup);
+          gdp = fmaf(lam, fmaf(An[i], ahp, bv[i] * u), gdp);
+          dA[i] = fmaf(lam * dl, ahp, dA[i]);
+          carry[i] = lam * at[j][i];
+        }
+        // sums over the channel's four lanes
+        gup += __shfl_xor_sync(0xffffffffu, gup, 8);
+        gup += __shfl_xor_sync(0xffffffffu, gup, 16);
+        gdp += __shfl_xor_sync(0xffffffffu, gdp, 8);
+        gdp += __shfl_xor_sync(0xffffffffu, gdp, 16);
+        if (g == 0) sm.gu[cl][t] = gup, sm.gd[cl][t] = gdp;
+        // dB, dC summed over the warp's 8 channels: reduce-scatter over cw, lane keeps value cw
+        float w[4], x[2];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float send = k1 ? v[q] : v[4 + q], keep = k1 ? v[4 + q] : v[q];
+          w[q] = keep + __shfl_xor_sync(0xffffffffu, send, 4);
+        }
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float send = k2 ? w[q] : w[2 + q], keep = k2 ? w[2 + q] : w[q];
+          x[q] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
+        }
+        const float send = k3 ? x[0] : x[1], keep = k3 ? x[1] : x[0];
+        const float r = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+        atomicAdd(&sm.acc[t][cw >> 2][4 * g + (cw & 3)], r);
+      }
+    }
+    __syncthreads();
+
+    // ---- epilogue: per-element gradients of the chunk, and its dB, dC ----
+#pragma unroll
+    for (int j = 0; j < kK / 4; ++j) {
+      const int t = eq + 4 * j, tg = t0 + t;
+      if (e_ok && tg < L) {
+        const float dl = sm.dl[ec][t], u = sm.uu[ec][t], dyv = sm.dy[ec][t];
+        const float dut = fmaf(dyv, eD, dl * sm.gu[ec][t]);
+        const float ddl = sm.gd[ec][t] * sm.sg[ec][t];
+        const size_t off = (size_t(b) * dim + ed) * L + tg;
+        static_cast<T*>(a.du)[off] = from_f32<T>(dut);
+        static_cast<T*>(a.ddelta)[off] = from_f32<T>(ddl);
+        // dz = dout silu'(z) y, with y = C.h + D u before the gate
+        if (a.dz && has_z) static_cast<T*>(a.dz)[off] = from_f32<T>(sm.qz[ec][t] * fmaf(eD, u, sm.yv[ec][t]));
+        accD = fmaf(dyv, u, accD);
+        accBias += ddl;
+      }
+    }
+    for (int e = tid; e < kK * 2 * 16; e += kThr) {
+      const int t = e >> 5, which = (e >> 4) & 1, n = e & 15;
+      const int tg = t0 + t;
+      if (n < N && tg < L) atomicAdd((which ? a.dC : a.dB) + (size_t(b) * N + n) * L + tg, sm.acc[t][which][n]);
+    }
+  }
+
+  if (ch_ok) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int n = 4 * g + i;
+      if (n < N) {
+        atomicAdd(a.dA + size_t(d) * N + n, dA[i]);
+        if (a.dh0) a.dh0[(size_t(b) * dim + d) * N + n] = carry[i];
+      }
+    }
+  }
+  accD += __shfl_xor_sync(0xffffffffu, accD, 1);
+  accD += __shfl_xor_sync(0xffffffffu, accD, 2);
+  accBias += __shfl_xor_sync(0xffffffffu, accBias, 1);
+  accBias += __shfl_xor_sync(0xffffffffu, accBias, 2);
+  if (eq == 0 && e_ok) {
+    if (a.dD && a.D) atomicAdd(a.dD + ed, accD);
+    if (a.ddt_bias && a.dt_bias) atomicAdd(a.ddt_bias + ed, accBias);
+  }
+}
+
+// Zero up to four float32 buffers (the gradients the backward accumulates with atomics).
+struct ZeroSpans {
+  float* p[4];
+  long long n[4];
+};
+
+__global__ void __launch_bounds__(256) zero_kernel(const ZeroSpans z) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (int s = 0; s < 4; ++s)
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < z.n[s]; i += stride) z.p[s][i] = 0.0f;
+}
+
+}  // namespace
+
+cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream) {
+  ZeroSpans zs{};
+  zs.p[0] = a.dA, zs.n[0] = (long long)a.dim * a.dstate;
+  zs.p[1] = a.dB, zs.n[1] = (long long)a.batch * a.dstate * a.seqlen;
+  zs.p[2] = a.dC, zs.n[2] = (long long)a.batch * a.dstate * a.seqlen;
+  // dD and ddt_bias are zeroed only when they are accumulated
+  float* small = (a.dD && a.D) ? a.dD : nullptr;
+  zs.p[3] = small, zs.n[3] = small ? a.dim : 0;
+  {
+    void* params[] = {&zs};
+    cudaError_t err = cudaLaunchKernel(reinterpret_cast<const void*>(zero_kernel), dim3(592), dim3(256), params, 0,
+                                       stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (a.ddt_bias && a.dt_bias) {
+    ZeroSpans zb{};
+    zb.p[0] = a.ddt_bias, zb.n[0] = a.dim;
+    void* params[] = {&zb};
+    cudaError_t err = cudaLaunchKernel(reinterpret_cast<const void*>(zero_kernel), dim3(8), dim3(256), params, 0,
+                                       stream);
+    if (err != cudaSuccess) return err;
+  }
+  if (a.seqlen <= 0) {
+    // no steps: the initial state's gradient is zero
+    if (!a.dh0) return cudaSuccess;
+    ZeroSpans zh{};
+    zh.p[0] = a.dh0, zh.n[0] = (long long)a.batch * a.dim * a.dstate;
+    void* params[] = {&zh};
+    return cudaLaunchKernel(reinterpret_cast<const void*>(zero_kernel), dim3(592), dim3(256), params, 0, stream);
+  }
+  const long long nblk = (long long)((a.dim + kCPB - 1) / kCPB) * a.batch;
+  if (nblk <= 0) return cudaSuccess;
+  if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  ScanBwdArgs args = a;
+  void* params[] = {&args};
+  const void* fn = a.io == kF32 ? reinterpret_cast<const void*>(scan_bwd_kernel<float>)
+                                : reinterpret_cast<const void*>(scan_bwd_kernel<__nv_bfloat16>);
+  return cudaLaunchKernel(fn, dim3(unsigned(nblk)), dim3(kThr), params, 0, stream);
+}
+
+}  // namespace ssm

@@ -39,7 +39,7 @@
 namespace ssm {
 namespace {
 
-constexpr int kChunk = 32;  // steps per chunk
+constexpr int kChunk = kScanChunk;  // steps per chunk (the checkpoint interval)
 constexpr int kWin = 16;    // steps per recurrence window (readout partials held in registers)
 constexpr int kPrepWarps = 4;
 
@@ -406,6 +406,14 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   for (int k = 0; k < nchunks; ++k) {
     const int s = k & 1;
     const int t0 = k * kChunk;
+    if (a.ckpt && ch_ok) {
+      // the state at the start of chunk k, for the backward pass: [batch][chunk][dim][dstate]
+      float* cp = a.ckpt + ((size_t(b) * nchunks + k) * a.dim + d) * N;
+      const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (4 * g + i < N) cp[4 * g + i] = hv[i];
+    }
     bar_sync(kBarFull0 + s, NT);
     const float* Bs = tabBs(s);
     const float* Cs = tabCs(s);
@@ -577,7 +585,7 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
     const long long warps = ((long long)a.batch * a.dim + 31) / 32;
     lane = warps >= 8LL * sm_count();
   }
-  return (lane && !a.zoh) ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);
+  return (lane && !a.zoh && !a.ckpt) ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);
 }
 
 }  // namespace ssm

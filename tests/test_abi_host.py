@@ -31,7 +31,8 @@ def declared_functions():
 def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_scan_fwd_ex", "ssm_state_update",
-         "ssm_state_update_ex", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update"])
+         "ssm_state_update_ex", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update",
+         "ssm_scan_num_checkpoints", "ssm_scan_fwd_train", "ssm_scan_bwd"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -193,3 +194,41 @@ def test_conv_update_validation(lib, over, expected):
         a["batch"] = 0  # a valid call that launches nothing
     args = [a[k] for k in ("state", "x", "weight", "bias", "out", "batch", "dim", "width", "silu", "io", "stream")]
     assert lib.ssm_causal_conv1d_update(*args) == expected
+
+
+def test_num_checkpoints(lib):
+    assert [lib.ssm_scan_num_checkpoints(L) for L in (0, 1, 31, 32, 33, 2048, 65536)] == [0, 1, 1, 1, 2, 64, 2048]
+
+
+def test_train_forward_validation(lib):
+    args = scan_args()
+    train = args[:9] + [None] + args[9:11] + [None] + args[11:]
+    assert lib.ssm_scan_fwd_train(*train) == _native.SSM_ERR_NULL  # checkpoints missing
+    train = args[:9] + [None] + args[9:11] + [P + 2] + args[11:]
+    assert lib.ssm_scan_fwd_train(*train) == _native.SSM_ERR_ALIGN
+
+
+def bwd_args(**over):
+    a = dict(u=P, delta=P, A=P, B=P, C=P, D=P, z=P, dt_bias=P, softplus=1, ckpt=P, dout=P, du=P, ddelta=P, dA=P,
+             dB=P, dC=P, dD=P, dz=P, ddt_bias=P, dh0=None, batch=2, dim=3, dstate=16, seqlen=5, io=_native.SSM_BF16,
+             stream=None)
+    a.update(over)
+    return [a[k] for k in ("u", "delta", "A", "B", "C", "D", "z", "dt_bias", "softplus", "ckpt", "dout", "du",
+                           "ddelta", "dA", "dB", "dC", "dD", "dz", "ddt_bias", "dh0", "batch", "dim", "dstate",
+                           "seqlen", "io", "stream")]
+
+
+@pytest.mark.parametrize("over,expected", [
+    (dict(ckpt=None), _native.SSM_ERR_NULL),
+    (dict(dout=None), _native.SSM_ERR_NULL),
+    (dict(dB=None), _native.SSM_ERR_NULL),
+    (dict(dA=None), _native.SSM_ERR_NULL),
+    (dict(dstate=17), _native.SSM_ERR_UNSUPPORTED),
+    (dict(io=2), _native.SSM_ERR_DTYPE),
+    (dict(du=P + 1), _native.SSM_ERR_ALIGN),
+    (dict(dC=P + 2), _native.SSM_ERR_ALIGN),
+    (dict(batch=-1), _native.SSM_ERR_SHAPE),
+    (dict(batch=0), _native.SSM_OK),
+])
+def test_bwd_validation(lib, over, expected):
+    assert lib.ssm_scan_bwd(*bwd_args(**over)) == expected
