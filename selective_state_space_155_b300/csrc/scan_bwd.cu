@@ -33,6 +33,8 @@
 namespace ssm {
 namespace {
 
+__device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
+
 constexpr int kK = kScanChunk;  // steps per chunk (the forward's checkpoint interval)
 constexpr int kS = 8;           // steps per register sub-chunk
 constexpr int kSub = kK / kS;
@@ -56,7 +58,7 @@ struct __align__(16) BwdSmem {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
+__global__ void __launch_bounds__(kThr, 4) scan_bwd_kernel(const ScanBwdArgs a) {
   __shared__ BwdSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int dim = a.dim, N = a.dstate, L = a.seqlen;
@@ -84,7 +86,7 @@ __global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
     carry[i] = 0.0f;
     dA[i] = 0.0f;
   }
-  // epilogue role: channel tid / 4, steps (tid % 4) + 4j
+  // epilogue role: channel tid / 4, steps 8 (tid % 4) + j
   const int ec = tid >> 2, eq = tid & 3;
   const int ed = d0 + ec;
   const bool e_ok = ed < dim;
@@ -124,7 +126,8 @@ __global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
       sm.dl[c][t] = dl, sm.uu[c][t] = u, sm.dy[c][t] = dyv, sm.sg[c][t] = sgv, sm.qz[c][t] = qzv;
     }
     for (int e = tid; e < 2 * 16 * kK; e += kThr) {
-      const int which = e / (16 * kK), r = e % (16 * kK), n = r / kK, t = r % kK;
+      // consecutive threads take consecutive states of a step: conflict-free table stores
+      const int which = e / (16 * kK), r = e % (16 * kK), n = r % 16, t = r / 16;
       const int tg = t0 + t;
       const T* src = which ? gC : gB;
       const float v = (n < N && tg < L) ? to_f32<T>(src[(size_t(b) * N + n) * L + tg]) : 0.0f;
@@ -152,13 +155,15 @@ __global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
           const float dl = sm.dl[cl][t], du = dl * sm.uu[cl][t];
           const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
           const float4 cc = *reinterpret_cast<const float4*>(&sm.Cs[t][4 * g]);
-          const float bv[4] = {bb.x, bb.y, bb.z, bb.w}, cv[4] = {cc.x, cc.y, cc.z, cc.w};
-          float yp = 0.0f;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            h[i] = fmaf(ex2_approx(dl * An2[i]), h[i], du * bv[i]);
-            yp = fmaf(cv[i], h[i], yp);
-          }
+          const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
+          const float2 g01 = __fmul2_rn(dl2, f2(An2[0], An2[1])), g23 = __fmul2_rn(dl2, f2(An2[2], An2[3]));
+          const float2 h01 = __ffma2_rn(f2(ex2_approx(g01.x), ex2_approx(g01.y)), f2(h[0], h[1]),
+                                        __fmul2_rn(du2, f2(bb.x, bb.y)));
+          const float2 h23 = __ffma2_rn(f2(ex2_approx(g23.x), ex2_approx(g23.y)), f2(h[2], h[3]),
+                                        __fmul2_rn(du2, f2(bb.z, bb.w)));
+          h[0] = h01.x, h[1] = h01.y, h[2] = h23.x, h[3] = h23.y;
+          const float2 yp2 = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
+          float yp = yp2.x + yp2.y;
           if (has_z) {
             yp += __shfl_xor_sync(0xffffffffu, yp, 8);
             yp += __shfl_xor_sync(0xffffffffu, yp, 16);
@@ -172,21 +177,19 @@ __global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
     const int k1 = (cw >> 2) & 1, k2 = (cw >> 1) & 1, k3 = cw & 1;
 #pragma unroll
     for (int sb = kSub - 1; sb >= 0; --sb) {
-      float ht[kS][4], at[kS][4];
+      float2 ht[kS][2];  // states after each step of the sub-chunk, as (0,1), (2,3) pairs
       {
-        float h[4] = {hs[sb][0], hs[sb][1], hs[sb][2], hs[sb][3]};
+        float2 h01 = f2(hs[sb][0], hs[sb][1]), h23 = f2(hs[sb][2], hs[sb][3]);
 #pragma unroll
         for (int j = 0; j < kS; ++j) {
           const int t = sb * kS + j;
           const float dl = sm.dl[cl][t], du = dl * sm.uu[cl][t];
           const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
-          const float bv[4] = {bb.x, bb.y, bb.z, bb.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            at[j][i] = ex2_approx(dl * An2[i]);
-            h[i] = fmaf(at[j][i], h[i], du * bv[i]);
-            ht[j][i] = h[i];
-          }
+          const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
+          const float2 g01 = __fmul2_rn(dl2, f2(An2[0], An2[1])), g23 = __fmul2_rn(dl2, f2(An2[2], An2[3]));
+          h01 = __ffma2_rn(f2(ex2_approx(g01.x), ex2_approx(g01.y)), h01, __fmul2_rn(du2, f2(bb.x, bb.y)));
+          h23 = __ffma2_rn(f2(ex2_approx(g23.x), ex2_approx(g23.y)), h23, __fmul2_rn(du2, f2(bb.z, bb.w)));
+          ht[j][0] = h01, ht[j][1] = h23;
         }
       }
 #pragma unroll
@@ -195,21 +198,29 @@ __global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
         const float dl = sm.dl[cl][t], u = sm.uu[cl][t], dyv = sm.dy[cl][t];
         const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
         const float4 cc = *reinterpret_cast<const float4*>(&sm.Cs[t][4 * g]);
-        const float bv[4] = {bb.x, bb.y, bb.z, bb.w}, cv[4] = {cc.x, cc.y, cc.z, cc.w};
-        const float du = dl * u;
-        float gup = 0.0f, gdp = 0.0f, v[8];
+        const float2 dl2 = f2(dl, dl), du2 = f2(dl * u, dl * u), u2 = f2(u, u), dy2 = f2(dyv, dyv);
+        const float2 bp[2] = {f2(bb.x, bb.y), f2(bb.z, bb.w)}, cp[2] = {f2(cc.x, cc.y), f2(cc.z, cc.w)};
+        float2 gu2 = f2(0.0f, 0.0f), gd2 = f2(0.0f, 0.0f);
+        float v[8];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float hp = j > 0 ? ht[j - 1][i] : hs[sb][i];  // h_{t-1}
-          const float lam = fmaf(dyv, cv[i], carry[i]);
-          const float ahp = at[j][i] * hp;
-          v[4 + i] = dyv * ht[j][i];  // dC
-          v[i] = lam * du;            // dB
-          gup = fmaf(lam, bv[i], gup);
-          gdp = fmaf(lam, fmaf(An[i], ahp, bv[i] * u), gdp);
-          dA[i] = fmaf(lam * dl, ahp, dA[i]);
-          carry[i] = lam * at[j][i];
+        for (int p = 0; p < 2; ++p) {
+          const float2 Ap = f2(An[2 * p], An[2 * p + 1]);
+          const float2 gp = __fmul2_rn(dl2, f2(An2[2 * p], An2[2 * p + 1]));
+          const float2 ap = f2(ex2_approx(gp.x), ex2_approx(gp.y));  // a_t, as in the recompute
+          const float2 hp = j > 0 ? ht[j - 1][p] : f2(hs[sb][2 * p], hs[sb][2 * p + 1]);  // h_{t-1}
+          const float2 lam = __ffma2_rn(dy2, cp[p], f2(carry[2 * p], carry[2 * p + 1]));
+          const float2 ahp = __fmul2_rn(ap, hp);
+          const float2 vc = __fmul2_rn(dy2, ht[j][p]);  // dC
+          const float2 vb = __fmul2_rn(lam, du2);       // dB
+          v[2 * p] = vb.x, v[2 * p + 1] = vb.y, v[4 + 2 * p] = vc.x, v[4 + 2 * p + 1] = vc.y;
+          gu2 = __ffma2_rn(lam, bp[p], gu2);
+          gd2 = __ffma2_rn(lam, __ffma2_rn(Ap, ahp, __fmul2_rn(bp[p], u2)), gd2);
+          const float2 da = __ffma2_rn(__fmul2_rn(lam, dl2), ahp, f2(dA[2 * p], dA[2 * p + 1]));
+          dA[2 * p] = da.x, dA[2 * p + 1] = da.y;
+          const float2 cr = __fmul2_rn(lam, ap);
+          carry[2 * p] = cr.x, carry[2 * p + 1] = cr.y;
         }
+        float gup = gu2.x + gu2.y, gdp = gd2.x + gd2.y;
         // sums over the channel's four lanes
         gup += __shfl_xor_sync(0xffffffffu, gup, 8);
         gup += __shfl_xor_sync(0xffffffffu, gup, 16);
@@ -238,7 +249,7 @@ __global__ void __launch_bounds__(kThr) scan_bwd_kernel(const ScanBwdArgs a) {
     // ---- epilogue: per-element gradients of the chunk, and its dB, dC ----
 #pragma unroll
     for (int j = 0; j < kK / 4; ++j) {
-      const int t = eq + 4 * j, tg = t0 + t;
+      const int t = eq * (kK / 4) + j, tg = t0 + t;
       if (e_ok && tg < L) {
         const float dl = sm.dl[ec][t], u = sm.uu[ec][t], dyv = sm.dy[ec][t];
         const float dut = fmaf(dyv, eD, dl * sm.gu[ec][t]);
