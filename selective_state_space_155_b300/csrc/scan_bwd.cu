@@ -14,7 +14,8 @@
 // Layout of the work.  A CTA owns 32 channels of one batch row; lane (g, cw) of warp w holds
 // states 4g .. 4g+3 of channel 8w + cw (the forward's four-lanes-per-channel layout).  Chunks of
 // 32 steps are processed last to first.  For each chunk all 128 threads stage the per-(channel,
-// step) values (Delta, u, dy, the softplus and silu derivatives) and B, C into shared memory;
+// step) values (Delta, u, dy, the softplus and silu derivatives) and B, C into shared memory from
+// registers that were loaded while the previous chunk was being computed;
 // then every lane recomputes the chunk forward from the state the forward pass checkpointed at
 // its start, keeping the state at the start of each 8-step sub-chunk, and walks the sub-chunks
 // last to first: it recomputes the sub-chunk's 8 states and decay factors into registers and
@@ -58,7 +59,7 @@ struct __align__(16) BwdSmem {
 };
 
 template <typename T>
-__global__ void __launch_bounds__(kThr, 4) scan_bwd_kernel(const ScanBwdArgs a) {
+__global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) {
   __shared__ BwdSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int dim = a.dim, N = a.dstate, L = a.seqlen;
@@ -94,57 +95,90 @@ __global__ void __launch_bounds__(kThr, 4) scan_bwd_kernel(const ScanBwdArgs a) 
   float accD = 0.0f, accBias = 0.0f;
   const bool has_z = gz != nullptr;
 
+  // Raw inputs of the next chunk to process (the previous one in time), loaded into registers
+  // while the current chunk is being computed.  Thread tid stages step tid % 32 of channels
+  // tid / 32 + 4j (j < 8), and (B or C, state, step) items tid + 128j (j < 8).
+  constexpr int kEl = kCPB * kK / kThr, kBC = 2 * 16 * kK / kThr;
+  static_assert(kEl == 8 && kBC == 8, "staging split");
+  T r_u[kEl], r_d[kEl], r_z[kEl], r_g[kEl], r_bc[kBC];
+  float r_ck[4];
+  auto prefetch = [&](int k) {
+    const int t0 = k * kK, t = tid & (kK - 1), tg = t0 + t;
+#pragma unroll
+    for (int j = 0; j < kEl; ++j) {
+      const int dd = d0 + (tid >> 5) + 4 * j;
+      const bool ok = dd < dim && tg < L;
+      const size_t off = (size_t(b) * dim + (ok ? dd : 0)) * L + (ok ? tg : 0);
+      r_u[j] = ok ? gu_[off] : from_f32<T>(0.0f);
+      r_d[j] = ok ? gdl[off] : from_f32<T>(0.0f);
+      r_z[j] = (ok && has_z) ? gz[off] : from_f32<T>(0.0f);
+      r_g[j] = ok ? gdo[off] : from_f32<T>(0.0f);
+    }
+#pragma unroll
+    for (int j = 0; j < kBC; ++j) {
+      // consecutive threads take consecutive states of a step: conflict-free table stores later
+      const int e = tid + kThr * j;
+      const int which = e / (16 * kK), r = e % (16 * kK), n = r % 16, tt = r / 16;
+      const int tgb = t0 + tt;
+      const T* src = which ? gC : gB;
+      r_bc[j] = (n < N && tgb < L) ? src[(size_t(b) * N + n) * L + tgb] : from_f32<T>(0.0f);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int n = 4 * g + i;
+      r_ck[i] = (ch_ok && n < N) ? a.ckpt[((size_t(b) * nck + k) * dim + d) * N + n] : 0.0f;
+    }
+  };
+  prefetch(nck - 1);
+
   for (int k = nck - 1; k >= 0; --k) {
     const int t0 = k * kK;
     __syncthreads();  // the previous chunk is finished with every table
-    // ---- stage the chunk ----
-    for (int e = tid; e < kCPB * kK; e += kThr) {
-      const int c = e / kK, t = e % kK;
-      const int dd = d0 + c, tg = t0 + t;
-      float dl = 0.0f, u = 0.0f, dyv = 0.0f, sgv = 0.0f, qzv = 0.0f;
-      if (dd < dim && tg < L) {
-        const size_t off = (size_t(b) * dim + dd) * L + tg;
-        u = to_f32<T>(gu_[off]);
-        const float raw = to_f32<T>(gdl[off]) + (a.dt_bias ? a.dt_bias[dd] : 0.0f);
-        if (a.softplus) {
-          dl = softplus_f32(raw);
-          sgv = rcp_approx(1.0f + ex2_approx(-raw * kLog2e));
-        } else {
-          dl = raw;
-          sgv = 1.0f;
+    // ---- stage the chunk from the prefetched registers ----
+    {
+      const int t = tid & (kK - 1), tg = t0 + t;
+#pragma unroll
+      for (int j = 0; j < kEl; ++j) {
+        const int c = (tid >> 5) + 4 * j, dd = d0 + c;
+        float dl = 0.0f, u = 0.0f, dyv = 0.0f, sgv = 0.0f, qzv = 0.0f;
+        if (dd < dim && tg < L) {
+          u = to_f32<T>(r_u[j]);
+          const float raw = to_f32<T>(r_d[j]) + (a.dt_bias ? a.dt_bias[dd] : 0.0f);
+          if (a.softplus) {
+            dl = softplus_f32(raw);
+            sgv = rcp_approx(1.0f + ex2_approx(-raw * kLog2e));
+          } else {
+            dl = raw;
+            sgv = 1.0f;
+          }
+          const float go = to_f32<T>(r_g[j]);
+          if (has_z) {
+            const float zz = to_f32<T>(r_z[j]);
+            const float s = rcp_approx(1.0f + ex2_approx(-zz * kLog2e));
+            dyv = go * (zz * s);
+            qzv = go * (s * (1.0f + zz * (1.0f - s)));
+          } else {
+            dyv = go;
+          }
         }
-        const float go = to_f32<T>(gdo[off]);
-        if (has_z) {
-          const float zz = to_f32<T>(gz[off]);
-          const float s = rcp_approx(1.0f + ex2_approx(-zz * kLog2e));
-          dyv = go * (zz * s);
-          qzv = go * (s * (1.0f + zz * (1.0f - s)));
-        } else {
-          dyv = go;
-        }
+        sm.dl[c][t] = dl, sm.uu[c][t] = u, sm.dy[c][t] = dyv, sm.sg[c][t] = sgv, sm.qz[c][t] = qzv;
       }
-      sm.dl[c][t] = dl, sm.uu[c][t] = u, sm.dy[c][t] = dyv, sm.sg[c][t] = sgv, sm.qz[c][t] = qzv;
-    }
-    for (int e = tid; e < 2 * 16 * kK; e += kThr) {
-      // consecutive threads take consecutive states of a step: conflict-free table stores
-      const int which = e / (16 * kK), r = e % (16 * kK), n = r % 16, t = r / 16;
-      const int tg = t0 + t;
-      const T* src = which ? gC : gB;
-      const float v = (n < N && tg < L) ? to_f32<T>(src[(size_t(b) * N + n) * L + tg]) : 0.0f;
-      (which ? sm.Cs : sm.Bs)[t][n] = v;
+#pragma unroll
+      for (int j = 0; j < kBC; ++j) {
+        const int e = tid + kThr * j;
+        const int which = e / (16 * kK), r = e % (16 * kK), n = r % 16, tt = r / 16;
+        (which ? sm.Cs : sm.Bs)[tt][n] = to_f32<T>(r_bc[j]);
+      }
     }
     for (int e = tid; e < kK * 2 * 16; e += kThr) (&sm.acc[0][0][0])[e] = 0.0f;
+    float ck0[4] = {r_ck[0], r_ck[1], r_ck[2], r_ck[3]};
+    if (k > 0) prefetch(k - 1);  // in flight while this chunk is computed
     __syncthreads();
 
     // ---- recurrence role: forward recompute of the chunk, keeping each sub-chunk's start ----
     float hs[kSub][4];
     {
-      float h[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int n = 4 * g + i;
-        h[i] = (ch_ok && n < N) ? a.ckpt[((size_t(b) * nck + k) * dim + d) * N + n] : 0.0f;
-      }
+      float h[4] = {ck0[0], ck0[1], ck0[2], ck0[3]};
 #pragma unroll
       for (int sb = 0; sb < kSub; ++sb) {
 #pragma unroll
