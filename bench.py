@@ -409,7 +409,8 @@ def run_zoh(w: wl.ScanWorkload, device, steps=200, warmup=5):
     hbm, _ = measured_peaks()
     gbs = w.algorithmic_bytes() / (ms * 1e-3) / 1e9
     return {"workload": w.name, "discretization": "zoh", "us_per_step": ms * 1e3,
-            "elements_per_s": w.elements / (ms * 1e-3), "hbm_gbs": gbs, "frac_of_hbm": gbs / hbm, "steps": steps}
+            "elements_per_s": w.elements / (ms * 1e-3), "hbm_gbs": gbs, "frac_of_hbm": gbs / hbm, "steps": steps,
+            "traffic": committed_traffic("scan_fwd_kernel_zoh")}
 
 
 def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_COPIES):
@@ -443,6 +444,7 @@ def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_CO
     torch.cuda.empty_cache()
     return {"workload": w.name, "fwd_train_us": ms_f * 1e3, "bwd_us": ms_b * 1e3, "step_us": (ms_f + ms_b) * 1e3,
             "elements_per_s": w.elements / ((ms_f + ms_b) * 1e-3), "steps": steps,
+            "bwd_traffic": committed_traffic("scan_bwd_kernel"),
             "note": "backward allocates its gradient tensors each call (torch caching allocator)"}
 
 
@@ -468,7 +470,8 @@ def run_conv(w: wl.ScanWorkload, device, steps=300, warmup=5, copies=ROTATING_CO
     torch.cuda.empty_cache()
     return {"workload": f"conv1d_{w.io}_b{w.batch}_d{w.dim}_l{w.seqlen}_w{width}_silu", "us_per_step": ms * 1e3,
             "elements_per_s": w.elements / (ms * 1e-3), "algorithmic_bytes_per_launch": nbytes, "hbm_gbs": gbs,
-            "frac_of_hbm": gbs / hbm, "steps": steps, "kernel": "conv_vec_kernel"}
+            "frac_of_hbm": gbs / hbm, "steps": steps, "kernel": "conv_vec_kernel",
+            "traffic": committed_traffic("conv_vec_kernel")}
 
 
 def run_decode(device, steps_graph=3, warmup=1):
@@ -501,6 +504,7 @@ def run_decode(device, steps_graph=3, warmup=1):
         "cold_l2_frac_of_hbm": bytes_step / (cold_ms * 1e-3) / 1e9 / hbm,
         "algorithmic_bytes_per_step": bytes_step, "peak": hbm, "peak_source": src,
         "note": "the 84 MB float32 state fits in L2, so back-to-back steps can exceed HBM bandwidth",
+        "traffic": committed_traffic("state_update_kernel"),
     }
 
 
