@@ -327,7 +327,7 @@ def cpu_baseline(w: wl.ScanWorkload, target_s: float = 12.0):
     cores = cpu_cores()
     sample = oracle_sample(w, channels=w.dim)
     t1 = time_oracle(sample, cores)
-    reps = int(max(1, min(200, target_s / max(t1, 1e-6))))
+    reps = int(max(1, min(5000, target_s / max(t1, 1e-6))))
     t = time_oracle(sample, cores, reps=reps)
     elems = w.dim * w.seqlen
     return {"value": elems / t, "unit": "elements/s", "cores": cores, "kind": "oracle",
