@@ -144,6 +144,73 @@ __global__ void __launch_bounds__(kThreads) conv_vec_kernel(const ConvArgs a) {
   }
 }
 
+// Rows of an even number of vectors: each thread takes two consecutive vectors of one row (32
+// contiguous bytes), so the channel's filter is loaded once and the second vector's W-1 earlier
+// inputs are the first vector's last ones; only the first vector needs the previous lane.
+template <typename T, int W>
+__global__ void __launch_bounds__(kThreads) conv_pair_kernel(const ConvArgs a) {
+  constexpr int E = Vec16<T>::N, H = W - 1;
+  const long long vpr = a.seqlen / E;  // even
+  const long long npair = (long long)a.batch * a.dim * (vpr / 2);
+  const long long pidx = (long long)blockIdx.x * kThreads + threadIdx.x;
+  const bool active = pidx < npair;
+  const long long v = 2 * pidx;  // first vector; v + 1 is in the same row
+  const int lane = threadIdx.x & 31;
+  const T* x = static_cast<const T*>(a.x);
+
+  float xv[2][E];
+#pragma unroll
+  for (int i = 0; i < 2; ++i)
+#pragma unroll
+    for (int e = 0; e < E; ++e) xv[i][e] = 0.0f;
+  if (active) {
+    Vec16<T>::load(x + v * E, xv[0]);
+    Vec16<T>::load(x + (v + 1) * E, xv[1]);
+  }
+  float hl[H > 0 ? H : 1];
+#pragma unroll
+  for (int h = 0; h < H; ++h) hl[h] = __shfl_up_sync(0xffffffffu, xv[1][E - H + h], 1);
+  if (!active) return;
+  long long row, j, dq, dr;
+  divmod(v, a.div_row, row, j);  // div_row divides by vpr here
+  if (j == 0) {
+    const T* si = static_cast<const T*>(a.state_in);
+#pragma unroll
+    for (int h = 0; h < H; ++h) hl[h] = si ? to_f32<T>(si[row * H + h]) : 0.0f;
+  } else if (lane == 0) {
+#pragma unroll
+    for (int h = 0; h < H; ++h) hl[h] = to_f32<T>(x[v * E - H + h]);
+  }
+  divmod(row, a.div_dim, dq, dr);
+  const int d = int(dr);
+  float w[W];
+#pragma unroll
+  for (int k = 0; k < W; ++k) w[k] = __ldg(a.weight + (size_t)d * W + k);
+  const float bias = a.bias ? __ldg(a.bias + d) : 0.0f;
+  const bool silu = a.silu != 0;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    float ov[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float acc = bias;
+#pragma unroll
+      for (int k = 0; k < W; ++k) {
+        const int s = e - H + k;  // position relative to xv[i][0]
+        const float in = s >= 0 ? xv[i][s] : (i == 0 ? hl[H + s] : xv[0][E + s]);
+        acc = fmaf(w[k], in, acc);
+      }
+      ov[e] = act(acc, silu);
+    }
+    Vec16<T>::store(static_cast<T*>(a.out) + (v + i) * E, ov);
+  }
+  if (a.state_out && j + 2 == vpr) {
+    T* so = static_cast<T*>(a.state_out);
+#pragma unroll
+    for (int h = 0; h < H; ++h) so[row * H + h] = from_f32<T>(xv[1][E - H + h]);
+  }
+}
+
 // One thread per output element, then one per state slot (rows x H items after the outputs).
 template <typename T, int W>
 __global__ void __launch_bounds__(kThreads) conv_scalar_kernel(const ConvArgs a) {
@@ -200,17 +267,20 @@ template <typename T, int W>
 cudaError_t launch_fwd(const ConvArgs& a, bool vec, cudaStream_t stream) {
   const long long rows = (long long)a.batch * a.dim;
   constexpr int E = 16 / sizeof(T);
-  const long long items = vec ? rows * (a.seqlen / E) : rows * a.seqlen + (a.state_out ? rows * (W - 1) : 0);
+  const long long vpr = a.seqlen / E;
+  const bool pair = vec && vpr % 2 == 0;
+  const long long items = vec ? rows * vpr : rows * a.seqlen + (a.state_out ? rows * (W - 1) : 0);
   if (items <= 0) return cudaSuccess;
-  const long long per_block = vec ? (long long)kThreads * kVecPerThread : kThreads;
+  const long long per_block = pair ? 2LL * kThreads : (vec ? (long long)kThreads * kVecPerThread : kThreads);
   const long long nblk = (items + per_block - 1) / per_block;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   ConvArgs args = a;
   args.div_row = make_fastdiv(uint32_t(vec ? a.seqlen / E : (a.seqlen > 0 ? a.seqlen : 1)));
   args.div_dim = make_fastdiv(uint32_t(a.dim));
   void* params[] = {&args};
-  const void* fn = vec ? reinterpret_cast<const void*>(conv_vec_kernel<T, W>)
-                       : reinterpret_cast<const void*>(conv_scalar_kernel<T, W>);
+  const void* fn = pair  ? reinterpret_cast<const void*>(conv_pair_kernel<T, W>)
+                   : vec ? reinterpret_cast<const void*>(conv_vec_kernel<T, W>)
+                         : reinterpret_cast<const void*>(conv_scalar_kernel<T, W>);
   return cudaLaunchKernel(fn, dim3(unsigned(nblk)), dim3(kThreads), params, 0, stream);
 }
 
