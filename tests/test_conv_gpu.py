@@ -43,6 +43,8 @@ def test_mid_shape_full_parity():
     (2, 33, 64, 4, "bf16"), (2, 33, 64, 4, "f32"), (1, 7, 61, 4, "bf16"), (3, 5, 2, 4, "f32"),
     (2, 9, 1, 3, "bf16"), (2, 40, 96, 1, "bf16"), (2, 40, 96, 2, "f32"), (1, 300, 8, 3, "bf16"),
     (4, 17, 1000, 4, "f32"), (1, 1, 3, 4, "bf16"),
+    # rows of an odd number of 16-byte vectors (the strided two-vector form), and of one vector
+    (2, 37, 40, 4, "bf16"), (3, 9, 12, 3, "f32"), (2, 70, 8, 4, "bf16"), (1, 33, 4, 2, "f32"),
 ], ids=lambda s: "b{}_d{}_l{}_w{}_{}".format(*s))
 @pytest.mark.parametrize("silu,with_state", [(True, True), (False, False), (True, False)])
 def test_edge_shapes(shape, silu, with_state):
