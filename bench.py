@@ -321,7 +321,7 @@ def time_oracle(sample, nthreads, reps=1):
     return (time.perf_counter() - t0) / reps
 
 
-def cpu_baseline(w: wl.ScanWorkload, target_s: float = 12.0):
+def cpu_baseline(w: wl.ScanWorkload, target_s: float = 15.0):
     """Time the oracle on the host cores for about `target_s` seconds: batch row 0 of the workload
     (all its channels, the full sequence), repeated until the budget is used."""
     cores = cpu_cores()
@@ -470,8 +470,8 @@ def run_conv(w: wl.ScanWorkload, device, steps=300, warmup=5, copies=ROTATING_CO
     torch.cuda.empty_cache()
     return {"workload": f"conv1d_{w.io}_b{w.batch}_d{w.dim}_l{w.seqlen}_w{width}_silu", "us_per_step": ms * 1e3,
             "elements_per_s": w.elements / (ms * 1e-3), "algorithmic_bytes_per_launch": nbytes, "hbm_gbs": gbs,
-            "frac_of_hbm": gbs / hbm, "steps": steps, "kernel": "conv_vec_kernel",
-            "traffic": committed_traffic("conv_vec_kernel")}
+            "frac_of_hbm": gbs / hbm, "steps": steps, "kernel": "conv_pair_kernel",
+            "traffic": committed_traffic("conv_pair_kernel")}
 
 
 def run_decode(device, steps_graph=3, warmup=1):
