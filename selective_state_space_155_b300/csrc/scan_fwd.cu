@@ -22,8 +22,13 @@
 //    16/R consecutive steps of channel c, (y + D u) * silu(z), stored straight to HBM.
 //  * Hand-off is by named barriers (bar.arrive / bar.sync; no spin loops): table stage s is FULL
 //    once the prep warps arrive on it and EMPTY once the recurrence warps are done with it.
+//  * For dstate 9..16 (four recurrence warps, one warpgroup each) setmaxnreg moves registers from
+//    the prep warpgroup (48) to the recurrence warpgroup (112), whose unrolled window is the long
+//    pole; the kernel is launched at 80 registers per thread and the shares add up to that.
 //  * Padded states (n >= dstate) have A = 0 and B = C = 0; padded steps (t >= seqlen) have
 //    Delta = 0.  Both leave the state unchanged, so one code path serves every size.
+//  * With a checkpoint buffer (the training forward), the recurrence lanes also store the state
+//    at the start of every chunk, which is what the backward pass restarts from.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
