@@ -13,6 +13,7 @@ Extra objects on the line:
   roofline      the scan kernel against the measured HBM copy bandwidth (algorithmic bytes
                 per launch / average launch time), plus its DRAM traffic from the committed ncu
                 capture;
+  roofline_alu  the same launches against the special-function (MUFU) peak, the scan's co-bound;
   e2e           the same metric through the public API with pinned host buffers: host->device
                 copy of the step's inputs, the scan, device->host copy of y and the final state;
   cpu_baseline  the float64 oracle on the host cores (reported baseline, not a target);
@@ -400,6 +401,31 @@ def run_e2e(w, device, steps, warmup, dist):
     return ms, h2d, d2h
 
 
+# The scan is a co-bound of HBM and the special-function unit: per element the recurrence takes
+# one ex2 per state and the step size and gate one softplus (ex2 + lg2) and one silu (ex2 + rcp).
+# The MUFU rate on this machine's B300 was measured at 32 operations per clock per SM (a probe of
+# dependent-free ex2.approx), so the peak is 32 x SMs x the maximum SM clock.
+MUFU_OPS_PER_CLK_PER_SM = 32
+B300_SMS = 148
+
+
+def alu_roofline(w: wl.ScanWorkload, ms: float):
+    """The scan's MUFU operations per second against the MUFU peak (a secondary roofline)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            sm_mhz = float(json.load(f)["sm_max_mhz"])
+    except (OSError, KeyError, ValueError):
+        sm_mhz = 2032.0
+    sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else B300_SMS
+    per_element = w.dstate + (4 if w.gate else 2)  # ex2 per state; softplus 2; silu 2
+    achieved = w.elements * per_element / (ms * 1e-3) / 1e9
+    peak = MUFU_OPS_PER_CLK_PER_SM * sms * sm_mhz * 1e6 / 1e9
+    return {"bound": "alu", "what": "MUFU ex2/lg2/rcp operations", "per_element": per_element,
+            "achieved": achieved, "peak": peak, "unit": "Gop/s", "frac": achieved / peak,
+            "peak_source": f"{MUFU_OPS_PER_CLK_PER_SM} ops/clk/SM (measured by a probe on this pool) x {sms} SMs x "
+                           f"{sm_mhz:.0f} MHz"}
+
+
 def run_zoh(w: wl.ScanWorkload, device, steps=200, warmup=5):
     """The same scan workload with the exact zero-order-hold discretisation (same bytes moved)."""
     run = ScanRun(w, device, discretization="zoh")
@@ -622,6 +648,7 @@ def main(argv=None):
                      "algorithmic_bytes_per_launch": bytes_launch},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(),
+        "roofline_alu": alu_roofline(w, ms),
     }
     if not args.no_e2e:
         e2e_ms, h2d, d2h = run_e2e(w, device, max(3, min(args.steps, 20)), 2, dist)
