@@ -313,6 +313,17 @@ def cpu_cores():
         return os.cpu_count() or 1
 
 
+def cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
 def time_oracle(sample, nthreads, reps=1):
     from oracle import oracle
     t0 = time.perf_counter()
@@ -331,9 +342,15 @@ def cpu_baseline(w: wl.ScanWorkload, target_s: float = 15.0):
     reps = int(max(1, min(5000, target_s / max(t1, 1e-6))))
     t = time_oracle(sample, cores, reps=reps)
     elems = w.dim * w.seqlen
+    # one thread on a smaller slice of the same row (64 channels), for the per-core figure
+    small = oracle_sample(w, channels=64)
+    t_one = time_oracle(small, 1, reps=3)
     return {"value": elems / t, "unit": "elements/s", "cores": cores, "kind": "oracle",
             "sample": f"batch row 0 of {w.name} ({w.dim} channels x {w.seqlen} steps) x {reps} repetitions, "
-                      f"float64, OpenMP over channels, {t * reps:.1f} s"}
+                      f"float64, OpenMP over channels, {t * reps:.1f} s",
+            "single_thread": {"value": 64 * w.seqlen / t_one, "unit": "elements/s",
+                              "sample": f"64 channels x {w.seqlen} steps of batch row 0, 3 repetitions"},
+            "cpu_model": cpu_model()}
 
 
 # ----------------------------------------------------------------------------------------------
