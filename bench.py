@@ -333,7 +333,7 @@ def time_oracle(sample, nthreads, reps=1):
     return (time.perf_counter() - t0) / reps
 
 
-def cpu_baseline(w: wl.ScanWorkload, target_s: float = 15.0):
+def cpu_baseline(w: wl.ScanWorkload, target_s: float = 25.0):
     """Time the oracle on the host cores for about `target_s` seconds: batch row 0 of the workload
     (all its channels, the full sequence), repeated until the budget is used."""
     cores = cpu_cores()
