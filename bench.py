@@ -13,7 +13,8 @@ Extra objects on the line:
   roofline      the scan kernel against the measured HBM copy bandwidth (algorithmic bytes
                 per launch / average launch time), plus its DRAM traffic from the committed ncu
                 capture;
-  roofline_alu  the same launches against the special-function (MUFU) peak, the scan's co-bound;
+  roofline_alu  the same launches against the special-function (MUFU) peak, the scan's co-bound,
+                with the per-SM rate measured by the library's probe kernels (unit_rates);
   e2e           the same metric through the public API with pinned host buffers: host->device
                 copy of the step's inputs, the scan, device->host copy of y and the final state;
   cpu_baseline  the float64 oracle on the host cores (reported baseline, not a target);
@@ -426,8 +427,9 @@ MUFU_OPS_PER_CLK_PER_SM = 32
 B300_SMS = 148
 
 
-def alu_roofline(w: wl.ScanWorkload, ms: float):
-    """The scan's MUFU operations per second against the MUFU peak (a secondary roofline)."""
+def alu_roofline(w: wl.ScanWorkload, ms: float, rates=None):
+    """The scan's MUFU operations per second against the MUFU peak (a secondary roofline).  The
+    per-SM rate comes from the library's ex2 probe run on this GPU when `rates` is given."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             sm_mhz = float(json.load(f)["sm_max_mhz"])
@@ -436,11 +438,12 @@ def alu_roofline(w: wl.ScanWorkload, ms: float):
     sms = torch.cuda.get_device_properties(0).multi_processor_count if torch.cuda.is_available() else B300_SMS
     per_element = w.dstate + (4 if w.gate else 2)  # ex2 per state; softplus 2; silu 2
     achieved = w.elements * per_element / (ms * 1e-3) / 1e9
-    peak = MUFU_OPS_PER_CLK_PER_SM * sms * sm_mhz * 1e6 / 1e9
+    per_clk = rates["ex2"] if rates else float(MUFU_OPS_PER_CLK_PER_SM)
+    src = "ex2 probe on this GPU (ssm_probe_cycles)" if rates else "a probe on this pool"
+    peak = per_clk * sms * sm_mhz * 1e6 / 1e9
     return {"bound": "alu", "what": "MUFU ex2/lg2/rcp operations", "per_element": per_element,
             "achieved": achieved, "peak": peak, "unit": "Gop/s", "frac": achieved / peak,
-            "peak_source": f"{MUFU_OPS_PER_CLK_PER_SM} ops/clk/SM (measured by a probe on this pool) x {sms} SMs x "
-                           f"{sm_mhz:.0f} MHz"}
+            "peak_source": f"{per_clk:.1f} ops/clk/SM ({src}) x {sms} SMs x {sm_mhz:.0f} MHz (maximum SM clock)"}
 
 
 def run_zoh(w: wl.ScanWorkload, device, steps=200, warmup=5):
@@ -640,6 +643,8 @@ def main(argv=None):
         dist.barrier()
 
     w = wl.MID
+    import selective_state_space_155_b300 as ssm
+    rates = ssm.probe_unit_rates(device)
     run = ScanRun(w, device)
     sampler = ClockSampler(local)
     ms = timed(run.step, args.steps, args.warmup, dist, sampler)
@@ -665,7 +670,8 @@ def main(argv=None):
                      "algorithmic_bytes_per_launch": bytes_launch},
         "gpu_launches": args.steps,
         "clocks": sampler.summary(),
-        "roofline_alu": alu_roofline(w, ms),
+        "roofline_alu": alu_roofline(w, ms, rates),
+        "unit_rates": {"unit": "lane-operations per clock per SM", **rates},
     }
     if not args.no_e2e:
         e2e_ms, h2d, d2h = run_e2e(w, device, max(3, min(args.steps, 20)), 2, dist)

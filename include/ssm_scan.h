@@ -220,6 +220,20 @@ int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias,
 int ssm_causal_conv1d_update(void* state, const void* x, const float* weight, const float* bias, void* out,
                              int batch, int dim, int width, int silu, int io_dtype, void* stream);
 
+/*
+ * Throughput probes of the units the scan leans on (used to measure the peak of the benchmark's
+ * special-function roofline on the machine it runs on).  kind: SSM_PROBE_EX2 (ex2.approx),
+ * SSM_PROBE_FFMA (FP32 fused multiply-add), SSM_PROBE_FFMA2 (packed f32x2 fused multiply-add).
+ * Launches nblocks CTAs (use the SM count: one CTA per SM) of independent dependency chains and
+ * writes each CTA's clock cycles for the measured loop to cycles[0..nblocks-1] (device memory,
+ * int64).  ssm_probe_ops_per_cta(kind) is the number of lane-operations one CTA performs (an
+ * f32x2 operation counts as two), so ops / cycles is that unit's rate per SM per clock.
+ * Returns an ssm_status (SSM_ERR_ARG for an unknown kind).
+ */
+typedef enum { SSM_PROBE_EX2 = 0, SSM_PROBE_FFMA = 1, SSM_PROBE_FFMA2 = 2 } ssm_probe_kind;
+int ssm_probe_cycles(int kind, long long* cycles, int nblocks, void* stream);
+double ssm_probe_ops_per_cta(int kind);
+
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_status_string(int status);
 

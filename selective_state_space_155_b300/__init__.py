@@ -18,7 +18,7 @@ from . import _native
 from ._native import SsmError, lib, status_string  # noqa: F401
 
 __all__ = ["ssm_scan_fwd", "ssm_scan_bwd", "scan_num_checkpoints", "ssm_state_update", "causal_conv1d_fwd",
-           "causal_conv1d_update", "SsmError", "lib", "status_string", "io_dtype_code"]
+           "causal_conv1d_update", "probe_unit_rates", "SsmError", "lib", "status_string", "io_dtype_code"]
 
 _IO = {torch.float32: _native.SSM_F32, torch.bfloat16: _native.SSM_BF16}
 _DISC = {"delta_b": _native.SSM_DISC_DELTA_B, "zoh": _native.SSM_DISC_ZOH}
@@ -231,4 +231,22 @@ def causal_conv1d_update(state, x, weight, bias=None, silu=True, out=None, strea
         batch, dim, width, int(bool(silu)), io, _stream(stream),
     )
     _native.check("ssm_causal_conv1d_update", st)
+    return out
+
+
+def probe_unit_rates(device=None) -> dict:
+    """Measured lane-operations per clock per SM of ex2.approx, FP32 FMA and packed f32x2 FMA
+    (``ssm_probe_cycles``), the median over one CTA per SM."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    cycles = torch.empty(sms, dtype=torch.int64, device=dev)
+    out = {}
+    for name, kind in (("ex2", _native.SSM_PROBE_EX2), ("ffma", _native.SSM_PROBE_FFMA),
+                       ("ffma2", _native.SSM_PROBE_FFMA2)):
+        for _ in range(2):  # the first launch warms up
+            _native.check("ssm_probe_cycles", lib().ssm_probe_cycles(kind, _ptr(cycles, torch.int64, None, "cycles"),
+                                                                     sms, _stream(None)))
+        torch.cuda.synchronize(dev)
+        med = float(cycles.to("cpu").double().median())
+        out[name] = lib().ssm_probe_ops_per_cta(kind) / med
     return out

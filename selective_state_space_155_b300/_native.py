@@ -27,6 +27,10 @@ SSM_BF16 = 1
 SSM_DISC_DELTA_B = 0
 SSM_DISC_ZOH = 1
 
+SSM_PROBE_EX2 = 0
+SSM_PROBE_FFMA = 1
+SSM_PROBE_FFMA2 = 2
+
 # Every symbol the header declares, with its ctypes signature.
 _vp, _fp, _i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
 SIGNATURES = {
@@ -42,6 +46,8 @@ SIGNATURES = {
                                 _vp]),
     "ssm_scan_bwd": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp, _fp,
                           _fp, _i, _i, _i, _i, _i, _vp]),
+    "ssm_probe_cycles": (_i, [_i, _vp, _i, _vp]),
+    "ssm_probe_ops_per_cta": (ctypes.c_double, [_i]),
     "ssm_causal_conv1d_fwd": (_i, [_vp, _fp, _fp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),
     "ssm_causal_conv1d_update": (_i, [_vp, _vp, _fp, _fp, _vp, _i, _i, _i, _i, _i, _vp]),
 }

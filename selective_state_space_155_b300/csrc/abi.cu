@@ -239,4 +239,18 @@ int ssm_causal_conv1d_update(void* state, const void* x, const float* weight, co
   return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
+int ssm_probe_cycles(int kind, long long* cycles, int nblocks, void* stream) {
+  if (kind < SSM_PROBE_EX2 || kind > SSM_PROBE_FFMA2) return SSM_ERR_ARG;
+  if (nblocks < 0) return SSM_ERR_SHAPE;
+  if (nblocks == 0) return SSM_OK;
+  if (!cycles) return SSM_ERR_NULL;
+  if (!aligned(cycles, 8)) return SSM_ERR_ALIGN;
+  const cudaError_t err = ssm::launch_probe(kind, nblocks, cycles, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+double ssm_probe_ops_per_cta(int kind) {
+  return (kind < SSM_PROBE_EX2 || kind > SSM_PROBE_FFMA2) ? 0.0 : ssm::probe_ops_per_cta(kind);
+}
+
 }  // extern "C"

@@ -144,6 +144,10 @@ cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);
 // gradients, then one launch.  Arguments are already validated.
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);
 
+// Unit-throughput probes (probe.cu): kind 0 = ex2.approx, 1 = FP32 FMA, 2 = packed f32x2 FMA.
+cudaError_t launch_probe(int kind, int nblocks, long long* cycles, cudaStream_t stream);
+double probe_ops_per_cta(int kind);
+
 // Enqueue the causal conv1d / its decode step on `stream` (causal_conv1d.cu).  Arguments are
 // already validated (width 1..4).
 cudaError_t launch_causal_conv1d(const ConvArgs& a, cudaStream_t stream);

@@ -32,7 +32,8 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_scan_fwd_ex", "ssm_state_update",
          "ssm_state_update_ex", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update",
-         "ssm_scan_num_checkpoints", "ssm_scan_fwd_train", "ssm_scan_bwd"])
+         "ssm_scan_num_checkpoints", "ssm_scan_fwd_train", "ssm_scan_bwd", "ssm_probe_cycles",
+         "ssm_probe_ops_per_cta"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -232,3 +233,15 @@ def bwd_args(**over):
 ])
 def test_bwd_validation(lib, over, expected):
     assert lib.ssm_scan_bwd(*bwd_args(**over)) == expected
+
+
+def test_probe_validation(lib):
+    assert lib.ssm_probe_cycles(3, P, 4, None) == _native.SSM_ERR_ARG
+    assert lib.ssm_probe_cycles(-1, P, 4, None) == _native.SSM_ERR_ARG
+    assert lib.ssm_probe_cycles(0, None, 4, None) == _native.SSM_ERR_NULL
+    assert lib.ssm_probe_cycles(1, P + 4, 4, None) == _native.SSM_ERR_ALIGN
+    assert lib.ssm_probe_cycles(2, None, 0, None) == _native.SSM_OK
+    assert lib.ssm_probe_cycles(0, P, -1, None) == _native.SSM_ERR_SHAPE
+    ops = [lib.ssm_probe_ops_per_cta(k) for k in (0, 1, 2)]
+    assert ops[0] == ops[1] > 0 and ops[2] == 2 * ops[1]
+    assert lib.ssm_probe_ops_per_cta(7) == 0.0
