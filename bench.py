@@ -17,7 +17,9 @@ Extra objects on the line:
                 with the per-SM rate measured by the library's probe kernels (unit_rates);
   e2e           the same metric through the public API with pinned host buffers: host->device
                 copy of the step's inputs, the scan, device->host copy of y and the final state;
-  cpu_baseline  the float64 oracle on the host cores (reported baseline, not a target);
+  cpu_baseline  the float64 oracle on the host cores (reported baseline, not a target), all
+                cores and one thread, and the benchmarked kernel's output checked against it on a
+                slice of the workload (parity);
   decode        the decode workload (batch 256, d_inner 5120, d_state 16): 1024 in-place steps
                 captured in one CUDA graph, and one step after an L2 flush;
   zoh           the same scan workload with the exact zero-order-hold discretisation;
@@ -334,6 +336,27 @@ def time_oracle(sample, nthreads, reps=1):
     return (time.perf_counter() - t0) / reps
 
 
+def gpu_vs_oracle(w: wl.ScanWorkload, small: dict) -> dict:
+    """The benchmarked kernel's output for the oracle's 64-channel slice of batch row 0, against the
+    oracle on the same inputs: the largest |y - y_ref| / (1 + |y_ref|) and the same for the state."""
+    from oracle import oracle
+    import selective_state_space_155_b300 as ssm
+    n = small["u"].shape[1]
+    inp = wl.scan_inputs(w, device=torch.device("cuda", torch.cuda.current_device()))
+    y, last = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                               inp["dt_bias"], delta_softplus=True)
+    y0 = wl.to_f64(y[:1, :n])
+    s0 = wl.to_f64(last[:1, :n])
+    del inp, y, last
+    torch.cuda.empty_cache()
+    y_ref, s_ref = oracle.scan(small["u"], small["delta"], small["A"], small["B"], small["C"], small["D"], small["z"],
+                               small["dt_bias"], delta_softplus=True)
+    rel = lambda a, b: float(np.max(np.abs(a - b) / (1.0 + np.abs(b))))
+    return {"channels": f"batch row 0, channels 0..{n - 1}", "max_rel_err_y": rel(y0, y_ref),
+            "max_rel_err_state": rel(s0, s_ref), "tolerance_y": 2e-2 if w.io == "bf16" else 1e-4,
+            "tolerance_state": 1e-4}
+
+
 def cpu_baseline(w: wl.ScanWorkload, target_s: float = 25.0):
     """Time the oracle on the host cores for about `target_s` seconds: batch row 0 of the workload
     (all its channels, the full sequence), repeated until the budget is used."""
@@ -346,12 +369,13 @@ def cpu_baseline(w: wl.ScanWorkload, target_s: float = 25.0):
     # one thread on a smaller slice of the same row (64 channels), for the per-core figure
     small = oracle_sample(w, channels=64)
     t_one = time_oracle(small, 1, reps=3)
+    parity = gpu_vs_oracle(w, small)
     return {"value": elems / t, "unit": "elements/s", "cores": cores, "kind": "oracle",
             "sample": f"batch row 0 of {w.name} ({w.dim} channels x {w.seqlen} steps) x {reps} repetitions, "
                       f"float64, OpenMP over channels, {t * reps:.1f} s",
             "single_thread": {"value": 64 * w.seqlen / t_one, "unit": "elements/s",
                               "sample": f"64 channels x {w.seqlen} steps of batch row 0, 3 repetitions"},
-            "cpu_model": cpu_model()}
+            "cpu_model": cpu_model(), "parity": parity}
 
 
 # ----------------------------------------------------------------------------------------------
