@@ -125,10 +125,9 @@ struct ConvUpdateArgs {
   FastDiv div_dim;  // filled at launch
 };
 
-// Enqueue the scan on `stream`.  Arguments are already validated.  Picks the lane-per-channel
-// form when there are enough channels to give every SM eight or more of its warps, otherwise the
-// four-lanes-per-channel form; SSM_SCAN_VARIANT=lane|quad in the environment forces one.  The
-// zero-order-hold discretization always runs the four-lanes-per-channel form.
+// Enqueue the scan on `stream`.  Arguments are already validated.  Runs the four-lanes-per-channel
+// form; SSM_SCAN_VARIANT=lane in the environment selects the lane-per-channel form instead (not for
+// the zero-order hold or the training forward, which always run the four-lanes form).
 cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream);
 
 // The four-lanes-per-channel form (scan_fwd.cu).

@@ -14,10 +14,10 @@
 //    16-byte cp.async into a three-stage ring, so a chunk's rows stay valid while every lane reads
 //    them and the next chunk is already in flight; B and C are converted once per CTA into
 //    float32 [t][n] tables.
-// Each warp carries NPAD independent state chains per lane, but its latencies still need about two
-// warps per scheduler to hide; this form is used when there are enough channels to give every SM
-// eight or more of its warps (batch x dim >= 256 x SMs), and never for the zero-order hold or
-// the training forward.
+// Each warp carries NPAD independent state chains per lane.  Measured on B300 this form is slower
+// than the four-lanes-per-channel form at every size tried (1.45x with 27-69 channel warps per
+// SM), so it runs only when SSM_SCAN_VARIANT=lane selects it; it is kept, and parity-tested, as
+// the other point of the lanes-per-channel trade-off.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
