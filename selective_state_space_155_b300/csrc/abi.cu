@@ -204,7 +204,9 @@ int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias,
   for (const void* p : io_ptrs)
     if (!aligned(p, es)) return SSM_ERR_ALIGN;
   if (!aligned(weight, 4) || !aligned(bias, 4)) return SSM_ERR_ALIGN;
-  if ((long long)batch * dim * ((long long)seqlen + width) / 256 + 1 > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+  // work items over 256-thread CTAs must fit a grid; formed in double, where the product cannot overflow
+  if (double(batch) * double(dim) * (double(seqlen) + width) / 256.0 + 1.0 > double(0x7fffffff))
+    return SSM_ERR_UNSUPPORTED;
 
   ssm::ConvArgs a{};
   a.x = x, a.weight = weight, a.bias = bias, a.state_in = state_in, a.out = out, a.state_out = state_out;

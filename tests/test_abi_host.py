@@ -245,3 +245,12 @@ def test_probe_validation(lib):
     ops = [lib.ssm_probe_ops_per_cta(k) for k in (0, 1, 2)]
     assert ops[0] == ops[1] > 0 and ops[2] == 2 * ops[1]
     assert lib.ssm_probe_ops_per_cta(7) == 0.0
+
+
+def test_grid_overflow_is_refused_before_any_launch(lib):
+    """Sizes whose grid would not fit a launch are refused on the host (no memory is touched)."""
+    big = 2 ** 31 - 1
+    assert lib.ssm_scan_fwd(*scan_args(batch=big, dim=64)) == _native.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_state_update(*update_args(batch=big, dim=big)) == _native.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_causal_conv1d_fwd(*conv_args(batch=big, dim=big)) == _native.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_scan_bwd(*bwd_args(batch=big, dim=64)) == _native.SSM_ERR_UNSUPPORTED
