@@ -22,8 +22,9 @@ Parity status per function (what pins it, see tests/test_oracle_pins.py):
   assoc_scan      pinned: prefix-sum worked example; equals the closed-form products.
   scan_tree       pinned: equals the sequential scan (associativity).
   scan_bwd        pinned: central finite differences of <dout, out> along random directions for
-                  every input (u, delta, A, B, C, D, z, dt_bias, h0; softplus on and off), and
-                  the closed-form gradient of the prefix-sum special case.
+                  every input (u, delta, A, B, C, D, z, dt_bias, h0; softplus on and off; both
+                  discretisations, ZOH also with A near and at 0), and the closed-form gradient of
+                  the prefix-sum special case.
   causal_conv1d   pinned: numpy's full convolution (first L outputs), torch's grouped Conv1d with
                   padding W-1 as the gsyq.cn sketch writes it, streaming in two pieces, impulse
                   response, silu special values.
@@ -81,7 +82,7 @@ def _load():
             lib.oracle_scan_tree_f64.restype = ctypes.c_int
             lib.oracle_scan_tree_f64.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP] + [ctypes.c_int] * 4
             lib.oracle_scan_bwd_f64.restype = ctypes.c_int
-            lib.oracle_scan_bwd_f64.argtypes = [_DP] * 8 + [ctypes.c_int] + [_DP] * 11 + [ctypes.c_int] * 4
+            lib.oracle_scan_bwd_f64.argtypes = [_DP] * 8 + [ctypes.c_int, ctypes.c_int] + [_DP] * 11 + [ctypes.c_int] * 4
             lib.oracle_causal_conv1d_f64.restype = ctypes.c_int
             lib.oracle_causal_conv1d_f64.argtypes = [_DP] * 6 + [ctypes.c_int] * 5
             lib.oracle_softplus_f64.restype = ctypes.c_double
@@ -187,8 +188,9 @@ def scan_tree(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=Tr
     return y, last
 
 
-def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None):
-    """Gradients of the scan (Delta*B form) for the output gradient dout [batch, dim, L].
+def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, zoh=False):
+    """Gradients of the scan (Delta*B form, or the exact zero-order hold with zoh) for the output
+    gradient dout [batch, dim, L].
     Returns a dict with du, ddelta, dA, dB, dC and, where the input is given, dD, dz,
     ddt_bias, dh0 (float64 arrays shaped like their inputs)."""
     u = _f64(u)
@@ -210,7 +212,8 @@ def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
     g["ddt_bias"] = np.zeros(dim) if dt_bias is not None else None
     g["dh0"] = np.zeros((batch, dim, dstate)) if h0 is not None else None
     rc = _load().oracle_scan_bwd_f64(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
-                                     _ptr(dt_bias), int(bool(delta_softplus)), _ptr(h0), _ptr(dout), _ptr(g["du"]),
+                                     _ptr(dt_bias), int(bool(delta_softplus)), int(bool(zoh)), _ptr(h0), _ptr(dout),
+                                     _ptr(g["du"]),
                                      _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
                                      _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dh0"]), batch, dim, dstate, seqlen)
     if rc != 0:

@@ -40,7 +40,7 @@
  *   Decode step    the same single recurrence step applied to a stored state
  *                  (constant-memory inference: gsyq.cn page, complexity table
  *                  row "推理内存 O(d) 状态向量").
- *   Backward       reverse-mode gradients of the scan (Delta*B form) for a
+ *   Backward       reverse-mode gradients of the scan (either B discretisation) for a
  *                  loss whose gradient with respect to the outputs is dout:
  *                  the same recurrence run backwards with the adjoint state
  *                  lambda_t = dy_t C_t + Abar_{t+1} lambda_{t+1} (chain rule
@@ -185,8 +185,8 @@ static double dsilu_f64(double z) {
 }
 
 /*
- * Gradients of the scan (Delta*B discretisation) given dout = dLoss/dout, same layouts as the
- * forward.  Outputs (all overwritten, summed over what the parameter is shared by):
+ * Gradients of the scan (Delta*B form, or the exact zero-order hold with zoh set) given
+ * dout = dLoss/dout, same layouts as the forward.  Outputs (all overwritten, summed over what the parameter is shared by):
  *   du, ddelta, dz        [batch][dim][seqlen]   (dz only when z is given; NULL skips it)
  *   dA                    [dim][dstate]          (summed over batch)
  *   dB, dC                [batch][dstate][seqlen] (summed over channels)
@@ -195,7 +195,7 @@ static double dsilu_f64(double z) {
  * ddelta is with respect to the raw delta (before dt_bias and softplus).
  */
 int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, const double* B, const double* C,
-                        const double* D, const double* z, const double* dt_bias, int delta_softplus,
+                        const double* D, const double* z, const double* dt_bias, int delta_softplus, int zoh,
                         const double* h0, const double* dout, double* du, double* ddelta, double* dA, double* dB,
                         double* dC, double* dD, double* dz, double* ddt_bias, double* dh0, int batch, int dim,
                         int dstate, int seqlen) {
@@ -223,8 +223,9 @@ int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, c
       dts[t] = dt;
       double acc = 0.0;
       for (long n = 0; n < N; ++n) {
-        double a = exp(dt * A[(long)d * N + n]);
-        double h = a * hs[t * N + n] + dt * B[((long)b * N + n) * L + t] * ur[t];
+        double an = A[(long)d * N + n];
+        double a = exp(dt * an);
+        double h = a * hs[t * N + n] + bbar_factor(dt, an, zoh) * B[((long)b * N + n) * L + t] * ur[t];
         hs[(t + 1) * N + n] = h;
         acc += C[((long)b * N + n) * L + t] * h;
       }
@@ -246,11 +247,20 @@ int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, c
         double bn = B[((long)b * N + n) * L + t];
         double hp = hs[t * N + n];        /* h_{t-1} */
         double lam = dy * C[((long)b * N + n) * L + t] + carry[n];
+        /* Bbar = c B with c = Delta (Delta*B form) or (exp(Delta a) - 1) / a (zero-order hold):
+         * dc/dDelta = 1 or exp(Delta a); dc/da = 0 or (Delta exp(Delta a) - c) / a, whose limit
+         * at Delta a -> 0 is Delta^2 (1/2 + x/3 + x^2/8 + x^3/30 + ...), x = Delta a. */
+        double c = bbar_factor(dt, an, zoh), dc_ddt = 1.0, dc_da = 0.0;
+        if (zoh) {
+          double x = dt * an;
+          dc_ddt = a;
+          dc_da = fabs(x) < 1e-3 ? dt * dt * (0.5 + x / 3.0 + x * x / 8.0 + x * x * x / 30.0) : (dt * a - c) / an;
+        }
         dC[((long)b * N + n) * L + t] += dy * hs[(t + 1) * N + n];
-        dB[((long)b * N + n) * L + t] += lam * dt * ur[t];
-        dut += lam * dt * bn;
-        ddt += lam * (an * a * hp + bn * ur[t]);
-        dA[(long)d * N + n] += lam * dt * a * hp;
+        dB[((long)b * N + n) * L + t] += lam * c * ur[t];
+        dut += lam * c * bn;
+        ddt += lam * (an * a * hp + dc_ddt * bn * ur[t]);
+        dA[(long)d * N + n] += lam * (dt * a * hp + dc_da * bn * ur[t]);
         carry[n] = lam * a;
       }
       du[ch * L + t] = dut;

@@ -40,10 +40,15 @@ MUTANTS = {
     "conv_off_by_one": ("int s = t - hw + k; /* input time index */", "int s = t - hw + k - 1; /* input time index */"),
     "conv_state_ignored": ("double v = s >= 0 ? xr[s] : (sr ? sr[hw + s] : 0.0);", "double v = s >= 0 ? xr[s] : 0.0;"),
     "conv_no_bias": ("double acc = bias ? bias[d] : 0.0;", "double acc = 0.0;"),
+    "bwd_zoh_dc_ddelta": ("          dc_ddt = a;\n", "          dc_ddt = 1.0;\n"),
+    "bwd_zoh_dc_da": ("dc_da = fabs(x) < 1e-3 ? dt * dt * (0.5 + x / 3.0 + x * x / 8.0 + x * x * x / 30.0) : (dt * a - c) / an;",
+                      "dc_da = 0.0;"),
+    "bwd_zoh_small_x_series": ("dt * dt * (0.5 + x / 3.0 + x * x / 8.0 + x * x * x / 30.0)", "dt * dt * (0.5 - x / 3.0)"),
     "bwd_no_carry": ("double lam = dy * C[((long)b * N + n) * L + t] + carry[n];",
                      "double lam = dy * C[((long)b * N + n) * L + t];"),
     "bwd_carry_without_decay": ("carry[n] = lam * a;", "carry[n] = lam;"),
-    "bwd_dA_missing_state": ("dA[(long)d * N + n] += lam * dt * a * hp;", "dA[(long)d * N + n] += lam * dt * a;"),
+    "bwd_dA_missing_state": ("dA[(long)d * N + n] += lam * (dt * a * hp + dc_da * bn * ur[t]);",
+                             "dA[(long)d * N + n] += lam * (dt * a + dc_da * bn * ur[t]);"),
     "bwd_dC_previous_state": ("dC[((long)b * N + n) * L + t] += dy * hs[(t + 1) * N + n];",
                               "dC[((long)b * N + n) * L + t] += dy * hs[t * N + n];"),
     "bwd_softplus_grad": ("double dd = delta_softplus ? ddt / (1.0 + exp(-raw)) : ddt;",

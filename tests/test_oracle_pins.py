@@ -495,9 +495,9 @@ def _bwd_case(seed, softplus=True, h0=True, gate=True, use_D=True, use_bias=True
     return case, dout
 
 
-def _loss(case, dout, softplus):
+def _loss(case, dout, softplus, zoh=False):
     y, _ = oracle.scan(case["u"], case["delta"], case["A"], case["B"], case["C"], D=case["D"], z=case["z"],
-                       dt_bias=case["dt_bias"], delta_softplus=softplus, h0=case["h0"])
+                       dt_bias=case["dt_bias"], delta_softplus=softplus, h0=case["h0"], zoh=zoh)
     return float(np.sum(dout * y))
 
 
@@ -538,3 +538,45 @@ def test_backward_prefix_sum_closed_form():
     np.testing.assert_allclose(g["du"][0, 0], tail + 0.7 * dout[0, 0], rtol=1e-13)
     np.testing.assert_allclose(g["dD"], [np.sum(dout * u)], rtol=1e-13)
     np.testing.assert_allclose(g["ddelta"][0, 0], tail * u[0, 0, :], rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("softplus", [True, False])
+@pytest.mark.parametrize("name", sorted(GRAD_OF))
+def test_zoh_backward_matches_finite_differences(name, softplus):
+    """The same finite-difference pin for the exact zero-order hold; A holds one state at exactly
+    0 and one at -1e-5 so that both limits of the factor's derivative are exercised."""
+    case, dout = _bwd_case(23 + len(name), softplus=softplus)
+    case["A"] = case["A"].copy()
+    case["A"][0, 0] = 0.0
+    case["A"][1, 1] = -1e-5
+    g = oracle.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dout, D=case["D"], z=case["z"],
+                        dt_bias=case["dt_bias"], delta_softplus=softplus, h0=case["h0"], zoh=True)
+    rng = np.random.default_rng(98)
+    v = rng.standard_normal(case[name].shape)
+    eps = 1e-5
+    plus = dict(case)
+    plus[name] = case[name] + eps * v
+    minus = dict(case)
+    minus[name] = case[name] - eps * v
+    fd = (_loss(plus, dout, softplus, zoh=True) - _loss(minus, dout, softplus, zoh=True)) / (2 * eps)
+    an = float(np.sum(g[GRAD_OF[name]] * v))
+    assert abs(fd - an) <= 1e-7 * (1.0 + abs(fd)), (name, fd, an)
+
+
+def test_zoh_backward_small_decay_branch_matches_finite_differences():
+    """Every A in [-2e-3, 0): Delta*A lands on both sides of the point where the hold factor's
+    A-derivative switches from its direct form to its series, so dA is pinned on both branches."""
+    case, dout = _bwd_case(41, softplus=True)
+    rng = np.random.default_rng(5)
+    case["A"] = -rng.uniform(0.0, 2e-3, case["A"].shape)
+    g = oracle.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dout, D=case["D"], z=case["z"],
+                        dt_bias=case["dt_bias"], delta_softplus=True, h0=case["h0"], zoh=True)
+    for seed in range(3):
+        v = np.random.default_rng(200 + seed).standard_normal(case["A"].shape)
+        eps = 1e-6
+        plus, minus = dict(case), dict(case)
+        plus["A"] = case["A"] + eps * v
+        minus["A"] = case["A"] - eps * v
+        fd = (_loss(plus, dout, True, zoh=True) - _loss(minus, dout, True, zoh=True)) / (2 * eps)
+        an = float(np.sum(g["dA"] * v))
+        assert abs(fd - an) <= 1e-8 * (1.0 + abs(fd)), (seed, fd, an)
