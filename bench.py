@@ -25,6 +25,7 @@ Extra objects on the line:
   zoh           the same scan workload with the exact zero-order-hold discretisation;
   conv1d        the causal conv1d (width 4, silu) that produces u, on the same activation shape;
   train         the training pair on the same workload: forward with state checkpoints, backward;
+  train_zoh     the same training pair under the exact zero-order hold;
   clocks        SM clocks and throttle reasons sampled (NVML) during the timed region.
 
 Under torchrun each rank runs the same workload on its own GPU with no collective on the data
@@ -483,11 +484,12 @@ def run_zoh(w: wl.ScanWorkload, device, steps=200, warmup=5):
             "traffic": committed_traffic("scan_fwd_kernel_zoh")}
 
 
-def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_COPIES):
+def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_COPIES, discretization="delta_b"):
     """The training pair on the scan workload: the forward that keeps chunk checkpoints, then the
     backward pass from them and a synthetic dout (rotating input copies, as for the forward)."""
     import selective_state_space_155_b300 as ssm
     run = ScanRun(w, device, copies=copies)
+    disc = discretization
     nck = ssm.scan_num_checkpoints(w.seqlen)
     cks = [torch.empty((w.batch, nck, w.dim, w.dstate), dtype=torch.float32, device=device) for _ in range(copies)]
     gen = torch.Generator(device=device).manual_seed(w.seed)
@@ -498,13 +500,13 @@ def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_CO
         k = i % copies
         s = run.sets[k]
         ssm.ssm_scan_fwd(s["u"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"], s["dt_bias"],
-                         y=run.y[k], last_state=run.last[k], checkpoints=cks[k])
+                         y=run.y[k], last_state=run.last[k], checkpoints=cks[k], discretization=disc)
 
     def bwd(i):
         k = i % copies
         s = run.sets[k]
         ssm.ssm_scan_bwd(s["u"], s["delta"], s["A"], s["B"], s["C"], cks[k], douts[k], D=s["D"], z=s["z"],
-                         dt_bias=s["dt_bias"])
+                         dt_bias=s["dt_bias"], discretization=disc)
 
     for i in range(copies):
         fwd(i)
@@ -512,9 +514,9 @@ def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_CO
     ms_b = timed(bwd, steps, warmup)
     del run, cks, douts
     torch.cuda.empty_cache()
-    return {"workload": w.name, "fwd_train_us": ms_f * 1e3, "bwd_us": ms_b * 1e3, "step_us": (ms_f + ms_b) * 1e3,
-            "elements_per_s": w.elements / ((ms_f + ms_b) * 1e-3), "steps": steps,
-            "bwd_traffic": committed_traffic("scan_bwd_kernel"),
+    return {"workload": w.name, "discretization": disc, "fwd_train_us": ms_f * 1e3, "bwd_us": ms_b * 1e3,
+            "step_us": (ms_f + ms_b) * 1e3, "elements_per_s": w.elements / ((ms_f + ms_b) * 1e-3), "steps": steps,
+            "bwd_traffic": committed_traffic("scan_bwd_kernel" + ("_zoh" if disc == "zoh" else "")),
             "note": "backward allocates its gradient tensors each call (torch caching allocator)"}
 
 
@@ -591,17 +593,18 @@ def profile_mode(which: str) -> int:
     elif which == "zoh":
         run = ScanRun(wl.MID, device, copies=1, discretization="zoh")
         fn = run.step
-    elif which == "bwd":
+    elif which in ("bwd", "bwd_zoh"):
         import selective_state_space_155_b300 as ssm
+        disc = "zoh" if which == "bwd_zoh" else "delta_b"
         run = ScanRun(wl.MID, device, copies=1)
         s0 = run.sets[0]
         ck = torch.empty((wl.MID.batch, ssm.scan_num_checkpoints(wl.MID.seqlen), wl.MID.dim, wl.MID.dstate),
                          dtype=torch.float32, device=device)
         ssm.ssm_scan_fwd(s0["u"], s0["delta"], s0["A"], s0["B"], s0["C"], s0["D"], s0["z"], s0["dt_bias"],
-                         checkpoints=ck)
+                         checkpoints=ck, discretization=disc)
         dout = torch.randn_like(s0["u"], dtype=torch.float32).to(s0["u"].dtype)
         fn = lambda i: ssm.ssm_scan_bwd(s0["u"], s0["delta"], s0["A"], s0["B"], s0["C"], ck, dout, D=s0["D"],
-                                        z=s0["z"], dt_bias=s0["dt_bias"])
+                                        z=s0["z"], dt_bias=s0["dt_bias"], discretization=disc)
     elif which == "conv":
         import selective_state_space_155_b300 as ssm
         w = wl.MID
@@ -632,7 +635,7 @@ def main(argv=None):
     ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-train", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "zoh", "bwd", "conv", "decode"], default=None,
+    ap.add_argument("--profile", choices=["scan", "zoh", "bwd", "bwd_zoh", "conv", "decode"], default=None,
                     help="run 2 warm-up and 3 profiled launches of one kernel on its workload and exit "
                          "(a small command for ncu; prints no JSON line)")
     args = ap.parse_args(argv)
@@ -709,6 +712,7 @@ def main(argv=None):
         res["conv1d"] = run_conv(w, device)
     if rank == 0 and not args.no_train:
         res["train"] = run_train(w, device)
+        res["train_zoh"] = run_train(w, device, discretization="zoh")
     if rank == 0 and not args.no_cpu_baseline:
         res["cpu_baseline"] = cpu_baseline(w)
     if dist is not None:

@@ -25,7 +25,7 @@
  *                    row "推理内存 O(d) 状态向量"; 53ai.com Mamba article, §1 on
  *                    RNN-style inference from the previous hidden state only).
  *
- *  ssm_scan_fwd_train / ssm_scan_bwd
+ *  ssm_scan_fwd_train / ssm_scan_bwd (and their _ex forms, either discretization)
  *                    The training pair: a forward that keeps chunk checkpoints of
  *                    the state, and the backward pass from them.
  *
@@ -86,7 +86,7 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  */
 typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization;
 
-/* Version of this ABI (bumped when a signature changes). */
+/* Version of this ABI (bumped when a signature changes or an entry point is added): 3. */
 int ssm_abi_version(void);
 
 /*
@@ -142,6 +142,15 @@ int ssm_scan_fwd_train(const void* u, const void* delta, const float* A, const v
                        int io_dtype, void* stream);
 
 /*
+ * ssm_scan_fwd_train with a choice of discretization (as ssm_scan_fwd_ex; anything else returns
+ * SSM_ERR_ARG).  Pair an SSM_DISC_ZOH training forward with ssm_scan_bwd_ex(..., SSM_DISC_ZOH).
+ */
+int ssm_scan_fwd_train_ex(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                          const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,
+                          void* y, float* last_state, float* checkpoints, int batch, int dim, int dstate, int seqlen,
+                          int io_dtype, int discretization, void* stream);
+
+/*
  * Backward pass of the scan (Delta*B discretization): the gradients of a loss given
  * dout = dLoss/dout ([batch][dim][seqlen], io dtype), from the same inputs as the forward and the
  * forward's checkpoints (ssm_scan_fwd_train).  Reverse-mode differentiation of the recurrence
@@ -164,6 +173,21 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B
                  const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
                  float* ddt_bias, float* dh0, int batch, int dim, int dstate, int seqlen, int io_dtype,
                  void* stream);
+
+/*
+ * ssm_scan_bwd with a choice of discretization (an ssm_discretization value; anything else
+ * returns SSM_ERR_ARG).  Under SSM_DISC_ZOH the B term is c B u with c = (exp(Delta A) - 1) / A,
+ * so dB and du carry c in place of Delta, dDelta gains exp(Delta A) B u in place of B u, and dA
+ * gains dc/dA B u, dc/dA = (Delta exp(Delta A) - c) / A (its limit Delta^2 / 2 at A = 0).  The
+ * checkpoints must come from ssm_scan_fwd_train_ex with the same discretization.  Arguments,
+ * outputs and errors are otherwise those of ssm_scan_bwd, which equals this call with
+ * SSM_DISC_DELTA_B.
+ */
+int ssm_scan_bwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* checkpoints,
+                    const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                    float* ddt_bias, float* dh0, int batch, int dim, int dstate, int seqlen, int io_dtype,
+                    int discretization, void* stream);
 
 /*
  * Single-token decode step, state updated in place.

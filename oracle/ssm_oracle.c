@@ -105,7 +105,7 @@ static double step_size(double raw, const double* dt_bias, int d, int use_softpl
   return v;
 }
 
-int oracle_abi_version(void) { return 2; }
+int oracle_abi_version(void) { return 3; }
 
 /* Selective scan over seqlen steps for every (batch, channel). */
 int oracle_scan_f64(const double* u, const double* delta, const double* A, const double* B, const double* C,

@@ -69,7 +69,7 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus
     A: [dim, dstate], D, dt_bias: [dim], h0: [batch, dim, dstate] (float32).
     discretization: "delta_b" (Bbar = Delta B) or "zoh" (exact zero-order hold).
     checkpoints: a float32 [batch, scan_num_checkpoints(L), dim, dstate] tensor to receive the
-    chunk-start states for ssm_scan_bwd (training forward; "delta_b" only).
+    chunk-start states for ssm_scan_bwd (training forward, either discretization).
     Returns (y, last_state); y has u's dtype, last_state is float32 (None if not requested).
     """
     disc = _disc(discretization)
@@ -98,10 +98,12 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus
     ]
     h0p = _ptr(h0, torch.float32, (batch, dim, dstate), "h0")
     if checkpoints is not None:
-        if disc != _native.SSM_DISC_DELTA_B:
-            raise ValueError("the training forward (checkpoints) uses the delta_b discretization")
         ck = _ptr(checkpoints, torch.float32, (batch, scan_num_checkpoints(L), dim, dstate), "checkpoints")
-        _native.check("ssm_scan_fwd_train", lib().ssm_scan_fwd_train(*args, h0p, tail[0], tail[1], ck, *tail[2:]))
+        if disc == _native.SSM_DISC_DELTA_B:
+            _native.check("ssm_scan_fwd_train", lib().ssm_scan_fwd_train(*args, h0p, tail[0], tail[1], ck, *tail[2:]))
+        else:
+            _native.check("ssm_scan_fwd_train_ex",
+                          lib().ssm_scan_fwd_train_ex(*args, h0p, tail[0], tail[1], ck, *tail[2:-1], disc, tail[-1]))
     elif disc != _native.SSM_DISC_DELTA_B:
         _native.check("ssm_scan_fwd_ex", lib().ssm_scan_fwd_ex(*args, h0p, *tail[:-1], disc, tail[-1]))
     elif h0 is None:
@@ -112,11 +114,13 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus
 
 
 def ssm_scan_bwd(u, delta, A, B, C, checkpoints, dout, D=None, z=None, dt_bias=None, delta_softplus=True,
-                 need_dh0=False, stream=None):
-    """Backward pass of the scan (``ssm_scan_bwd`` of the C-ABI) from the training forward's
-    checkpoints and dout = dLoss/dout [batch, dim, L].  Returns a dict of gradients: du, ddelta
-    (and dz when z is given) in u's dtype; dA, dB, dC (and dD, ddt_bias, dh0 when D, dt_bias are
-    given / need_dh0) in float32."""
+                 need_dh0=False, stream=None, discretization="delta_b"):
+    """Backward pass of the scan (``ssm_scan_bwd`` / ``ssm_scan_bwd_ex`` of the C-ABI) from the
+    training forward's checkpoints and dout = dLoss/dout [batch, dim, L].  discretization must be
+    the training forward's.  Returns a dict of gradients: du, ddelta (and dz when z is given) in
+    u's dtype; dA, dB, dC (and dD, ddt_bias, dh0 when D, dt_bias are given / need_dh0) in
+    float32."""
+    disc = _disc(discretization)
     batch, dim, L = u.shape
     dstate = A.shape[1]
     io = io_dtype_code(u.dtype)
@@ -131,7 +135,7 @@ def ssm_scan_bwd(u, delta, A, B, C, checkpoints, dout, D=None, z=None, dt_bias=N
         g["ddt_bias"] = torch.empty((dim,), **f32)
     if need_dh0:
         g["dh0"] = torch.empty((batch, dim, dstate), **f32)
-    st = lib().ssm_scan_bwd(
+    args = [
         _ptr(u, u.dtype, (batch, dim, L), "u"),
         _ptr(delta, u.dtype, (batch, dim, L), "delta"),
         _ptr(A, torch.float32, (dim, dstate), "A"),
@@ -145,9 +149,12 @@ def ssm_scan_bwd(u, delta, A, B, C, checkpoints, dout, D=None, z=None, dt_bias=N
         _ptr(dout, u.dtype, (batch, dim, L), "dout"),
         _ptr(g["du"]), _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g.get("dD")),
         _ptr(g.get("dz")), _ptr(g.get("ddt_bias")), _ptr(g.get("dh0")),
-        batch, dim, dstate, L, io, _stream(stream),
-    )
-    _native.check("ssm_scan_bwd", st)
+        batch, dim, dstate, L, io,
+    ]
+    if disc == _native.SSM_DISC_DELTA_B:
+        _native.check("ssm_scan_bwd", lib().ssm_scan_bwd(*args, _stream(stream)))
+    else:
+        _native.check("ssm_scan_bwd_ex", lib().ssm_scan_bwd_ex(*args, disc, _stream(stream)))
     return g
 
 

@@ -46,6 +46,10 @@ SIGNATURES = {
                                 _vp]),
     "ssm_scan_bwd": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp, _fp,
                           _fp, _i, _i, _i, _i, _i, _vp]),
+    "ssm_scan_fwd_train_ex": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _fp, _fp, _i, _i, _i, _i, _i,
+                                   _i, _vp]),
+    "ssm_scan_bwd_ex": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
+                             _fp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
     "ssm_probe_cycles": (_i, [_i, _vp, _i, _vp]),
     "ssm_probe_ops_per_cta": (ctypes.c_double, [_i]),
     "ssm_causal_conv1d_fwd": (_i, [_vp, _fp, _fp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),

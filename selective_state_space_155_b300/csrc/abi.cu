@@ -16,7 +16,7 @@ size_t io_size(int io) { return io == SSM_F32 ? 4 : 2; }
 
 extern "C" {
 
-int ssm_abi_version(void) { return 2; }
+int ssm_abi_version(void) { return 3; }
 
 const char* ssm_status_string(int status) {
   switch (status) {
@@ -86,22 +86,31 @@ int ssm_scan_num_checkpoints(int seqlen) {
   return seqlen > 0 ? (seqlen + SSM_SCAN_CHECKPOINT_STEPS - 1) / SSM_SCAN_CHECKPOINT_STEPS : 0;
 }
 
-int ssm_scan_fwd_train(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                       const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,
-                       void* y, float* last_state, float* checkpoints, int batch, int dim, int dstate, int seqlen,
-                       int io_dtype, void* stream) {
+int ssm_scan_fwd_train_ex(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                          const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,
+                          void* y, float* last_state, float* checkpoints, int batch, int dim, int dstate, int seqlen,
+                          int io_dtype, int discretization, void* stream) {
   static_assert(SSM_SCAN_CHECKPOINT_STEPS == ssm::kScanChunk, "checkpoint interval");
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
   if (dstate > 16) return SSM_ERR_UNSUPPORTED;
   if (batch == 0 || dim == 0 || seqlen == 0) {
     return ssm_scan_fwd_ex(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, batch, dim, dstate,
-                           seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
+                           seqlen, io_dtype, discretization, stream);
   }
   if (!checkpoints) return SSM_ERR_NULL;
   if (!aligned(checkpoints, 4)) return SSM_ERR_ALIGN;
   return scan_fwd_common(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, checkpoints, batch,
-                         dim, dstate, seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
+                         dim, dstate, seqlen, io_dtype, discretization, stream);
+}
+
+int ssm_scan_fwd_train(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                       const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,
+                       void* y, float* last_state, float* checkpoints, int batch, int dim, int dstate, int seqlen,
+                       int io_dtype, void* stream) {
+  return ssm_scan_fwd_train_ex(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, checkpoints,
+                               batch, dim, dstate, seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
 }
 
 int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -154,13 +163,14 @@ int ssm_state_update(float* state, const void* x, const void* dt, const float* A
                              SSM_DISC_DELTA_B, stream);
 }
 
-int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
-                 const void* z, const float* dt_bias, int delta_softplus, const float* checkpoints,
-                 const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
-                 float* ddt_bias, float* dh0, int batch, int dim, int dstate, int seqlen, int io_dtype,
-                 void* stream) {
+int ssm_scan_bwd_ex(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* checkpoints,
+                    const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                    float* ddt_bias, float* dh0, int batch, int dim, int dstate, int seqlen, int io_dtype,
+                    int discretization, void* stream) {
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
   if (dstate > 16) return SSM_ERR_UNSUPPORTED;
   if (batch == 0 || dim == 0) return SSM_OK;
   if (!A || !dA) return SSM_ERR_NULL;
@@ -183,8 +193,18 @@ int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B
   a.batch = batch, a.dim = dim, a.dstate = dstate, a.seqlen = seqlen;
   a.softplus = delta_softplus ? 1 : 0;
   a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  a.zoh = discretization == SSM_DISC_ZOH ? 1 : 0;
   const cudaError_t err = ssm::launch_scan_bwd(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+int ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                 const void* z, const float* dt_bias, int delta_softplus, const float* checkpoints,
+                 const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD, void* dz,
+                 float* ddt_bias, float* dh0, int batch, int dim, int dstate, int seqlen, int io_dtype,
+                 void* stream) {
+  return ssm_scan_bwd_ex(u, delta, A, B, C, D, z, dt_bias, delta_softplus, checkpoints, dout, du, ddelta, dA, dB, dC,
+                         dD, dz, ddt_bias, dh0, batch, dim, dstate, seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
 }
 
 int ssm_causal_conv1d_fwd(const void* x, const float* weight, const float* bias, const void* state_in, void* out,

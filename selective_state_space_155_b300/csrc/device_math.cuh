@@ -81,6 +81,24 @@ __device__ __forceinline__ float2 zoh_factor2(float2 x, float2 abar, float2 delt
   return make_float2(fabsf(x.x) < 0.125f ? p.x : q.x, fabsf(x.y) < 0.125f ? p.y : q.y);
 }
 
+// d(Bbar/B)/da of the zero-order hold, for the backward pass: with c = zoh_factor(...),
+// dc/da = (Delta abar - c) / a = Delta^2 phi(x), phi(x) = (x e^x - e^x + 1) / x^2.  For |x| >= 1/2
+// the first form cancels by at most a few bits.  Below that it is Delta^2 times phi's Taylor
+// series, sum_k (k+1)/(k+2)! x^k through x^7, whose first omitted term is under 1e-7 relative
+// there; that branch also covers a = 0 (limit Delta^2 / 2), where inv_a is never used.
+__device__ __forceinline__ float2 zoh_factor_da2(float2 x, float2 abar, float2 delta, float2 c, float2 inv_a) {
+  float2 p = __ffma2_rn(x, make_float2(1.0f / 45360.0f, 1.0f / 45360.0f), make_float2(1.0f / 5760.0f, 1.0f / 5760.0f));
+  p = __ffma2_rn(x, p, make_float2(1.0f / 840.0f, 1.0f / 840.0f));
+  p = __ffma2_rn(x, p, make_float2(1.0f / 144.0f, 1.0f / 144.0f));
+  p = __ffma2_rn(x, p, make_float2(1.0f / 30.0f, 1.0f / 30.0f));
+  p = __ffma2_rn(x, p, make_float2(1.0f / 8.0f, 1.0f / 8.0f));
+  p = __ffma2_rn(x, p, make_float2(1.0f / 3.0f, 1.0f / 3.0f));
+  p = __ffma2_rn(x, p, make_float2(0.5f, 0.5f));
+  p = __fmul2_rn(p, __fmul2_rn(delta, delta));
+  const float2 q = __fmul2_rn(__ffma2_rn(delta, abar, make_float2(-c.x, -c.y)), inv_a);
+  return make_float2(fabsf(x.x) < 0.5f ? p.x : q.x, fabsf(x.y) < 0.5f ? p.y : q.y);
+}
+
 // 1/a for the zero-order-hold factor (0 where a = 0: that state always takes the series branch).
 __device__ __forceinline__ float zoh_inv(float a) { return a != 0.0f ? 1.0f / a : 0.0f; }
 

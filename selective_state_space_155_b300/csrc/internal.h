@@ -76,6 +76,7 @@ struct ScanBwdArgs {
   int batch, dim, dstate, seqlen;
   int softplus;
   int io;
+  int zoh;  // 1: exact zero-order hold for B, 0: Delta*B
 };
 
 // Arguments of one decode step; pointer and layout meaning as in ssm_scan.h.

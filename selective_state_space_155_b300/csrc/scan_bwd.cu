@@ -1,15 +1,18 @@
-// Backward pass of the selective scan (Delta*B discretisation) for sm_103a.
+// Backward pass of the selective scan for sm_103a, for either discretisation of B.
 //
 // Forward, per batch row b, channel d, state n (see scan_fwd.cu):
-//   Delta_t = softplus(delta_t + dt_bias[d]),  a_t = exp(Delta_t A[d,n]),  h_t = a_t h_{t-1} + Delta_t B_t u_t
+//   Delta_t = softplus(delta_t + dt_bias[d]),  a_t = exp(Delta_t A[d,n]),  h_t = a_t h_{t-1} + c_t B_t u_t
 //   y_t = sum_n C_t h_t + D u_t,  out_t = y_t silu(z_t)
+// with c_t = Delta_t (Delta*B form) or c_t = (a_t - 1) / A (exact zero-order hold, ZOH).
 // Backward, for dout_t = dLoss/dout_t, with dy_t = dout_t silu(z_t) and the adjoint state
 //   lambda_t = dy_t C_t + a_{t+1} lambda_{t+1}      (run from t = L-1 down to 0):
-//   du_t     = dy_t D + Delta_t sum_n lambda_t B_t
-//   dDelta_t = sum_n lambda_t (A a_t h_{t-1} + B_t u_t),   ddelta_t = dDelta_t sigmoid(delta_t + dt_bias)
-//   dA       = sum_{b,t} lambda_t Delta_t a_t h_{t-1},     dB_t = sum_d lambda_t Delta_t u_t
+//   du_t     = dy_t D + sum_n lambda_t c_t B_t
+//   dDelta_t = sum_n lambda_t (A a_t h_{t-1} + dc/dDelta B_t u_t),   ddelta_t = dDelta_t sigmoid(delta_t + dt_bias)
+//   dA       = sum_{b,t} lambda_t (Delta_t a_t h_{t-1} + dc/dA B_t u_t),    dB_t = sum_d lambda_t c_t u_t
 //   dC_t     = sum_d dy_t h_t,   dD = sum_{b,t} dy_t u_t,   dz_t = dout_t y_t silu'(z_t)
 //   ddt_bias = sum_{b,t} ddelta_t,   dh0 = a_0 lambda_0
+// where dc/dDelta = 1 and dc/dA = 0 in the Delta*B form, and dc/dDelta = a_t and
+// dc/dA = (Delta_t a_t - c_t) / A under the hold (zoh_factor_da in device_math.cuh).
 //
 // Layout of the work.  A CTA owns 32 channels of one batch row; lane (g, cw) of warp w holds
 // states 4g .. 4g+3 of channel 8w + cw (the forward's four-lanes-per-channel layout).  Chunks of
@@ -54,11 +57,11 @@ struct __align__(16) BwdSmem {
   float sg[kCPB][kTS];   // dDelta/ddelta: sigmoid(delta + dt_bias) with softplus, else 1
   float qz[kCPB][kTS];   // dout * silu'(z)
   float yv[kCPB][kTS];   // y before the gate, recomputed
-  float gu[kCPB][kTS];   // sum_n lambda B
+  float gu[kCPB][kTS];   // sum_n lambda B (Delta*B form) or sum_n lambda c B (hold)
   float gd[kCPB][kTS];   // dDelta
 };
 
-template <typename T>
+template <typename T, bool ZOH>
 __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) {
   __shared__ BwdSmem sm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -78,15 +81,25 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
   const int cw = lane & 7, g = lane >> 3;
   const int cl = warp * 8 + cw, d = d0 + cl;
   const bool ch_ok = d < dim;
-  float An[4], An2[4], carry[4], dA[4];
+  float An[4], An2[4], iA[4], carry[4], dA[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int n = 4 * g + i;
     An[i] = (ch_ok && n < N) ? a.A[size_t(d) * N + n] : 0.0f;
     An2[i] = An[i] * kLog2e;
+    iA[i] = ZOH ? zoh_inv(An[i]) : 0.0f;
     carry[i] = 0.0f;
     dA[i] = 0.0f;
   }
+  const float2 ln2 = f2(kLn2, kLn2);
+  // B's factor c_t (and a_t) of one state pair at step t: Bbar u = c (u B) as in the forward
+  auto bbar_u = [&](float2 dl2, float2 gp, float2 ap, int p, float2 ub) {
+    if constexpr (ZOH) {
+      return __fmul2_rn(zoh_factor2(__fmul2_rn(gp, ln2), ap, dl2, f2(iA[2 * p], iA[2 * p + 1])), ub);
+    } else {
+      return ub;  // u already carries Delta
+    }
+  };
   // epilogue role: channel tid / 4, steps 8 (tid % 4) + j
   const int ec = tid >> 2, eq = tid & 3;
   const int ed = d0 + ec;
@@ -186,15 +199,14 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
 #pragma unroll
         for (int j = 0; j < kS; ++j) {
           const int t = sb * kS + j;
-          const float dl = sm.dl[cl][t], du = dl * sm.uu[cl][t];
+          const float dl = sm.dl[cl][t], du = ZOH ? sm.uu[cl][t] : dl * sm.uu[cl][t];
           const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
           const float4 cc = *reinterpret_cast<const float4*>(&sm.Cs[t][4 * g]);
           const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
           const float2 g01 = __fmul2_rn(dl2, f2(An2[0], An2[1])), g23 = __fmul2_rn(dl2, f2(An2[2], An2[3]));
-          const float2 h01 = __ffma2_rn(f2(ex2_approx(g01.x), ex2_approx(g01.y)), f2(h[0], h[1]),
-                                        __fmul2_rn(du2, f2(bb.x, bb.y)));
-          const float2 h23 = __ffma2_rn(f2(ex2_approx(g23.x), ex2_approx(g23.y)), f2(h[2], h[3]),
-                                        __fmul2_rn(du2, f2(bb.z, bb.w)));
+          const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y)), a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
+          const float2 h01 = __ffma2_rn(a01, f2(h[0], h[1]), bbar_u(dl2, g01, a01, 0, __fmul2_rn(du2, f2(bb.x, bb.y))));
+          const float2 h23 = __ffma2_rn(a23, f2(h[2], h[3]), bbar_u(dl2, g23, a23, 1, __fmul2_rn(du2, f2(bb.z, bb.w))));
           h[0] = h01.x, h[1] = h01.y, h[2] = h23.x, h[3] = h23.y;
           const float2 yp2 = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
           float yp = yp2.x + yp2.y;
@@ -217,12 +229,13 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
 #pragma unroll
         for (int j = 0; j < kS; ++j) {
           const int t = sb * kS + j;
-          const float dl = sm.dl[cl][t], du = dl * sm.uu[cl][t];
+          const float dl = sm.dl[cl][t], du = ZOH ? sm.uu[cl][t] : dl * sm.uu[cl][t];
           const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
           const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
           const float2 g01 = __fmul2_rn(dl2, f2(An2[0], An2[1])), g23 = __fmul2_rn(dl2, f2(An2[2], An2[3]));
-          h01 = __ffma2_rn(f2(ex2_approx(g01.x), ex2_approx(g01.y)), h01, __fmul2_rn(du2, f2(bb.x, bb.y)));
-          h23 = __ffma2_rn(f2(ex2_approx(g23.x), ex2_approx(g23.y)), h23, __fmul2_rn(du2, f2(bb.z, bb.w)));
+          const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y)), a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
+          h01 = __ffma2_rn(a01, h01, bbar_u(dl2, g01, a01, 0, __fmul2_rn(du2, f2(bb.x, bb.y))));
+          h23 = __ffma2_rn(a23, h23, bbar_u(dl2, g23, a23, 1, __fmul2_rn(du2, f2(bb.z, bb.w))));
           ht[j][0] = h01, ht[j][1] = h23;
         }
       }
@@ -245,12 +258,26 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
           const float2 lam = __ffma2_rn(dy2, cp[p], f2(carry[2 * p], carry[2 * p + 1]));
           const float2 ahp = __fmul2_rn(ap, hp);
           const float2 vc = __fmul2_rn(dy2, ht[j][p]);  // dC
-          const float2 vb = __fmul2_rn(lam, du2);       // dB
-          v[2 * p] = vb.x, v[2 * p + 1] = vb.y, v[4 + 2 * p] = vc.x, v[4 + 2 * p + 1] = vc.y;
-          gu2 = __ffma2_rn(lam, bp[p], gu2);
-          gd2 = __ffma2_rn(lam, __ffma2_rn(Ap, ahp, __fmul2_rn(bp[p], u2)), gd2);
-          const float2 da = __ffma2_rn(__fmul2_rn(lam, dl2), ahp, f2(dA[2 * p], dA[2 * p + 1]));
-          dA[2 * p] = da.x, dA[2 * p + 1] = da.y;
+          if constexpr (ZOH) {
+            const float2 xp = __fmul2_rn(gp, ln2), ia = f2(iA[2 * p], iA[2 * p + 1]);
+            const float2 cz = zoh_factor2(xp, ap, dl2, ia);
+            const float2 lc = __fmul2_rn(lam, cz), bu = __fmul2_rn(bp[p], u2);
+            const float2 vb = __fmul2_rn(lc, u2);  // dB = lambda c u
+            v[2 * p] = vb.x, v[2 * p + 1] = vb.y, v[4 + 2 * p] = vc.x, v[4 + 2 * p + 1] = vc.y;
+            gu2 = __ffma2_rn(lc, bp[p], gu2);
+            // dc/dDelta = a: dDelta gets lambda a (A h_{t-1} + B u)
+            gd2 = __ffma2_rn(lam, __fmul2_rn(ap, __ffma2_rn(Ap, hp, bu)), gd2);
+            const float2 dcda = zoh_factor_da2(xp, ap, dl2, cz, ia);
+            const float2 da = __ffma2_rn(lam, __ffma2_rn(dl2, ahp, __fmul2_rn(dcda, bu)), f2(dA[2 * p], dA[2 * p + 1]));
+            dA[2 * p] = da.x, dA[2 * p + 1] = da.y;
+          } else {
+            const float2 vb = __fmul2_rn(lam, du2);  // dB
+            v[2 * p] = vb.x, v[2 * p + 1] = vb.y, v[4 + 2 * p] = vc.x, v[4 + 2 * p + 1] = vc.y;
+            gu2 = __ffma2_rn(lam, bp[p], gu2);
+            gd2 = __ffma2_rn(lam, __ffma2_rn(Ap, ahp, __fmul2_rn(bp[p], u2)), gd2);
+            const float2 da = __ffma2_rn(__fmul2_rn(lam, dl2), ahp, f2(dA[2 * p], dA[2 * p + 1]));
+            dA[2 * p] = da.x, dA[2 * p + 1] = da.y;
+          }
           const float2 cr = __fmul2_rn(lam, ap);
           carry[2 * p] = cr.x, carry[2 * p + 1] = cr.y;
         }
@@ -286,7 +313,8 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
       const int t = eq * (kK / 4) + j, tg = t0 + t;
       if (e_ok && tg < L) {
         const float dl = sm.dl[ec][t], u = sm.uu[ec][t], dyv = sm.dy[ec][t];
-        const float dut = fmaf(dyv, eD, dl * sm.gu[ec][t]);
+        // sum_n lambda c B: the Delta*B form leaves c = Delta out of the sum
+        const float dut = fmaf(dyv, eD, ZOH ? sm.gu[ec][t] : dl * sm.gu[ec][t]);
         const float ddl = sm.gd[ec][t] * sm.sg[ec][t];
         const size_t off = (size_t(b) * dim + ed) * L + tg;
         static_cast<T*>(a.du)[off] = from_f32<T>(dut);
@@ -373,8 +401,11 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream) {
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   ScanBwdArgs args = a;
   void* params[] = {&args};
-  const void* fn = a.io == kF32 ? reinterpret_cast<const void*>(scan_bwd_kernel<float>)
-                                : reinterpret_cast<const void*>(scan_bwd_kernel<__nv_bfloat16>);
+  const void* fn =
+      a.io == kF32 ? (a.zoh ? reinterpret_cast<const void*>(scan_bwd_kernel<float, true>)
+                            : reinterpret_cast<const void*>(scan_bwd_kernel<float, false>))
+                   : (a.zoh ? reinterpret_cast<const void*>(scan_bwd_kernel<__nv_bfloat16, true>)
+                            : reinterpret_cast<const void*>(scan_bwd_kernel<__nv_bfloat16, false>));
   return cudaLaunchKernel(fn, dim3(unsigned(nblk)), dim3(kThr), params, 0, stream);
 }
 

@@ -32,8 +32,8 @@ def test_header_declares_the_boundary():
     assert declared_functions() == sorted(
         ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_scan_fwd_ex", "ssm_state_update",
          "ssm_state_update_ex", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update",
-         "ssm_scan_num_checkpoints", "ssm_scan_fwd_train", "ssm_scan_bwd", "ssm_probe_cycles",
-         "ssm_probe_ops_per_cta"])
+         "ssm_scan_num_checkpoints", "ssm_scan_fwd_train", "ssm_scan_fwd_train_ex", "ssm_scan_bwd",
+         "ssm_scan_bwd_ex", "ssm_probe_cycles", "ssm_probe_ops_per_cta"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.ssm_abi_version() == 2
+    assert lib.ssm_abi_version() == 3
     for code in range(-8, 1):
         s = lib.ssm_status_string(code).decode()
         assert s and s != "unknown status"
@@ -207,6 +207,12 @@ def test_train_forward_validation(lib):
     assert lib.ssm_scan_fwd_train(*train) == _native.SSM_ERR_NULL  # checkpoints missing
     train = args[:9] + [None] + args[9:11] + [P + 2] + args[11:]
     assert lib.ssm_scan_fwd_train(*train) == _native.SSM_ERR_ALIGN
+    # the _ex form: same checks, plus the discretization code
+    train = args[:9] + [None] + args[9:11] + [None] + args[11:-1]
+    for disc in (_native.SSM_DISC_DELTA_B, _native.SSM_DISC_ZOH):
+        assert lib.ssm_scan_fwd_train_ex(*train, disc, None) == _native.SSM_ERR_NULL
+    for disc in (-1, 2):
+        assert lib.ssm_scan_fwd_train_ex(*train, disc, None) == _native.SSM_ERR_ARG
 
 
 def bwd_args(**over):
@@ -233,6 +239,13 @@ def bwd_args(**over):
 ])
 def test_bwd_validation(lib, over, expected):
     assert lib.ssm_scan_bwd(*bwd_args(**over)) == expected
+    for disc in (_native.SSM_DISC_DELTA_B, _native.SSM_DISC_ZOH):
+        assert lib.ssm_scan_bwd_ex(*bwd_args(**over)[:-1], disc, None) == expected
+
+
+@pytest.mark.parametrize("disc", [-1, 2, 7])
+def test_bwd_ex_rejects_unknown_discretization(lib, disc):
+    assert lib.ssm_scan_bwd_ex(*bwd_args()[:-1], disc, None) == _native.SSM_ERR_ARG
 
 
 def test_probe_validation(lib):
@@ -254,3 +267,5 @@ def test_grid_overflow_is_refused_before_any_launch(lib):
     assert lib.ssm_state_update(*update_args(batch=big, dim=big)) == _native.SSM_ERR_UNSUPPORTED
     assert lib.ssm_causal_conv1d_fwd(*conv_args(batch=big, dim=big)) == _native.SSM_ERR_UNSUPPORTED
     assert lib.ssm_scan_bwd(*bwd_args(batch=big, dim=64)) == _native.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_scan_bwd_ex(*bwd_args(batch=big, dim=64)[:-1], _native.SSM_DISC_ZOH, None) == \
+        _native.SSM_ERR_UNSUPPORTED

@@ -29,26 +29,28 @@ def norm_close(got, ref, tol, what):
     assert err <= tol * scale, f"{what}: max|got-ref| = {err:.3e} > {tol:.1e} * {scale:.3e}"
 
 
-def train_step(inp, dout, softplus=True, h0=None, need_dh0=False):
+def train_step(inp, dout, softplus=True, h0=None, need_dh0=False, disc="delta_b"):
     batch, dim, L = inp["u"].shape
     N = inp["A"].shape[1]
     ck = torch.empty((batch, ssm.scan_num_checkpoints(L), dim, N), dtype=torch.float32, device=DEV)
     y, last = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp.get("D"), inp.get("z"),
-                               inp.get("dt_bias"), delta_softplus=softplus, h0=h0, checkpoints=ck)
+                               inp.get("dt_bias"), delta_softplus=softplus, h0=h0, checkpoints=ck,
+                               discretization=disc)
     g = ssm.ssm_scan_bwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], ck, dout, D=inp.get("D"),
-                         z=inp.get("z"), dt_bias=inp.get("dt_bias"), delta_softplus=softplus, need_dh0=need_dh0)
+                         z=inp.get("z"), dt_bias=inp.get("dt_bias"), delta_softplus=softplus, need_dh0=need_dh0,
+                         discretization=disc)
     torch.cuda.synchronize()
     return y, last, ck, g
 
 
-def check_bwd(inp, softplus=True, h0=None, seed=0, what=""):
+def check_bwd(inp, softplus=True, h0=None, seed=0, what="", disc="delta_b"):
     io = io_name(inp["u"])
     gen = torch.Generator().manual_seed(seed)
     dout = torch.randn(inp["u"].shape, generator=gen).to(inp["u"].dtype).to(DEV)
-    y, last, ck, g = train_step(inp, dout, softplus, h0, need_dh0=h0 is not None)
+    y, last, ck, g = train_step(inp, dout, softplus, h0, need_dh0=h0 is not None, disc=disc)
     ref = oracle.scan_bwd(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), f(dout),
                           D=f(inp.get("D")), z=f(inp.get("z")), dt_bias=f(inp.get("dt_bias")),
-                          delta_softplus=softplus, h0=f(h0) if h0 is not None else None)
+                          delta_softplus=softplus, h0=f(h0) if h0 is not None else None, zoh=disc == "zoh")
     assert set(ref) <= set(g) | ({"dh0"} if h0 is None else set()), (sorted(ref), sorted(g))
     for k, r in ref.items():
         if k == "dh0" and h0 is None:
@@ -116,3 +118,75 @@ def test_training_forward_matches_forward_and_checkpoints(io):
         pre = {k: (v[..., :32 * c].contiguous() if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
         _, s_ref = oracle_scan(pre, h0=inp["h0"])
         assert_close(ckn[:, c], s_ref, 1e-4, f"checkpoint {c}")
+
+
+# ---- the exact zero-order hold: the same cases, plus the decay regimes its factor branches on ----
+
+@pytest.mark.parametrize("w", [wl.TINY, wl.SMALL], ids=lambda w: w.name)
+def test_zoh_workload_backward_parity(w):
+    inp = wl.scan_inputs(w, device=DEV)
+    check_bwd(inp, what="zoh " + w.name, disc="zoh")
+
+
+def test_zoh_mid_workload_backward_parity():
+    """Batch 8, d_inner 1536, d_state 16, L 2048, bf16, under the hold: every gradient element."""
+    inp = wl.scan_inputs(wl.MID, device=DEV)
+    check_bwd(inp, seed=4, what="zoh mid", disc="zoh")
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 1, 1, 1, "f32"), (2, 33, 16, 65, "f32"), (3, 31, 3, 100, "f32"), (2, 40, 5, 63, "bf16"),
+    (2, 65, 8, 129, "bf16"), (2, 7, 16, 1, "f32"), (1, 50, 16, 300, "f32"),
+], ids=lambda s: "b{}_d{}_n{}_l{}_{}".format(*s))
+def test_zoh_edge_shapes_backward(shape):
+    batch, dim, dstate, seqlen, io = shape
+    inp = to_device(wl.random_scan_case(batch, dim, dstate, seqlen, io=io, seed=seqlen * 5 + dim), DEV)
+    check_bwd(inp, seed=seqlen + 1, what="zoh " + str(shape), disc="zoh")
+
+
+@pytest.mark.parametrize("gate,use_D,use_bias,softplus", [
+    (False, False, False, False), (True, True, True, True), (True, False, True, False)])
+def test_zoh_optional_arguments_backward(gate, use_D, use_bias, softplus):
+    inp = to_device(wl.random_scan_case(2, 48, 16, 136, io="f32", seed=6, gate=gate, use_D=use_D,
+                                        use_bias=use_bias, softplus=softplus), DEV)
+    check_bwd(inp, softplus=softplus, what="zoh optional args", disc="zoh")
+
+
+def test_zoh_initial_state_gradient():
+    inp = to_device(wl.random_scan_case(2, 40, 16, 96, io="f32", seed=8, h0=True), DEV)
+    check_bwd(inp, h0=inp["h0"], what="zoh h0", disc="zoh")
+
+
+@pytest.mark.parametrize("regime", ["near_zero", "mixed"])
+def test_zoh_backward_decay_regimes(regime):
+    """A on both sides of the factor's series/direct switch: near_zero puts every A in [-2e-3, 0]
+    with some exactly 0 (the limits Delta and Delta^2/2); mixed spreads |A| over 1e-4 .. 30, so
+    Delta*A runs from about -1e-4 to beyond -50 in one channel."""
+    inp = to_device(wl.random_scan_case(2, 64, 16, 160, io="f32", seed=13), DEV)
+    rng = np.random.default_rng(17 if regime == "near_zero" else 19)
+    if regime == "near_zero":
+        A = -rng.uniform(0.0, 2e-3, tuple(inp["A"].shape))
+        A[:, ::5] = 0.0
+    else:
+        A = -np.exp(rng.uniform(np.log(1e-4), np.log(30.0), tuple(inp["A"].shape)))
+    inp["A"] = torch.from_numpy(A.astype(np.float32)).to(DEV)
+    check_bwd(inp, seed=3, what="zoh " + regime, disc="zoh")
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+def test_zoh_training_forward_matches_forward_and_checkpoints(io):
+    """The training forward under the hold returns the plain hold forward's y and last_state, and
+    its checkpoint c is the oracle's hold state after the first 32c steps."""
+    inp = to_device(wl.random_scan_case(2, 40, 16, 200, io=io, seed=10, h0=True), DEV)
+    dout = torch.zeros_like(inp["u"])
+    y, last, ck, _ = train_step(inp, dout, h0=inp["h0"], disc="zoh")
+    y0, last0 = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                 inp["dt_bias"], h0=inp["h0"], discretization="zoh")
+    torch.cuda.synchronize()
+    assert torch.equal(y, y0) and torch.equal(last, last0)
+    ckn = f(ck)
+    np.testing.assert_array_equal(ckn[:, 0], f(inp["h0"]))
+    for c in range(1, ckn.shape[1]):
+        pre = {k: (v[..., :32 * c].contiguous() if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
+        _, s_ref = oracle_scan(pre, h0=inp["h0"], zoh=True)
+        assert_close(ckn[:, c], s_ref, 1e-4, f"zoh checkpoint {c}")
