@@ -58,13 +58,14 @@ def test_scan_outputs_stay_in_bounds(shape, variant, monkeypatch):
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}_d{}_n{}_l{}_{}".format(*s))
-def test_training_pair_outputs_stay_in_bounds(shape):
+@pytest.mark.parametrize("disc", ["delta_b", "zoh"])
+def test_training_pair_outputs_stay_in_bounds(shape, disc):
     batch, dim, N, L, io = shape
     inp = to_device(wl.random_scan_case(batch, dim, N, L, io=io, seed=L + 1), DEV)
     ck = Guarded((batch, ssm.scan_num_checkpoints(L), dim, N), torch.float32)
     y = Guarded((batch, dim, L), inp["u"].dtype)
     ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["dt_bias"],
-                     y=y.view, checkpoints=ck.view)
+                     y=y.view, checkpoints=ck.view, discretization=disc)
     ck.check("checkpoints")
     y.check("y (training forward)")
     dout = torch.randn(inp["u"].shape, device=DEV).to(inp["u"].dtype)
@@ -74,11 +75,12 @@ def test_training_pair_outputs_stay_in_bounds(shape):
         "dB": ((batch, N, L), torch.float32), "dC": ((batch, N, L), torch.float32), "dD": ((dim,), torch.float32),
         "ddt_bias": ((dim,), torch.float32), "dh0": ((batch, dim, N), torch.float32)}.items()}
     p = lambda t: t.data_ptr()
-    st = ssm.lib().ssm_scan_bwd(p(inp["u"]), p(inp["delta"]), p(inp["A"]), p(inp["B"]), p(inp["C"]), p(inp["D"]),
-                                p(inp["z"]), p(inp["dt_bias"]), 1, p(ck.view), p(dout), p(g["du"].view),
-                                p(g["ddelta"].view), p(g["dA"].view), p(g["dB"].view), p(g["dC"].view),
-                                p(g["dD"].view), p(g["dz"].view), p(g["ddt_bias"].view), p(g["dh0"].view),
-                                batch, dim, N, L, ssm.io_dtype_code(inp["u"].dtype), None)
+    st = ssm.lib().ssm_scan_bwd_ex(p(inp["u"]), p(inp["delta"]), p(inp["A"]), p(inp["B"]), p(inp["C"]),
+                                   p(inp["D"]), p(inp["z"]), p(inp["dt_bias"]), 1, p(ck.view), p(dout),
+                                   p(g["du"].view), p(g["ddelta"].view), p(g["dA"].view), p(g["dB"].view),
+                                   p(g["dC"].view), p(g["dD"].view), p(g["dz"].view), p(g["ddt_bias"].view),
+                                   p(g["dh0"].view), batch, dim, N, L, ssm.io_dtype_code(inp["u"].dtype),
+                                   1 if disc == "zoh" else 0, None)
     assert st == 0
     for k, b in g.items():
         b.check(k)
