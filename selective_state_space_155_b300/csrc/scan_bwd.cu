@@ -17,8 +17,9 @@
 // Layout of the work.  A CTA owns 32 channels of one batch row; lane (g, cw) of warp w holds
 // states 4g .. 4g+3 of channel 8w + cw (the forward's four-lanes-per-channel layout).  Chunks of
 // 32 steps are processed last to first.  For each chunk all 128 threads stage the per-(channel,
-// step) values (Delta, u, dy, the softplus and silu derivatives) and B, C into shared memory from
-// registers that were loaded while the previous chunk was being computed;
+// step) values (Delta, u, dy, the softplus and silu derivatives) and B, C into shared-memory
+// tables from raw input rows that were copied into shared memory (16-byte cp.async when rows are
+// 16-byte aligned) while the previous chunk was being computed;
 // then every lane recomputes the chunk forward from the state the forward pass checkpointed at
 // its start, keeping the state at the start of each 8-step sub-chunk, and walks the sub-chunks
 // last to first: it recomputes the sub-chunk's 8 states and decay factors into registers and
@@ -30,6 +31,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
+
+#include <atomic>
 
 #include "device_math.cuh"
 #include "internal.h"
@@ -61,9 +64,28 @@ struct __align__(16) BwdSmem {
   float gd[kCPB][kTS];   // dDelta
 };
 
-template <typename T, bool ZOH>
+// Raw input rows of one chunk, as copied from global memory.
+template <typename T>
+struct __align__(16) BwdRaw {
+  static constexpr int kEPV = 16 / int(sizeof(T));  // elements per 16-byte copy
+  static constexpr int kPPR = kK / kEPV;            // 16-byte copies per 32-step row
+  static constexpr int kRSBC = kK + kEPV;           // B/C row stride, padded against bank conflicts
+  T x[4][kCPB][kK];    // u, delta, z, dout
+  T bc[2][16][kRSBC];  // B, C
+  float ck[kCPB][16];  // the state at the chunk's start
+};
+
+template <typename T>
+constexpr size_t bwd_smem_bytes() {
+  return sizeof(BwdSmem) + sizeof(BwdRaw<T>);
+}
+
+template <typename T, bool ZOH, bool VEC>
 __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) {
-  __shared__ BwdSmem sm;
+  extern __shared__ __align__(16) unsigned char smem_bytes[];
+  BwdSmem& sm = *reinterpret_cast<BwdSmem*>(smem_bytes);
+  using Raw = BwdRaw<T>;
+  Raw& raw = *reinterpret_cast<Raw*>(smem_bytes + sizeof(BwdSmem));
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int dim = a.dim, N = a.dstate, L = a.seqlen;
   const int nblk_d = (dim + kCPB - 1) / kCPB;
@@ -108,65 +130,95 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
   float accD = 0.0f, accBias = 0.0f;
   const bool has_z = gz != nullptr;
 
-  // Raw inputs of the next chunk to process (the previous one in time), loaded into registers
-  // while the current chunk is being computed.  Thread tid stages step tid % 32 of channels
-  // tid / 32 + 4j (j < 8), and (B or C, state, step) items tid + 128j (j < 8).
-  constexpr int kEl = kCPB * kK / kThr, kBC = 2 * 16 * kK / kThr;
-  static_assert(kEl == 8 && kBC == 8, "staging split");
-  T r_u[kEl], r_d[kEl], r_z[kEl], r_g[kEl], r_bc[kBC];
-  float r_ck[4];
-  auto prefetch = [&](int k) {
-    const int t0 = k * kK, t = tid & (kK - 1), tg = t0 + t;
+  // Copies of the raw inputs of chunk k (the next one to process, the previous one in time) into
+  // the raw rows.  With VEC (every row 16-byte aligned) they are asynchronous 16-byte copies that
+  // land while the current chunk is computed; otherwise plain loads and stores.  Copies past the
+  // end of a row or of the channels are skipped: the staging never reads those elements.
+  auto gx = [&](int x) { return x == 0 ? gu_ : x == 1 ? gdl : x == 2 ? gz : gdo; };  // x known at compile time
+  const bool ck_vec = VEC && (N % 4) == 0 && (reinterpret_cast<uintptr_t>(a.ckpt) & 15u) == 0;
+  auto issue = [&](int k) {
+    const int t0 = k * kK;
+    if constexpr (VEC) {
+      constexpr int kXP = kCPB * Raw::kPPR;  // copies per input tensor
+      static_assert(kXP % kThr == 0, "copy split");
 #pragma unroll
-    for (int j = 0; j < kEl; ++j) {
-      const int dd = d0 + (tid >> 5) + 4 * j;
-      const bool ok = dd < dim && tg < L;
-      const size_t off = (size_t(b) * dim + (ok ? dd : 0)) * L + (ok ? tg : 0);
-      r_u[j] = ok ? gu_[off] : from_f32<T>(0.0f);
-      r_d[j] = ok ? gdl[off] : from_f32<T>(0.0f);
-      r_z[j] = (ok && has_z) ? gz[off] : from_f32<T>(0.0f);
-      r_g[j] = ok ? gdo[off] : from_f32<T>(0.0f);
-    }
+      for (int x = 0; x < 4; ++x) {
+        const T* src = gx(x);
+        if (src == nullptr) continue;
 #pragma unroll
-    for (int j = 0; j < kBC; ++j) {
-      // consecutive threads take consecutive states of a step: conflict-free table stores later
-      const int e = tid + kThr * j;
-      const int which = e / (16 * kK), r = e % (16 * kK), n = r % 16, tt = r / 16;
-      const int tgb = t0 + tt;
-      const T* src = which ? gC : gB;
-      r_bc[j] = (n < N && tgb < L) ? src[(size_t(b) * N + n) * L + tgb] : from_f32<T>(0.0f);
-    }
+        for (int i = 0; i < kXP / kThr; ++i) {
+          const int p = tid + kThr * i;
+          const int r = p / Raw::kPPR, j = p % Raw::kPPR;
+          const int dd = d0 + r, t = t0 + j * Raw::kEPV;
+          if (dd < dim && t < L) cp_async_16(&raw.x[x][r][j * Raw::kEPV], src + (size_t(b) * dim + dd) * L + t, 16);
+        }
+      }
+      constexpr int kBP = 2 * 16 * Raw::kPPR;
+      static_assert(kBP % kThr == 0, "copy split");
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int n = 4 * g + i;
-      r_ck[i] = (ch_ok && n < N) ? a.ckpt[((size_t(b) * nck + k) * dim + d) * N + n] : 0.0f;
+      for (int i = 0; i < kBP / kThr; ++i) {
+        const int p = tid + kThr * i;
+        const int which = p / (16 * Raw::kPPR), n = (p / Raw::kPPR) % 16, j = p % Raw::kPPR;
+        const int t = t0 + j * Raw::kEPV;
+        if (n < N && t < L)
+          cp_async_16(&raw.bc[which][n][j * Raw::kEPV], (which ? gC : gB) + (size_t(b) * N + n) * L + t, 16);
+      }
+    } else {
+#pragma unroll
+      for (int x = 0; x < 4; ++x) {
+        const T* src = gx(x);
+        if (src == nullptr) continue;
+        for (int e = tid; e < kCPB * kK; e += kThr) {
+          const int r = e / kK, t = e % kK;
+          const int dd = d0 + r, tg = t0 + t;
+          if (dd < dim && tg < L) raw.x[x][r][t] = src[(size_t(b) * dim + dd) * L + tg];
+        }
+      }
+      for (int e = tid; e < 2 * 16 * kK; e += kThr) {
+        const int which = e / (16 * kK), n = (e / kK) % 16, t = e % kK;
+        const int tg = t0 + t;
+        if (n < N && tg < L) raw.bc[which][n][t] = (which ? gC : gB)[(size_t(b) * N + n) * L + tg];
+      }
     }
+    const float* ck = a.ckpt + (size_t(b) * nck + k) * dim * size_t(N);
+    if (ck_vec) {
+      // one 16-byte copy per (channel, 4 states): 32 x 4 = kThr copies
+      const int c = tid >> 2, q = tid & 3;
+      if (d0 + c < dim && 4 * q < N) cp_async_16(&raw.ck[c][4 * q], ck + size_t(d0 + c) * N + 4 * q, 16);
+    } else {
+      for (int e = tid; e < kCPB * 16; e += kThr) {
+        const int c = e >> 4, n = e & 15;
+        if (d0 + c < dim && n < N) raw.ck[c][n] = ck[size_t(d0 + c) * N + n];
+      }
+    }
+    cp_async_commit();
   };
-  prefetch(nck - 1);
+  issue(nck - 1);
 
   for (int k = nck - 1; k >= 0; --k) {
     const int t0 = k * kK;
-    __syncthreads();  // the previous chunk is finished with every table
-    // ---- stage the chunk from the prefetched registers ----
+    cp_async_wait<0>();  // this thread's copies of chunk k have landed
+    __syncthreads();     // everyone's have, and the previous chunk is finished with every table
+    // ---- stage the chunk's tables from the raw rows ----
     {
       const int t = tid & (kK - 1), tg = t0 + t;
 #pragma unroll
-      for (int j = 0; j < kEl; ++j) {
+      for (int j = 0; j < kCPB * kK / kThr; ++j) {
         const int c = (tid >> 5) + 4 * j, dd = d0 + c;
         float dl = 0.0f, u = 0.0f, dyv = 0.0f, sgv = 0.0f, qzv = 0.0f;
         if (dd < dim && tg < L) {
-          u = to_f32<T>(r_u[j]);
-          const float raw = to_f32<T>(r_d[j]) + (a.dt_bias ? a.dt_bias[dd] : 0.0f);
+          u = to_f32<T>(raw.x[0][c][t]);
+          const float raw_d = to_f32<T>(raw.x[1][c][t]) + (a.dt_bias ? a.dt_bias[dd] : 0.0f);
           if (a.softplus) {
-            dl = softplus_f32(raw);
-            sgv = rcp_approx(1.0f + ex2_approx(-raw * kLog2e));
+            dl = softplus_f32(raw_d);
+            sgv = rcp_approx(1.0f + ex2_approx(-raw_d * kLog2e));
           } else {
-            dl = raw;
+            dl = raw_d;
             sgv = 1.0f;
           }
-          const float go = to_f32<T>(r_g[j]);
+          const float go = to_f32<T>(raw.x[3][c][t]);
           if (has_z) {
-            const float zz = to_f32<T>(r_z[j]);
+            const float zz = to_f32<T>(raw.x[2][c][t]);
             const float s = rcp_approx(1.0f + ex2_approx(-zz * kLog2e));
             dyv = go * (zz * s);
             qzv = go * (s * (1.0f + zz * (1.0f - s)));
@@ -176,17 +228,20 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
         }
         sm.dl[c][t] = dl, sm.uu[c][t] = u, sm.dy[c][t] = dyv, sm.sg[c][t] = sgv, sm.qz[c][t] = qzv;
       }
+      // consecutive threads take consecutive states of a step: conflict-free table stores
 #pragma unroll
-      for (int j = 0; j < kBC; ++j) {
+      for (int j = 0; j < 2 * 16 * kK / kThr; ++j) {
         const int e = tid + kThr * j;
         const int which = e / (16 * kK), r = e % (16 * kK), n = r % 16, tt = r / 16;
-        (which ? sm.Cs : sm.Bs)[tt][n] = to_f32<T>(r_bc[j]);
+        (which ? sm.Cs : sm.Bs)[tt][n] = (n < N && t0 + tt < L) ? to_f32<T>(raw.bc[which][n][tt]) : 0.0f;
       }
     }
     for (int e = tid; e < kK * 2 * 16; e += kThr) (&sm.acc[0][0][0])[e] = 0.0f;
-    float ck0[4] = {r_ck[0], r_ck[1], r_ck[2], r_ck[3]};
-    if (k > 0) prefetch(k - 1);  // in flight while this chunk is computed
-    __syncthreads();
+    float ck0[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ck0[i] = (ch_ok && 4 * g + i < N) ? raw.ck[cl][4 * g + i] : 0.0f;
+    __syncthreads();     // tables written; the raw rows are free
+    if (k > 0) issue(k - 1);  // in flight while this chunk is computed
 
     // ---- recurrence role: forward recompute of the chunk, keeping each sub-chunk's start ----
     float hs[kSub][4];
@@ -364,6 +419,35 @@ __global__ void __launch_bounds__(256) zero_kernel(const ZeroSpans z) {
     for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < z.n[s]; i += stride) z.p[s][i] = 0.0f;
 }
 
+// Rows of every per-(batch, channel) and per-(batch, state) input are 16-byte aligned.
+template <typename T>
+bool rows_vectorisable(const ScanBwdArgs& a) {
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  return (size_t(a.seqlen) * sizeof(T)) % 16 == 0 && al(a.u) && al(a.delta) && al(a.z) && al(a.dout) && al(a.B) &&
+         al(a.C);
+}
+
+template <typename T, bool ZOH, bool VEC>
+cudaError_t launch_bwd(const ScanBwdArgs& a, long long nblk, cudaStream_t stream) {
+  auto kernel = scan_bwd_kernel<T, ZOH, VEC>;
+  constexpr size_t kSmem = bwd_smem_bytes<T>();
+  // the dynamic shared-memory opt-in is a per-device function attribute; set it once per device
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem));
+    if (err != cudaSuccess) return err;
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  ScanBwdArgs args = a;
+  void* params[] = {&args};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(unsigned(nblk)), dim3(kThr), params, kSmem,
+                          stream);
+}
+
 }  // namespace
 
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream) {
@@ -399,14 +483,15 @@ cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream) {
   const long long nblk = (long long)((a.dim + kCPB - 1) / kCPB) * a.batch;
   if (nblk <= 0) return cudaSuccess;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-  ScanBwdArgs args = a;
-  void* params[] = {&args};
-  const void* fn =
-      a.io == kF32 ? (a.zoh ? reinterpret_cast<const void*>(scan_bwd_kernel<float, true>)
-                            : reinterpret_cast<const void*>(scan_bwd_kernel<float, false>))
-                   : (a.zoh ? reinterpret_cast<const void*>(scan_bwd_kernel<__nv_bfloat16, true>)
-                            : reinterpret_cast<const void*>(scan_bwd_kernel<__nv_bfloat16, false>));
-  return cudaLaunchKernel(fn, dim3(unsigned(nblk)), dim3(kThr), params, 0, stream);
+  if (a.io == kF32) {
+    const bool vec = rows_vectorisable<float>(a);
+    if (a.zoh) return vec ? launch_bwd<float, true, true>(a, nblk, stream) : launch_bwd<float, true, false>(a, nblk, stream);
+    return vec ? launch_bwd<float, false, true>(a, nblk, stream) : launch_bwd<float, false, false>(a, nblk, stream);
+  }
+  using bf = __nv_bfloat16;
+  const bool vec = rows_vectorisable<bf>(a);
+  if (a.zoh) return vec ? launch_bwd<bf, true, true>(a, nblk, stream) : launch_bwd<bf, true, false>(a, nblk, stream);
+  return vec ? launch_bwd<bf, false, true>(a, nblk, stream) : launch_bwd<bf, false, false>(a, nblk, stream);
 }
 
 }  // namespace ssm
