@@ -16,7 +16,8 @@ Extra objects on the line:
   roofline_alu  the same launches against the special-function (MUFU) peak, the scan's co-bound,
                 with the per-SM rate measured by the library's probe kernels (unit_rates);
   e2e           the same metric through the public API with pinned host buffers: host->device
-                copy of the step's inputs, the scan, device->host copy of y and the final state;
+                copy of the step's inputs, the scan, device->host copy of y and the final state,
+                pipelined by batch row over three streams so that copies and scans overlap;
   cpu_baseline  the float64 oracle on the host cores (reported baseline, not a target), all
                 cores and one thread, and the benchmarked kernel's output checked against it on a
                 slice of the workload (parity);
@@ -418,8 +419,12 @@ def workload_config(w):
                   f"{w.algorithmic_bytes() / 1e6:.0f} MB", "parallelism": "independent replica per GPU"}
 
 
-def run_e2e(w, device, steps, warmup, dist):
-    """The scan through the public API from pinned host buffers: H2D inputs, scan, D2H y + state."""
+def run_e2e(w, device, steps, warmup, dist, slices=None):
+    """The scan through the public API from pinned host buffers: every step copies the step's
+    inputs host->device, scans, and copies y and the final state device->host.  Batch rows are
+    independent, so the step is pipelined over `slices` batch-row slices and three streams: the
+    scan of slice i and its device->host copies overlap the host->device copy of slice i + 1
+    (PCIe is full duplex).  Returns (ms per step, h2d bytes, d2h bytes, slices)."""
     import selective_state_space_155_b300 as ssm
     host = wl.scan_inputs(w, device="cpu")
     host = {k: (v.pin_memory() if v is not None else None) for k, v in host.items()}
@@ -430,18 +435,50 @@ def run_e2e(w, device, steps, warmup, dist):
     s_d = torch.empty((w.batch, w.dim, w.dstate), dtype=torch.float32, device=device)
     h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
     d2h = y_h.numel() * y_h.element_size() + s_h.numel() * 4
+    slices = slices or w.batch
+    bounds = [(w.batch * i // slices, w.batch * (i + 1) // slices) for i in range(slices)]
+    per_row = ("u", "delta", "z", "B", "C")  # [batch, ...] inputs; A, D, dt_bias are per channel
+    comp = torch.cuda.current_stream(device)
+    up, down = torch.cuda.Stream(device), torch.cuda.Stream(device)
 
     def step(_i):
-        for k, v in host.items():
-            if v is not None:
-                dev[k].copy_(v, non_blocking=True)
-        ssm.ssm_scan_fwd(dev["u"], dev["delta"], dev["A"], dev["B"], dev["C"], dev["D"], dev["z"], dev["dt_bias"],
-                         delta_softplus=True, y=y_d, last_state=s_d)
-        y_h.copy_(y_d, non_blocking=True)
-        s_h.copy_(s_d, non_blocking=True)
+        start = torch.cuda.Event()
+        start.record(comp)
+        up.wait_event(start)  # no copy starts before the step (or overwrites the previous step's inputs)
+        with torch.cuda.stream(up):
+            for k in ("A", "D", "dt_bias"):
+                if host[k] is not None:
+                    dev[k].copy_(host[k], non_blocking=True)
+        for b0, b1 in bounds:
+            with torch.cuda.stream(up):
+                for k in per_row:
+                    if host[k] is not None:
+                        dev[k][b0:b1].copy_(host[k][b0:b1], non_blocking=True)
+                landed = torch.cuda.Event()
+                landed.record(up)
+            comp.wait_event(landed)
+            d = {k: (dev[k][b0:b1] if k in per_row and dev[k] is not None else dev[k]) for k in dev}
+            ssm.ssm_scan_fwd(d["u"], d["delta"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
+                             delta_softplus=True, y=y_d[b0:b1], last_state=s_d[b0:b1], stream=comp)
+            done = torch.cuda.Event()
+            done.record(comp)
+            down.wait_event(done)
+            with torch.cuda.stream(down):
+                y_h[b0:b1].copy_(y_d[b0:b1], non_blocking=True)
+                s_h[b0:b1].copy_(s_d[b0:b1], non_blocking=True)
+        back = torch.cuda.Event()
+        back.record(down)
+        comp.wait_event(back)  # the step ends when its last device->host copy has
 
     ms = max_over_ranks(timed(step, steps, warmup, dist), dist)
-    return ms, h2d, d2h
+    # the pipelined result must be the scan's: compare with one plain call on the device inputs
+    torch.cuda.synchronize()
+    y_ref, s_ref = ssm.ssm_scan_fwd(dev["u"], dev["delta"], dev["A"], dev["B"], dev["C"], dev["D"], dev["z"],
+                                    dev["dt_bias"], delta_softplus=True)
+    torch.cuda.synchronize()
+    if not (torch.equal(y_h, y_ref.cpu()) and torch.equal(s_h, s_ref.cpu())):
+        raise RuntimeError("e2e: the pipelined step's output differs from one scan of the same inputs")
+    return ms, h2d, d2h, slices
 
 
 # The scan is a co-bound of HBM and the special-function unit: per element the recurrence takes
@@ -701,9 +738,10 @@ def main(argv=None):
         "unit_rates": {"unit": "lane-operations per clock per SM", **rates},
     }
     if not args.no_e2e:
-        e2e_ms, h2d, d2h = run_e2e(w, device, max(3, min(args.steps, 20)), 2, dist)
+        e2e_ms, h2d, d2h, nsl = run_e2e(w, device, max(3, min(args.steps, 20)), 2, dist)
         res["e2e"] = {"value": elems / (e2e_ms * 1e-3), "unit": "elements/s", "h2d_bytes_per_step": h2d,
-                      "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+                      "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                      "pipeline": f"{nsl} batch-row slices over three streams (H2D, scan, D2H)"}
     if rank == 0 and not args.no_decode:
         res["decode"] = run_decode(device)
     if rank == 0 and not args.no_zoh:

@@ -23,8 +23,9 @@
 // then every lane recomputes the chunk forward from the state the forward pass checkpointed at
 // its start, keeping the state at the start of each 8-step sub-chunk, and walks the sub-chunks
 // last to first: it recomputes the sub-chunk's 8 states and decay factors into registers and
-// runs the adjoint recurrence backwards over them.  Sums over a channel's 4 lanes (du, dDelta,
-// y) take two shuffles; dB and dC, shared by all channels, are reduce-scattered over the 8
+// runs the adjoint recurrence backwards over them.  Sums over a channel's 4 lanes take two
+// shuffles (y) or two shuffles for the du and dDelta sums together (a reduce-scatter that leaves
+// one of them on each lane); dB and dC, shared by all channels, are reduce-scattered over the 8
 // channels of a warp by shuffles and added across the warps in shared memory, then added to the
 // float32 outputs with one atomic per (state, step) and CTA.  dA, dD and ddt_bias are added
 // across CTAs the same way; the launcher zeroes these accumulated outputs first.
@@ -294,6 +295,12 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
           ht[j][0] = h01, ht[j][1] = h23;
         }
       }
+      // Each step's dB/dC sum (and, in the Delta*B form, its du/dDelta sums) is kept in registers
+      // and stored after the sub-chunk's steps, so that the stores and shared-memory atomics do
+      // not hold back the loads of the next steps.  Under ZOH, whose arithmetic needs more live
+      // registers, the du/dDelta sums are stored at once.
+      constexpr bool kDeferG = !ZOH;
+      float rr[kS], gg[kS];
 #pragma unroll
       for (int j = kS - 1; j >= 0; --j) {
         const int t = sb * kS + j;
@@ -336,13 +343,15 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
           const float2 cr = __fmul2_rn(lam, ap);
           carry[2 * p] = cr.x, carry[2 * p + 1] = cr.y;
         }
-        float gup = gu2.x + gu2.y, gdp = gd2.x + gd2.y;
-        // sums over the channel's four lanes
-        gup += __shfl_xor_sync(0xffffffffu, gup, 8);
-        gup += __shfl_xor_sync(0xffffffffu, gup, 16);
-        gdp += __shfl_xor_sync(0xffffffffu, gdp, 8);
-        gdp += __shfl_xor_sync(0xffffffffu, gdp, 16);
-        if (g == 0) sm.gu[cl][t] = gup, sm.gd[cl][t] = gdp;
+        const float gup = gu2.x + gu2.y, gdp = gd2.x + gd2.y;
+        // sums over the channel's four lanes, reduce-scattered: lanes with even g end with the
+        // du sum, lanes with odd g the dDelta sum
+        const bool odd = g & 1;
+        const float gs = (odd ? gdp : gup) + __shfl_xor_sync(0xffffffffu, odd ? gup : gdp, 8);
+        gg[j] = gs + __shfl_xor_sync(0xffffffffu, gs, 16);
+        if constexpr (!kDeferG) {
+          if (g < 2) (odd ? sm.gd : sm.gu)[cl][t] = gg[j];
+        }
         // dB, dC summed over the warp's 8 channels: reduce-scatter over cw, lane keeps value cw
         float w[4], x[2];
 #pragma unroll
@@ -356,8 +365,15 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
           x[q] = keep + __shfl_xor_sync(0xffffffffu, send, 2);
         }
         const float send = k3 ? x[0] : x[1], keep = k3 ? x[1] : x[0];
-        const float r = keep + __shfl_xor_sync(0xffffffffu, send, 1);
-        atomicAdd(&sm.acc[t][cw >> 2][4 * g + (cw & 3)], r);
+        rr[j] = keep + __shfl_xor_sync(0xffffffffu, send, 1);
+      }
+#pragma unroll
+      for (int j = 0; j < kS; ++j) {
+        const int t = sb * kS + j;
+        atomicAdd(&sm.acc[t][cw >> 2][4 * g + (cw & 3)], rr[j]);
+        if constexpr (kDeferG) {
+          if (g < 2) ((g & 1) ? sm.gd : sm.gu)[cl][t] = gg[j];
+        }
       }
     }
     __syncthreads();
