@@ -62,6 +62,7 @@ struct __align__(16) BwdSmem {
   float qz[kCPB][kTS];   // dout * silu'(z)
   float yv[kCPB][kTS];   // y before the gate, recomputed
   float gu[kCPB][kTS];   // sum_n lambda B (Delta*B form) or sum_n lambda c B (hold)
+  float pad[16];         // puts gd[c][t] 16 banks away from gu[c][t]: one store writes both
   float gd[kCPB][kTS];   // dDelta
 };
 
@@ -239,8 +240,12 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
     }
     for (int e = tid; e < kK * 2 * 16; e += kThr) (&sm.acc[0][0][0])[e] = 0.0f;
     float ck0[4];
+    {
+      const float4 c4 = *reinterpret_cast<const float4*>(&raw.ck[cl][4 * g]);  // conflict-free
+      const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) ck0[i] = (ch_ok && 4 * g + i < N) ? raw.ck[cl][4 * g + i] : 0.0f;
+      for (int i = 0; i < 4; ++i) ck0[i] = (ch_ok && 4 * g + i < N) ? cv[i] : 0.0f;
+    }
     __syncthreads();     // tables written; the raw rows are free
     if (k > 0) issue(k - 1);  // in flight while this chunk is computed
 
