@@ -12,7 +12,7 @@
 //   dC_t     = sum_d dy_t h_t,   dD = sum_{b,t} dy_t u_t,   dz_t = dout_t y_t silu'(z_t)
 //   ddt_bias = sum_{b,t} ddelta_t,   dh0 = a_0 lambda_0
 // where dc/dDelta = 1 and dc/dA = 0 in the Delta*B form, and dc/dDelta = a_t and
-// dc/dA = (Delta_t a_t - c_t) / A under the hold (zoh_factor_da in device_math.cuh).
+// dc/dA = (Delta_t a_t - c_t) / A under the hold (zoh_factor_da2 in device_math.cuh).
 //
 // Layout of the work.  A CTA owns 32 channels of one batch row; lane (g, cw) of warp w holds
 // states 4g .. 4g+3 of channel 8w + cw (the forward's four-lanes-per-channel layout).  Chunks of
@@ -26,8 +26,9 @@
 // runs the adjoint recurrence backwards over them.  Sums over a channel's 4 lanes take two
 // shuffles (y) or two shuffles for the du and dDelta sums together (a reduce-scatter that leaves
 // one of them on each lane); dB and dC, shared by all channels, are reduce-scattered over the 8
-// channels of a warp by shuffles and added across the warps in shared memory, then added to the
-// float32 outputs with one atomic per (state, step) and CTA.  dA, dD and ddt_bias are added
+// channels of a warp by shuffles; a step's sums wait in registers until its sub-chunk ends, are
+// then added across the warps in shared memory, and finally added to the float32 outputs with
+// one atomic per (state, step) and CTA.  dA, dD and ddt_bias are added
 // across CTAs the same way; the launcher zeroes these accumulated outputs first.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
