@@ -613,7 +613,8 @@ def run_decode(device, steps_graph=3, warmup=1):
         "cold_l2_frac_of_hbm": bytes_step / (cold_ms * 1e-3) / 1e9 / hbm,
         "algorithmic_bytes_per_step": bytes_step, "peak": hbm, "peak_source": src,
         "note": "the 84 MB float32 state fits in L2, so back-to-back steps can exceed HBM bandwidth",
-        "traffic": committed_traffic("state_update_kernel"),
+        "traffic": committed_traffic("state_update_tiled_kernel"),
+        "kernel": "state_update_tiled_kernel",
     }
 
 

@@ -86,7 +86,8 @@ def test_training_pair_outputs_stay_in_bounds(shape, disc):
         b.check(k)
 
 
-@pytest.mark.parametrize("shape", [(2, 33, 16, "bf16"), (3, 37, 5, "f32"), (1, 129, 8, "bf16")])
+@pytest.mark.parametrize("shape", [(2, 33, 16, "bf16"), (3, 37, 5, "f32"), (1, 129, 8, "bf16"),
+                                   (37, 1800, 16, "bf16"), (33, 2000, 16, "f32"), (16, 4096, 16, "bf16")])
 def test_decode_outputs_stay_in_bounds(shape):
     batch, dim, N, io = shape
     dt_ = torch.float32 if io == "f32" else torch.bfloat16
