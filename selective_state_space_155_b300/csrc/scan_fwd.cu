@@ -33,6 +33,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
@@ -179,14 +180,17 @@ __device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) 
   }
 }
 
+// One group of warps (4 prep + R recurrence) scanning the channels [d0, dlim) of batch row b, at
+// most CPB of them, with its own shared-memory block `smem` and the named barriers bar0 + 1 ..
+// bar0 + 5; tid is the thread's index within the group.  A CTA of the plain kernel is one group.
 template <typename T, int NPAD, bool VEC, bool ZOH>
-__global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const ScanArgs a) {
+__device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* smem, const int tid, const int b,
+                                           const int d0, const int dlim, const int bar0) {
   using Cfg = ScanCfg<T, NPAD>;
   constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, RS = Cfg::RS, VPR = Cfg::VPR;
   constexpr int NT = Cfg::NT, PT = Cfg::PT, ROWS = Cfg::ROWS, PSS = Cfg::PSS, DSS = Cfg::DSS, OPL = Cfg::OPL;
   constexpr int UPB = Cfg::UPB, CWARPS = Cfg::CWARPS;
 
-  extern __shared__ __align__(16) unsigned char smem[];
   T* raw = reinterpret_cast<T*>(smem);
   unsigned char* tab = smem + Cfg::kRaw;
   float4* red = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kTab);
@@ -197,10 +201,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
     return reinterpret_cast<float2*>(tab + s * Cfg::kTabStage + Cfg::kBCStage + Cfg::kPStage);
   };
 
-  const int tid = threadIdx.x;
-  const int nblk_d = (a.dim + CPB - 1) / CPB;
-  const int b = blockIdx.x / nblk_d;
-  const int d0 = (blockIdx.x % nblk_d) * CPB;
+  const int bFull0 = kBarFull0 + bar0, bEmpty0 = kBarEmpty0 + bar0, bPrep = kBarPrep + bar0;
   const int warp = tid >> 5, lane = tid & 31;
   const int L = a.seqlen, N = a.dstate;
   const bool has_z = a.z != nullptr;
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
       if (r < 3 * CPB) {
         const int which = r / CPB, c = r % CPB;
         const T* base = which == 0 ? gu : (which == 1 ? gd : gz);
-        ok = (d0 + c < dim) && (which < 2 || has_z);
+        ok = (d0 + c < dlim) && (which < 2 || has_z);
         fill = false;
         return ok ? base + (size_t(b) * dim + (d0 + c)) * L : gu;
       }
@@ -303,7 +304,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
     constexpr int PPL = 32 / PCW;          // step-pair lanes per channel (4)
     const int pcl = pw * PCW + (lane % PCW);
     const int tq = lane / PCW;
-    const bool pch_ok = d0 + pcl < dim;
+    const bool pch_ok = d0 + pcl < dlim;
     const float p_bias = (pch_ok && a.dt_bias) ? a.dt_bias[d0 + pcl] : 0.0f;
     const float p_D = (pch_ok && a.D) ? a.D[d0 + pcl] : 0.0f;
     const int r_ofs = pcl * RS + 2 * tq;     // element offset of this lane's first step pair in a row
@@ -319,8 +320,8 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
       const int s = k & 1;
       const int t0 = k * kChunk;
       cp_async_wait<1>();           // this thread's copies of chunk k have landed
-      bar_sync(kBarPrep, PT);       // ... and every prep thread's
-      if (k >= 2) bar_sync(kBarEmpty0 + s, NT);  // the recurrence warps are done with table stage s
+      bar_sync(bPrep, PT);          // ... and every prep thread's
+      if (k >= 2) bar_sync(bEmpty0 + s, NT);  // the recurrence warps are done with table stage s
 
       const T* st = raw + size_t(s) * ROWS * RS;
       float* BCs = tabBs(s);
@@ -370,14 +371,14 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
       else
         items(std::true_type{});
 
-      bar_sync(kBarPrep, PT);            // every prep thread is done reading raw stage s
-      bar_arrive(kBarFull0 + s, NT);     // table stage s is ready
+      bar_sync(bPrep, PT);               // every prep thread is done reading raw stage s
+      bar_arrive(bFull0 + s, NT);        // table stage s is ready
       if (k + 2 < nchunks) stage_load(s, t0 + 2 * kChunk);
       cp_async_commit();
     }
     cp_async_wait<0>();
     // match the recurrence warps' last arrivals so that no barrier is left half-arrived
-    for (int k = max(0, nchunks - 2); k < nchunks; ++k) bar_sync(kBarEmpty0 + (k & 1), NT);
+    for (int k = max(0, nchunks - 2); k < nchunks; ++k) bar_sync(bEmpty0 + (k & 1), NT);
     return;
   }
 
@@ -388,7 +389,15 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   const int cw = lane % CPW, g = lane / CPW;
   const int cl = warp * CPW + cw;  // this lane's channel within the CTA
   const int d = d0 + cl;
-  const bool ch_ok = d < a.dim;
+  const bool ch_ok = d < dlim;
+  if (d0 + warp * CPW >= dlim) {
+    // none of this warp's channels is in the group: keep the table hand-off, skip the work
+    for (int k = 0; k < nchunks; ++k) {
+      bar_sync(bFull0 + (k & 1), NT);
+      bar_arrive(bEmpty0 + (k & 1), NT);
+    }
+    return;
+  }
 
   float2 A01, A23, h01, h23, iA01, iA23;
   {
@@ -419,7 +428,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
       for (int i = 0; i < 4; ++i)
         if (4 * g + i < N) cp[4 * g + i] = hv[i];
     }
-    bar_sync(kBarFull0 + s, NT);
+    bar_sync(bFull0 + s, NT);
     const float* Bs = tabBs(s);
     const float* Cs = tabCs(s);
     const float2* Ps = tabPs(s);
@@ -492,7 +501,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
       const int tg = t0 + tb;  // first global step
       if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, L - tg);
     }
-    bar_arrive(kBarEmpty0 + s, NT);  // table stage s may be refilled
+    bar_arrive(bEmpty0 + s, NT);  // table stage s may be refilled
   }
 
   if (a.last_state && ch_ok) {
@@ -505,9 +514,120 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   }
 }
 
+// The plain kernel: CTA blockIdx.x scans 32-channel block (blockIdx.x % blocks per row) of batch
+// row blockIdx.x / blocks per row.
+template <typename T, int NPAD, bool VEC, bool ZOH>
+__global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const ScanArgs a) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  constexpr int CPB = ScanCfg<T, NPAD>::CPB;
+  const int nblk_d = (a.dim + CPB - 1) / CPB;
+  const int b = blockIdx.x / nblk_d;
+  const int d0 = (blockIdx.x % nblk_d) * CPB;
+  scan_group<T, NPAD, VEC, ZOH>(a, smem, threadIdx.x, b, d0, a.dim, 0);
+}
+
+// The balanced form: one CTA per SM holding kFusedGroups groups, each on a channel range (8 to 32
+// channels of one batch row) from a host plan that evens out the channels per SM.  With 32-channel
+// CTAs an SM carries 64 or 96 channels when the total is not a multiple of 96 per SM; the plan
+// gives every SM within 8 channels of the mean.  Plan entry: b << 16 | (d0 / 8) << 4 | (channels / 8),
+// 0 for an empty group.
+constexpr int kFusedGroups = 3;
+constexpr int kMaxFusedCtas = 160;
+struct FusedPlan {
+  uint32_t e[kFusedGroups * kMaxFusedCtas];
+};
+
+template <typename T, int NPAD, bool VEC, bool ZOH>
+__global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
+    scan_fwd_fused_kernel(const ScanArgs a, const FusedPlan plan) {
+  extern __shared__ __align__(16) unsigned char smem[];
+  using Cfg = ScanCfg<T, NPAD>;
+  const int grp = threadIdx.x / Cfg::NT;
+  const uint32_t e = plan.e[blockIdx.x * kFusedGroups + grp];
+  const int nch = int(e & 15u) * 8;
+  if (nch == 0) return;  // an empty group: its warps leave, the other groups do not wait on them
+  const int b = int(e >> 16), d0 = int((e >> 4) & 0xfffu) * 8;
+  scan_group<T, NPAD, VEC, ZOH>(a, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0,
+                                min(a.dim, d0 + nch), 5 * grp);
+}
+
+// Host plan for the balanced form: units of 8 channels, groups of at most 4 units inside one batch
+// row, at most kFusedGroups groups per CTA, CTA c taking ceil(units left / CTAs left) units.
+// Returns the CTA count, or 0 when the plan does not apply or does not lower the busiest SM's load
+// below that of the plain kernel (32-channel CTAs spread over the SMs).
+int make_fused_plan(const ScanArgs& a, int sms, FusedPlan& plan) {
+  if (a.dim % 8 != 0 || a.batch >= (1 << 16) || a.dim / 8 >= (1 << 12) || sms <= 0 || sms > kMaxFusedCtas) return 0;
+  const long long ur = a.dim / 8, units = (long long)a.batch * ur;
+  if (units == 0 || units > (long long)sms * kFusedGroups * 4) return 0;
+  const long long blocks = (long long)a.batch * ((a.dim + 31) / 32);
+  const long long plain_max = 4 * ((blocks + sms - 1) / sms);  // units on the busiest SM, plain kernel
+  long long left = units, row = 0, pos = 0, worst = 0;
+  int ctas = 0;
+  for (int c = 0; c < sms && left > 0; ++c) {
+    const long long target = (left + (sms - c) - 1) / (sms - c);
+    long long load = 0;
+    for (int g = 0; g < kFusedGroups; ++g) {
+      uint32_t entry = 0;
+      if (load < target && row < a.batch) {
+        const long long take = std::min(std::min(4LL, target - load), ur - pos);
+        entry = uint32_t(row) << 16 | uint32_t(pos) << 4 | uint32_t(take);
+        load += take, pos += take, left -= take;
+        if (pos == ur) ++row, pos = 0;
+      }
+      plan.e[c * kFusedGroups + g] = entry;
+    }
+    worst = std::max(worst, load);
+    ctas = c + 1;
+  }
+  return (left == 0 && worst < plain_max) ? ctas : 0;
+}
+
+// Launches the balanced form when its plan applies (bf16, dstate 9..16: three groups' shared
+// memory fit one CTA); returns false when the plain kernel should run instead.
+template <typename T, int NPAD, bool VEC, bool ZOH>
+bool launch_fused(const ScanArgs& a, cudaStream_t stream, cudaError_t& err) {
+  using Cfg = ScanCfg<T, NPAD>;
+  if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
+    return false;
+  } else {
+    const char* force = std::getenv("SSM_SCAN_VARIANT");
+    if (force && std::strcmp(force, "quad") == 0) return false;
+    int dev = 0, sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return true;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return true;
+    FusedPlan plan;
+    const int ctas = make_fused_plan(a, sms, plan);
+    if (ctas == 0) return false;
+    auto kernel = scan_fwd_fused_kernel<T, NPAD, VEC, ZOH>;
+    constexpr size_t kSmem = kFusedGroups * Cfg::kSmem;
+    // once per device: the shared-memory opt-in, and whether the build has the register count the
+    // setmaxnreg split was sized for (if not, the plain kernel runs)
+    static std::atomic<uint64_t> configured{0}, usable{0};
+    const uint64_t bit = uint64_t(1) << (dev & 63);
+    if (!(configured.load(std::memory_order_acquire) & bit)) {
+      if ((err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem))) != cudaSuccess)
+        return true;
+      cudaFuncAttributes fa{};
+      if ((err = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return true;
+      if (fa.numRegs == kLaunchRegs) usable.fetch_or(bit, std::memory_order_acq_rel);
+      configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    if (!(usable.load(std::memory_order_acquire) & bit)) return false;
+    ScanArgs args = a;
+    void* params[] = {&args, &plan};
+    err = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(unsigned(ctas)), dim3(kFusedGroups * Cfg::NT),
+                           params, kSmem, stream);
+    return true;
+  }
+}
+
 template <typename T, int NPAD, bool VEC, bool ZOH>
 cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   using Cfg = ScanCfg<T, NPAD>;
+  {
+    cudaError_t err = cudaSuccess;
+    if (launch_fused<T, NPAD, VEC, ZOH>(a, stream, err)) return err;
+  }
   auto kernel = scan_fwd_kernel<T, NPAD, VEC, ZOH>;
   // The dynamic shared-memory opt-in is a per-device function attribute; set it once per device.
   static std::atomic<uint64_t> configured{0};
@@ -569,7 +689,9 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
   const bool vec = a.io == kF32 ? rows_vectorisable<float>(a) : rows_vectorisable<__nv_bfloat16>(a);
   // The four-lanes-per-channel form is the default at every size: measured on B300 it is 1.45x
   // faster than the lane-per-channel form even with 27-69 channel warps per SM (batch x dim of
-  // 82k-131k channels).  The lane form runs only when SSM_SCAN_VARIANT=lane asks for it.
+  // 82k-131k channels).  The lane form runs only when SSM_SCAN_VARIANT=lane asks for it.  Within
+  // the four-lanes form the balanced layout runs wherever its plan applies, the plain 32-channel
+  // CTAs elsewhere or when SSM_SCAN_VARIANT=quad asks for them.
   const char* force = std::getenv("SSM_SCAN_VARIANT");
   const bool lane = force && std::strcmp(force, "lane") == 0;
   return (lane && !a.zoh && !a.ckpt) ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);

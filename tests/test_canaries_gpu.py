@@ -36,13 +36,18 @@ class Guarded:
         assert bool((lo == -12345).all()) and bool((hi == -12345).all()), f"{what}: write outside the buffer"
 
 
-SHAPES = [(2, 33, 16, 65, "bf16"), (1, 40, 5, 63, "f32"), (3, 7, 3, 100, "bf16"), (1, 65, 8, 31, "f32")]
+# the last two take the balanced forward (bf16, dstate 16, dim a multiple of 8)
+SHAPES = [(2, 33, 16, 65, "bf16"), (1, 40, 5, 63, "f32"), (3, 7, 3, 100, "bf16"), (1, 65, 8, 31, "f32"),
+          (2, 40, 16, 65, "bf16"), (3, 1032, 16, 70, "bf16")]
 
 
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}_d{}_n{}_l{}_{}".format(*s))
-@pytest.mark.parametrize("variant", ["quad", "lane"])
+@pytest.mark.parametrize("variant", ["default", "quad", "lane"])
 def test_scan_outputs_stay_in_bounds(shape, variant, monkeypatch):
-    monkeypatch.setenv("SSM_SCAN_VARIANT", variant)
+    if variant == "default":  # the balanced form wherever its plan applies
+        monkeypatch.delenv("SSM_SCAN_VARIANT", raising=False)
+    else:
+        monkeypatch.setenv("SSM_SCAN_VARIANT", variant)
     batch, dim, N, L, io = shape
     inp = to_device(wl.random_scan_case(batch, dim, N, L, io=io, seed=L, h0=True), DEV)
     y = Guarded((batch, dim, L), inp["u"].dtype)
