@@ -86,7 +86,7 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  */
 typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization;
 
-/* Version of this ABI (bumped when a signature changes or an entry point is added): 3. */
+/* Version of this ABI (bumped when a signature changes or an entry point is added): 5. */
 int ssm_abi_version(void);
 
 /*
@@ -99,7 +99,7 @@ int ssm_abi_version(void);
  *   last_state     : [batch][dim][dstate] float32, receives h after the last step.
  *   delta_softplus : non-zero applies softplus to delta + dt_bias.
  * Required: u, delta, A, B, C, y.  Nullable: D (no skip), z (no gate), dt_bias (no
- * bias), last_state (not written).  y must not alias any input.
+ * bias), last_state (not written).  y must not overlap u, delta, z, B or C (SSM_ERR_ARG).
  * Returns an ssm_status.
  */
 int ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -125,6 +125,22 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void
                     const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
                     float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
                     void* stream);
+
+/*
+ * Which kernel form a scan of these sizes launches on the current device, without launching it.
+ * Both forms compute the same recurrence in the same order per state, so their results are
+ * bitwise equal; they differ in how channels are spread over SMs:
+ *   SSM_FORM_PLAIN     one CTA per 32-channel block of a batch row;
+ *   SSM_FORM_BALANCED  one CTA per SM holding up to three warp groups on host-planned channel
+ *                      ranges (bf16, dstate 9..16, dim a multiple of 8, where the plan lowers the
+ *                      busiest SM's load; SSM_SCAN_VARIANT=quad_plain in the environment turns it off).
+ * aligned_rows: non-zero when u, delta, z, B, C and y will be 16-byte aligned.  *ctas (nullable)
+ * receives the grid size.  Returns the form (>= 0) or a negative ssm_status (SSM_ERR_LAUNCH when
+ * no device can be queried).
+ */
+typedef enum { SSM_FORM_PLAIN = 0, SSM_FORM_BALANCED = 1 } ssm_scan_form;
+int ssm_scan_fwd_form(int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization, int aligned_rows,
+                      int* ctas);
 
 /*
  * Training forward: ssm_scan_fwd_h0 (Delta*B discretization) that also stores, for the backward
@@ -245,18 +261,46 @@ int ssm_causal_conv1d_update(void* state, const void* x, const float* weight, co
                              int batch, int dim, int width, int silu, int io_dtype, void* stream);
 
 /*
- * Throughput probes of the units the scan leans on (used to measure the peak of the benchmark's
- * special-function roofline on the machine it runs on).  kind: SSM_PROBE_EX2 (ex2.approx),
- * SSM_PROBE_FFMA (FP32 fused multiply-add), SSM_PROBE_FFMA2 (packed f32x2 fused multiply-add).
+ * Throughput probes of the units the scan leans on (used to measure the peaks of the benchmark's
+ * arithmetic rooflines on the machine it runs on).  kind:
+ *   SSM_PROBE_EX2        ex2.approx alone;
+ *   SSM_PROBE_FFMA       FP32 fused multiply-add alone;
+ *   SSM_PROBE_FFMA2      packed f32x2 fused multiply-add alone;
+ *   SSM_PROBE_EX2_FFMA2  one ex2 and one independent packed f32x2 FMA per chain step (counted in
+ *                        ex2 operations): whether the special-function and FP32 pipes overlap;
+ *   SSM_PROBE_RECURRENCE the scan's arithmetic per pair of states and step, with no memory
+ *                        traffic: f32x2 Delta*A, two ex2, f32x2 (Delta*u)*B, f32x2 h = Abar*h + b,
+ *                        f32x2 y += C*h (counted in state-steps, two per pair and step);
+ *   SSM_PROBE_WAIT_TIMEOUT  the forward kernels' bounded barrier wait on a barrier that nothing
+ *                        completes, with a limit of 2^20 cycles: each CTA must give up and writes
+ *                        the cycles it waited (-1 if the wait completed); ops_per_cta is 0.
  * Launches nblocks CTAs (use the SM count: one CTA per SM) of independent dependency chains and
  * writes each CTA's clock cycles for the measured loop to cycles[0..nblocks-1] (device memory,
- * int64).  ssm_probe_ops_per_cta(kind) is the number of lane-operations one CTA performs (an
- * f32x2 operation counts as two), so ops / cycles is that unit's rate per SM per clock.
- * Returns an ssm_status (SSM_ERR_ARG for an unknown kind).
+ * int64).  ssm_probe_ops_per_cta(kind) is the number of operations one CTA performs in those
+ * units (lane-operations for the single-unit kinds, an f32x2 operation counting as two), so
+ * ops / cycles is the rate per SM per clock.  Returns an ssm_status (SSM_ERR_ARG for an unknown
+ * kind); ssm_probe_ops_per_cta returns 0 for an unknown kind.
  */
-typedef enum { SSM_PROBE_EX2 = 0, SSM_PROBE_FFMA = 1, SSM_PROBE_FFMA2 = 2 } ssm_probe_kind;
+typedef enum {
+  SSM_PROBE_EX2 = 0,
+  SSM_PROBE_FFMA = 1,
+  SSM_PROBE_FFMA2 = 2,
+  SSM_PROBE_EX2_FFMA2 = 3,
+  SSM_PROBE_RECURRENCE = 4,
+  SSM_PROBE_WAIT_TIMEOUT = 5
+} ssm_probe_kind;
 int ssm_probe_cycles(int kind, long long* cycles, int nblocks, void* stream);
 double ssm_probe_ops_per_cta(int kind);
+
+/*
+ * Inside the forward kernels the warps that load and prepare each chunk hand it to the warps that
+ * run the recurrence through shared-memory barriers.  Every wait on them is bounded (about a
+ * second); a wait that gives up ends the kernel early, leaving y and the states undefined, and is
+ * counted.  This writes the number of such waits since the library was loaded to *count (after
+ * synchronising the device).  A correct build never gives up: non-zero means a defect or a device
+ * that stopped a kernel's warps for over a second.  Returns SSM_OK, SSM_ERR_NULL or SSM_ERR_LAUNCH.
+ */
+int ssm_wait_timeouts(unsigned long long* count);
 
 /* Static, NUL-terminated description of a status code (never NULL). */
 const char* ssm_status_string(int status);

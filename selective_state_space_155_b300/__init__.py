@@ -17,8 +17,9 @@ import torch
 from . import _native
 from ._native import SsmError, lib, status_string  # noqa: F401
 
-__all__ = ["ssm_scan_fwd", "ssm_scan_bwd", "scan_num_checkpoints", "ssm_state_update", "causal_conv1d_fwd",
-           "causal_conv1d_update", "probe_unit_rates", "SsmError", "lib", "status_string", "io_dtype_code"]
+__all__ = ["ssm_scan_fwd", "prepare_scan_fwd", "scan_fwd_form", "wait_timeouts", "ssm_scan_bwd", "scan_num_checkpoints", "ssm_state_update",
+           "causal_conv1d_fwd", "causal_conv1d_update", "probe_unit_rates", "SsmError", "lib", "status_string",
+           "io_dtype_code"]
 
 _IO = {torch.float32: _native.SSM_F32, torch.bfloat16: _native.SSM_BF16}
 _DISC = {"delta_b": _native.SSM_DISC_DELTA_B, "zoh": _native.SSM_DISC_ZOH}
@@ -111,6 +112,80 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus
     else:
         _native.check("ssm_scan_fwd_h0", lib().ssm_scan_fwd_h0(*args, h0p, *tail))
     return y, last_state
+
+
+class PreparedCall:
+    """One C-ABI call whose arguments were validated and turned into pointers once.  Calling it
+    enqueues the same work again on the stream fixed at preparation, with no per-call checks: the
+    tensors it was prepared from must stay alive, in place and unchanged in shape and dtype."""
+
+    __slots__ = ("_fn", "_args", "_name", "outputs")
+
+    def __init__(self, name: str, args: tuple, outputs: tuple):
+        self._fn = getattr(lib(), name)
+        self._args = args
+        self._name = name
+        self.outputs = outputs
+
+    def __call__(self):
+        st = self._fn(*self._args)
+        if st:
+            raise SsmError(self._name, st)
+
+
+def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, y=None, last_state=None,
+                     h0=None, return_last_state=True, stream=None, discretization="delta_b") -> PreparedCall:
+    """``ssm_scan_fwd_ex`` with every argument checked and marshalled once, for callers that repeat
+    the same scan on the same buffers (a benchmark loop, a fixed serving shape): the returned
+    PreparedCall enqueues it with one foreign call and nothing else.  Arguments as ssm_scan_fwd;
+    ``.outputs`` is (y, last_state)."""
+    disc = _disc(discretization)
+    batch, dim, L = u.shape
+    dstate = A.shape[1]
+    io = io_dtype_code(u.dtype)
+    if y is None:
+        y = torch.empty_like(u)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((batch, dim, dstate), dtype=torch.float32, device=u.device)
+    args = (
+        _ptr(u, u.dtype, (batch, dim, L), "u"),
+        _ptr(delta, u.dtype, (batch, dim, L), "delta"),
+        _ptr(A, torch.float32, (dim, dstate), "A"),
+        _ptr(B, u.dtype, (batch, dstate, L), "B"),
+        _ptr(C, u.dtype, (batch, dstate, L), "C"),
+        _ptr(D, torch.float32, (dim,), "D"),
+        _ptr(z, u.dtype, (batch, dim, L), "z"),
+        _ptr(dt_bias, torch.float32, (dim,), "dt_bias"),
+        int(bool(delta_softplus)),
+        _ptr(h0, torch.float32, (batch, dim, dstate), "h0"),
+        _ptr(y, u.dtype, (batch, dim, L), "y"),
+        _ptr(last_state, torch.float32, (batch, dim, dstate), "last_state"),
+        batch, dim, dstate, L, io, disc, _stream(stream),
+    )
+    return PreparedCall("ssm_scan_fwd_ex", args, (y, last_state))
+
+
+def scan_fwd_form(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bfloat16, discretization="delta_b",
+                  aligned_rows: bool = True) -> tuple[str, int]:
+    """(form name, CTAs) of the kernel a scan of these sizes launches on the current device
+    (``ssm_scan_fwd_form``): "plain" (one CTA per 32-channel block) or "balanced" (one CTA per SM
+    with up to three warp groups on planned channel ranges)."""
+    import ctypes
+    n = ctypes.c_int(0)
+    st = lib().ssm_scan_fwd_form(int(batch), int(dim), int(dstate), int(seqlen), io_dtype_code(dtype),
+                                 _disc(discretization), int(bool(aligned_rows)), ctypes.byref(n))
+    if st < 0:
+        raise SsmError("ssm_scan_fwd_form", st)
+    return _native.FORM_NAMES[st], n.value
+
+
+def wait_timeouts() -> int:
+    """Hand-off waits inside the forward kernels that gave up since the library was loaded
+    (``ssm_wait_timeouts``; synchronises the device).  0 on a healthy device."""
+    import ctypes
+    n = ctypes.c_ulonglong(0)
+    _native.check("ssm_wait_timeouts", lib().ssm_wait_timeouts(ctypes.byref(n)))
+    return int(n.value)
 
 
 def ssm_scan_bwd(u, delta, A, B, C, checkpoints, dout, D=None, z=None, dt_bias=None, delta_softplus=True,
@@ -242,14 +317,17 @@ def causal_conv1d_update(state, x, weight, bias=None, silu=True, out=None, strea
 
 
 def probe_unit_rates(device=None) -> dict:
-    """Measured lane-operations per clock per SM of ex2.approx, FP32 FMA and packed f32x2 FMA
-    (``ssm_probe_cycles``), the median over one CTA per SM."""
+    """Measured rates per clock per SM (``ssm_probe_cycles``), the median over one CTA per SM:
+    lane-operations of ex2.approx, FP32 FMA and packed f32x2 FMA alone; ex2 operations when each
+    ex2 shares its chain step with an independent f32x2 FMA (``ex2_with_ffma2``); state-steps of
+    the recurrence's arithmetic mix with no memory traffic (``recurrence``)."""
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     cycles = torch.empty(sms, dtype=torch.int64, device=dev)
     out = {}
     for name, kind in (("ex2", _native.SSM_PROBE_EX2), ("ffma", _native.SSM_PROBE_FFMA),
-                       ("ffma2", _native.SSM_PROBE_FFMA2)):
+                       ("ffma2", _native.SSM_PROBE_FFMA2), ("ex2_with_ffma2", _native.SSM_PROBE_EX2_FFMA2),
+                       ("recurrence", _native.SSM_PROBE_RECURRENCE)):
         for _ in range(2):  # the first launch warms up
             _native.check("ssm_probe_cycles", lib().ssm_probe_cycles(kind, _ptr(cycles, torch.int64, None, "cycles"),
                                                                      sms, _stream(None)))

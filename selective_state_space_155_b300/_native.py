@@ -27,9 +27,16 @@ SSM_BF16 = 1
 SSM_DISC_DELTA_B = 0
 SSM_DISC_ZOH = 1
 
+SSM_FORM_PLAIN = 0
+SSM_FORM_BALANCED = 1
+FORM_NAMES = {0: "plain", 1: "balanced"}
+
 SSM_PROBE_EX2 = 0
 SSM_PROBE_FFMA = 1
 SSM_PROBE_FFMA2 = 2
+SSM_PROBE_EX2_FFMA2 = 3
+SSM_PROBE_RECURRENCE = 4
+SSM_PROBE_WAIT_TIMEOUT = 5
 
 # Every symbol the header declares, with its ctypes signature.
 _vp, _fp, _i = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int
@@ -50,6 +57,8 @@ SIGNATURES = {
                                    _i, _vp]),
     "ssm_scan_bwd_ex": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
                              _fp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
+    "ssm_scan_fwd_form": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
+    "ssm_wait_timeouts": (_i, [ctypes.POINTER(ctypes.c_ulonglong)]),
     "ssm_probe_cycles": (_i, [_i, _vp, _i, _vp]),
     "ssm_probe_ops_per_cta": (ctypes.c_double, [_i]),
     "ssm_causal_conv1d_fwd": (_i, [_vp, _fp, _fp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp]),

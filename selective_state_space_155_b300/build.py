@@ -33,11 +33,27 @@ def _inputs() -> list[str]:
         os.path.join(INCLUDE, "ssm_scan.h"), os.path.abspath(__file__)]
 
 
+def _digest() -> str:
+    """Hash of every build input's bytes and of the compiler command: what the library was built from."""
+    import hashlib
+    h = hashlib.sha256(" ".join(ARCH + NVCC_FLAGS).encode())
+    for p in _inputs():
+        h.update(os.path.relpath(p, ROOT).encode())
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+STAMP = LIB + ".sha256"
+
+
 def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+    """The in-tree library exists and was built from the current sources (by content, not mtime:
+    a copied tree can carry a stale library with a newer timestamp)."""
+    if not (os.path.exists(LIB) and os.path.exists(STAMP)):
         return False
-    t = os.path.getmtime(LIB)
-    return all(os.path.getmtime(p) <= t for p in _inputs())
+    with open(STAMP) as f:
+        return f.read().strip() == _digest()
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
@@ -53,6 +69,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
         raise RuntimeError(f"nvcc failed ({res.returncode}): {' '.join(cmd)}")
     if verbose:
         sys.stdout.write(res.stdout + res.stderr)
+    with open(STAMP, "w") as f:
+        f.write(_digest() + "\n")
     return LIB
 
 

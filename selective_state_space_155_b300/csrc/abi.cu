@@ -12,11 +12,18 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 size_t io_size(int io) { return io == SSM_F32 ? 4 : 2; }
 
+// Whether the byte ranges [p, p + np) and [q, q + nq) share a byte (a NULL pointer shares none).
+bool overlaps(const void* p, size_t np, const void* q, size_t nq) {
+  if (!p || !q || np == 0 || nq == 0) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+  return a < b + nq && b < a + np;
+}
+
 }  // namespace
 
 extern "C" {
 
-int ssm_abi_version(void) { return 3; }
+int ssm_abi_version(void) { return 5; }
 
 const char* ssm_status_string(int status) {
   switch (status) {
@@ -57,6 +64,19 @@ int scan_fwd_common(const void* u, const void* delta, const float* A, const void
   for (const void* p : f_ptrs)
     if (!aligned(p, 4)) return SSM_ERR_ALIGN;
   if ((long long)((dim + 31) / 32) * batch > 0x7fffffffLL) return SSM_ERR_UNSUPPORTED;
+  // y is written while the inputs are still being read, so it must not overlap any of them; the
+  // checkpoints likewise must not overlap y, the state buffers or the inputs they are read with
+  const size_t ny = size_t(batch) * dim * seqlen * es, nbc = size_t(batch) * dstate * seqlen * es;
+  const size_t nst = size_t(batch) * dim * dstate * 4;
+  if (overlaps(y, ny, u, ny) || overlaps(y, ny, delta, ny) || overlaps(y, ny, z, ny) || overlaps(y, ny, B, nbc) ||
+      overlaps(y, ny, C, nbc))
+    return SSM_ERR_ARG;
+  if (ckpt) {
+    const size_t nck = size_t(batch) * ((seqlen + 31) / 32) * dim * dstate * 4;
+    if (overlaps(ckpt, nck, y, ny) || overlaps(ckpt, nck, last_state, nst) || overlaps(ckpt, nck, h0, nst) ||
+        overlaps(ckpt, nck, u, ny) || overlaps(ckpt, nck, delta, ny))
+      return SSM_ERR_ARG;
+  }
 
   ssm::ScanArgs a{};
   a.u = u, a.delta = delta, a.A = A, a.B = B, a.C = C, a.D = D, a.z = z, a.dt_bias = dt_bias, a.h0 = h0;
@@ -111,6 +131,23 @@ int ssm_scan_fwd_train(const void* u, const void* delta, const float* A, const v
                        int io_dtype, void* stream) {
   return ssm_scan_fwd_train_ex(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, checkpoints,
                                batch, dim, dstate, seqlen, io_dtype, SSM_DISC_DELTA_B, stream);
+}
+
+int ssm_scan_fwd_form(int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization, int aligned_rows,
+                      int* ctas) {
+  if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
+  if (dstate > 16) return SSM_ERR_UNSUPPORTED;
+  ssm::ScanArgs a{};
+  a.batch = batch, a.dim = dim, a.dstate = dstate, a.seqlen = seqlen;
+  a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  a.zoh = discretization == SSM_DISC_ZOH ? 1 : 0;
+  const bool vec = aligned_rows != 0 && (size_t(seqlen) * io_size(io_dtype)) % 16 == 0;
+  int form = 0, n = 0;
+  if (ssm::scan_fwd_form(a, vec, form, n) != cudaSuccess) return SSM_ERR_LAUNCH;
+  if (ctas) *ctas = n;
+  return form;
 }
 
 int ssm_scan_fwd_h0(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
@@ -261,8 +298,16 @@ int ssm_causal_conv1d_update(void* state, const void* x, const float* weight, co
   return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 
+int ssm_wait_timeouts(unsigned long long* count) {
+  if (!count) return SSM_ERR_NULL;
+  unsigned long long n = 0;
+  if (ssm::scan_wait_timeouts(n) != cudaSuccess) return SSM_ERR_LAUNCH;
+  *count = n;
+  return SSM_OK;
+}
+
 int ssm_probe_cycles(int kind, long long* cycles, int nblocks, void* stream) {
-  if (kind < SSM_PROBE_EX2 || kind > SSM_PROBE_FFMA2) return SSM_ERR_ARG;
+  if (kind < SSM_PROBE_EX2 || kind > SSM_PROBE_WAIT_TIMEOUT) return SSM_ERR_ARG;
   if (nblocks < 0) return SSM_ERR_SHAPE;
   if (nblocks == 0) return SSM_OK;
   if (!cycles) return SSM_ERR_NULL;
@@ -272,7 +317,7 @@ int ssm_probe_cycles(int kind, long long* cycles, int nblocks, void* stream) {
 }
 
 double ssm_probe_ops_per_cta(int kind) {
-  return (kind < SSM_PROBE_EX2 || kind > SSM_PROBE_FFMA2) ? 0.0 : ssm::probe_ops_per_cta(kind);
+  return (kind < SSM_PROBE_EX2 || kind > SSM_PROBE_WAIT_TIMEOUT) ? 0.0 : ssm::probe_ops_per_cta(kind);
 }
 
 }  // extern "C"

@@ -1,14 +1,17 @@
-// Device helpers for the scan kernels: MUFU approximations, softplus, silu, io conversions.
+// Device helpers for the scan kernels: MUFU approximations, softplus, silu, io conversions,
+// mbarriers with bounded waits.
 //
 // Accuracy (float32 arithmetic throughout):
-//  * ex2.approx.ftz.f32 / lg2.approx.ftz.f32 / rcp.approx.ftz.f32 are the PTX special-function
-//    approximations (a few ulp; subnormal results flush to zero).
-//  * softplus(x) = max(x, 0) + log1p(e), e = exp(-|x|) in (0, 1].  log1p(e) uses the alternating
-//    Taylor series e - e^2/2 + ... - e^6/6 when e < 1/16 (truncation below e^7/7 < 5e-10
-//    relative), and lg2(1 + e) * ln 2 otherwise (there 1 + e >= 17/16, so lg2's absolute error
-//    stays small next to the result).  This avoids the relative-precision loss of log(1 + e)
-//    for small e, which feeds Delta and therefore every state update.
-//  * silu(z) = z / (1 + 2^(-z log2 e)).
+//  * ex2.approx.ftz.f32 / lg2.approx.ftz.f32 / rcp.approx.ftz.f32 / tanh.approx.f32 are the PTX
+//    special-function approximations (a few ulp for ex2, lg2, rcp; about 2^-11 relative for tanh;
+//    subnormal results flush to zero).
+//  * softplus_f32 (decode step, backward): max(x, 0) + log1p(e), e = exp(-|x|) in (0, 1]; log1p(e)
+//    is the alternating Taylor series e - e^2/2 + ... - e^6/6 when e < 1/16 (truncation below
+//    e^7/7 < 5e-10 relative) and lg2(1 + e) * ln 2 otherwise (1 + e >= 17/16 there, so lg2's
+//    absolute error stays small next to the result).
+//  * softplus2 (forward scan): the same max(x, 0) + log1p(e) with log1p(e) = e P(e), P a degree-7
+//    polynomial (below): one MUFU op per value and no branch.
+//  * silu(z) = z / (1 + 2^(-z log2 e)), or h + h tanh(h) with h = z / 2 where the output is bf16.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -52,6 +55,87 @@ __device__ __forceinline__ float softplus_f32(float x) {
 }
 
 __device__ __forceinline__ float silu_f32(float z) { return z * rcp_approx(1.0f + ex2_approx(-z * kLog2e)); }
+
+__device__ __forceinline__ float tanh_approx(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// softplus of two values: max(x, 0) + log1p(e), e = exp(-|x|) in (0, 1], with log1p(e) = e P(e)
+// and P a degree-7 polynomial for log1p(e) / e on [0, 1] (Chebyshev interpolation of that function,
+// coefficients rounded to float32; relative error of e P(e) below 3.3e-7 evaluated in float32, so
+// softplus stays within 6e-7 relative over |x| <= 10).  One MUFU op per value, no branch, and no
+// loss of relative precision for small e.
+__device__ __forceinline__ float2 softplus2(float2 x) {
+  const float2 e = make_float2(ex2_approx(-fabsf(x.x) * kLog2e), ex2_approx(-fabsf(x.y) * kLog2e));
+  auto c = [](float v) { return make_float2(v, v); };
+  float2 p = __ffma2_rn(e, c(-0.00837115291506052f), c(0.04349390044808388f));
+  p = __ffma2_rn(e, p, c(-0.1068500280380249f));
+  p = __ffma2_rn(e, p, c(0.1768747717142105f));
+  p = __ffma2_rn(e, p, c(-0.24474774301052094f));
+  p = __ffma2_rn(e, p, c(0.3327192962169647f));
+  p = __ffma2_rn(e, p, c(-0.49997174739837646f));
+  p = __ffma2_rn(e, p, c(0.9999997615814209f));
+  return __ffma2_rn(p, e, make_float2(fmaxf(x.x, 0.0f), fmaxf(x.y, 0.0f)));
+}
+
+// silu of two values, z sigmoid(z).  BF16 selects h + h tanh(h), h = z / 2: one MUFU op, whose
+// relative error (about 2^-11) stays far below bf16 output rounding.  Otherwise z / (1 + 2^(-z
+// log2 e)) with ex2 and rcp (a few ulp), for float outputs.
+template <bool BF16>
+__device__ __forceinline__ float2 silu2(float2 z) {
+  if constexpr (BF16) {
+    const float2 h = __fmul2_rn(z, make_float2(0.5f, 0.5f));
+    return __ffma2_rn(h, make_float2(tanh_approx(h.x), tanh_approx(h.y)), h);
+  } else {
+    return make_float2(silu_f32(z.x), silu_f32(z.y));
+  }
+}
+
+// ---- mbarriers with bounded waits ----
+// A CTA-scope shared-memory mbarrier.  Arrivals release the arriving thread's prior shared-memory
+// accesses; a completed wait acquires them.
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t done;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(done)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return done != 0;
+}
+// Wait until `bar` completes the phase of the given parity.  The wait is bounded: it gives up after
+// `limit` clock cycles, or at once when *abort (a CTA-wide flag in shared memory) is set; giving up
+// sets *abort, adds one to *timeouts for the wait that ran out, and returns false, so that a broken
+// hand-off ends the kernel (with garbage outputs and a counted timeout) instead of hanging it.
+// Between tests the warp sleeps for `backoff_ns` nanoseconds, so that a waiting warp takes almost
+// no issue slots from the warps doing the work.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit,
+                                          unsigned long long* timeouts, unsigned backoff_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(backoff_ns);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    if (clock64() - t0 > limit) {
+      *abort = 1;
+      atomicAdd(timeouts, 1ull);
+      return false;
+    }
+  }
+}
 
 // Exact zero-order hold: Bbar = (exp(Delta a) - 1) / a * B for a diagonal A.  This returns the
 // factor Bbar / B from x = Delta*a, abar = exp(x) (already computed by the caller), Delta and

@@ -126,16 +126,20 @@ struct ConvUpdateArgs {
   FastDiv div_dim;  // filled at launch
 };
 
-// Enqueue the scan on `stream`.  Arguments are already validated.  Runs the four-lanes-per-channel
-// form; SSM_SCAN_VARIANT=lane in the environment selects the lane-per-channel form instead (not for
-// the zero-order hold or the training forward, which always run the four-lanes form).
+// Enqueue the scan on `stream`.  Arguments are already validated.
 cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream);
 
-// The four-lanes-per-channel form (scan_fwd.cu).
+// The four-lanes-per-channel scan (scan_fwd.cu): balanced layout where its plan applies (bf16,
+// dstate 9..16; SSM_SCAN_VARIANT=quad_plain in the environment forces the 32-channel CTAs).
 cudaError_t launch_scan_fwd_quad(const ScanArgs& a, bool vec, cudaStream_t stream);
 
-// The lane-per-channel form (scan_fwd_lane.cu).
-cudaError_t launch_scan_fwd_lane(const ScanArgs& a, bool vec, cudaStream_t stream);
+// The form launch_scan_fwd runs for `a` (vec: rows take the 16-byte copy path) and its grid size.
+enum ScanForm { kFormPlain = 0, kFormBalanced = 1 };
+cudaError_t scan_fwd_form(const ScanArgs& a, bool vec, int& form, int& ctas);
+
+// Hand-off waits of the forward kernels that gave up since the library was loaded (synchronises
+// the device first).
+cudaError_t scan_wait_timeouts(unsigned long long& count);
 
 // Enqueue one decode step on `stream`.  Arguments are already validated.
 cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);
@@ -144,7 +148,9 @@ cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);
 // gradients, then one launch.  Arguments are already validated.
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);
 
-// Unit-throughput probes (probe.cu): kind 0 = ex2.approx, 1 = FP32 FMA, 2 = packed f32x2 FMA.
+// Unit-throughput probes (probe.cu): kind 0 = ex2.approx, 1 = FP32 FMA, 2 = packed f32x2 FMA,
+// 3 = ex2 + packed f32x2 FMA interleaved, 4 = the recurrence's per-state-pair mix, 5 = a bounded
+// mbarrier wait that nothing completes (it must give up).
 cudaError_t launch_probe(int kind, int nblocks, long long* cycles, cudaStream_t stream);
 double probe_ops_per_cta(int kind);
 

@@ -18,10 +18,19 @@
 //    quarter-warp share one n-group, so their B/C loads hit one address).  The float32 state lives
 //    in registers for the whole sequence.  Per 16-step window the recurrence runs on float2 pairs
 //    (mul/fma.f32x2) keeping the readout partials C.h in registers; the sum over the R lanes of a
-//    channel goes through a rotated, conflict-free shared-memory layout; lane (g, c) then finishes
-//    16/R consecutive steps of channel c, (y + D u) * silu(z), stored straight to HBM.
-//  * Hand-off is by named barriers (bar.arrive / bar.sync; no spin loops): table stage s is FULL
-//    once the prep warps arrive on it and EMPTY once the recurrence warps are done with it.
+//    channel is a reduce-scatter of warp shuffles (no shared-memory traffic: the kernel is bound by
+//    the shared-memory data path, which its B, C and step-table loads already fill); lane (g, c)
+//    then finishes 16/R consecutive steps of channel c, (y + D u) * silu(z), stored straight to HBM.
+//  * Hand-off is by mbarriers in shared memory: table stage s is FULL once every prep thread has
+//    arrived on it, EMPTY once every lane of the group's recurrence warps has.  Each recurrence
+//    warp waits for FULL on its own, so the warps of a group are not re-aligned at every chunk
+//    (aligned warps reach their window-end readouts together and leave the schedulers idle).  The
+//    prep, which runs ahead and waits at almost every chunk, waits for EMPTY in one warp while the
+//    other prep warps block on their own named barrier, and the waiting warp sleeps between tests,
+//    so waiting costs the recurrence warps almost no issue slots.  Every wait is bounded (about a
+//    second): one that gives up sets a CTA-wide abort flag that ends every other wait at once and
+//    is counted in g_scan_wait_timeouts (ssm_wait_timeouts), so the kernel always ends.  The only
+//    named barriers left are among the prep threads, which all run the same control flow.
 //  * For dstate 9..16 (four recurrence warps, one warpgroup each) setmaxnreg moves registers from
 //    the prep warpgroup (48) to the recurrence warpgroup (112), whose unrolled window is the long
 //    pole; the kernel is launched at 80 registers per thread and the shares add up to that.
@@ -56,8 +65,21 @@ constexpr int kLaunchRegs = 80, kPrepRegs = 48, kRecRegs = 112;
 static_assert(4 * kPrepRegs + 4 * kRecRegs == 8 * kLaunchRegs && kPrepWarps == 4,
               "setmaxnreg shares (one warpgroup each) must add up to the launch total");
 
-// named barrier ids (0 is __syncthreads)
-constexpr int kBarFull0 = 1, kBarEmpty0 = 3, kBarPrep = 5;
+// named barrier ids within a group's block of five (0 is __syncthreads): the one-time sync after
+// the mbarriers are initialised, and the prep threads' own syncs
+constexpr int kBarInit = 1, kBarPrep = 5;
+// sleep between two tests of a hand-off barrier: the prep (ahead, waiting long) and the recurrence
+// warps (rarely waiting, and then only briefly), in nanoseconds
+constexpr unsigned kPrepBackoff = 256, kRecBackoff = 32;
+// longest a hand-off wait may take before the kernel gives up on it, in SM clock cycles (~1 s)
+constexpr long long kWaitLimit = 1LL << 31;
+
+}  // namespace
+
+// Hand-off waits of the forward kernels that gave up, since the library was loaded.
+__device__ unsigned long long g_scan_wait_timeouts;
+
+namespace {
 
 template <typename T, int NPAD>
 struct ScanCfg {
@@ -74,7 +96,6 @@ struct ScanCfg {
   static constexpr int PSS = CPB + 4;                 // row stride (float2) of the (Delta, Delta*u) table
   static constexpr int DSS = kChunk + 2;              // row stride (float2) of the (D*u, silu z) table
   static constexpr int OPL = kWin / R;                // outputs each lane finishes per window
-  static constexpr int UPB = kWin / 4;                // 16-byte units per lane block of readout partials
   // shared memory map (bytes)
   static constexpr size_t kRawStage = size_t(ROWS) * RS * sizeof(T);
   static constexpr int kCOfs = kChunk * NPAD + 16;    // float offset of the C table after the B table
@@ -84,8 +105,8 @@ struct ScanCfg {
   static constexpr size_t kTabStage = kBCStage + kPStage + kDSStage;
   static constexpr size_t kRaw = 2 * kRawStage;
   static constexpr size_t kTab = 2 * kTabStage;
-  static constexpr size_t kRed = R > 1 ? size_t(32 * CWARPS) * UPB * 16 : 0;    // red [lanes][UPB] float4
-  static constexpr size_t kSmem = kRaw + kTab + kRed;
+  static constexpr size_t kBarOfs = kRaw + kTab;                 // FULL0, FULL1, EMPTY0, EMPTY1 mbarriers
+  static constexpr size_t kSmem = kBarOfs + 4 * sizeof(uint64_t);
   static_assert(kRawStage % 16 == 0 && kBCStage % 16 == 0 && kPStage % 16 == 0 && kDSStage % 16 == 0, "align");
   static_assert(OPL % 4 == 0 && kChunk % kWin == 0, "each lane finishes whole 16-byte units of the window");
   static_assert((RS * sizeof(T)) % 16 == 0 && kChunk % 8 == 0, "staged rows hold whole 16-byte vectors");
@@ -96,26 +117,6 @@ __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
 __device__ __forceinline__ void bar_arrive(int id, int n) {
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
-// Position of 16-byte unit i (readout partials of steps 4i .. 4i+3) in the block of lane
-// (g, cw) = lane g*CPW + cw.  The rotation by cw/2 makes both access patterns conflict-free for
-// R = 4: a quarter-warp (fixed g) storing unit i, and a quarter-warp loading unit g of the
-// blocks of partner gp.
-__device__ __forceinline__ int red_rot(int cw, int i) { return (i + (cw >> 1)) & (kWin / 4 - 1); }
-
-// softplus of two values with packed arithmetic where it exists (see device_math.cuh for the method)
-__device__ __forceinline__ float2 softplus2(float2 x) {
-  const float2 e = f2(ex2_approx(-fabsf(x.x) * kLog2e), ex2_approx(-fabsf(x.y) * kLog2e));
-  // e * (1 - e/2 + e^2/3 - e^3/4 + e^4/5 - e^5/6) in Horner form
-  float2 s = __ffma2_rn(e, f2(-1.0f / 6.0f, -1.0f / 6.0f), f2(1.0f / 5.0f, 1.0f / 5.0f));
-  s = __ffma2_rn(e, s, f2(-1.0f / 4.0f, -1.0f / 4.0f));
-  s = __ffma2_rn(e, s, f2(1.0f / 3.0f, 1.0f / 3.0f));
-  s = __ffma2_rn(e, s, f2(-1.0f / 2.0f, -1.0f / 2.0f));
-  s = __ffma2_rn(e, s, f2(1.0f, 1.0f));
-  s = __fmul2_rn(s, e);
-  const float2 l = __fmul2_rn(f2(lg2_approx(1.0f + e.x), lg2_approx(1.0f + e.y)), f2(kLn2, kLn2));
-  return f2(fmaxf(x.x, 0.0f) + (e.x < 0.0625f ? s.x : l.x), fmaxf(x.y, 0.0f) + (e.y < 0.0625f ? s.y : l.y));
 }
 
 template <typename T>
@@ -181,19 +182,19 @@ __device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) 
 }
 
 // One group of warps (4 prep + R recurrence) scanning the channels [d0, dlim) of batch row b, at
-// most CPB of them, with its own shared-memory block `smem` and the named barriers bar0 + 1 ..
-// bar0 + 5; tid is the thread's index within the group.  A CTA of the plain kernel is one group.
+// most CPB of them, with its own shared-memory block `smem` (mbarriers included) and the named
+// barriers bar0 + 1 .. bar0 + 5; tid is the thread's index within the group, abort the CTA's
+// give-up flag.  A CTA of the plain kernel is one group.
 template <typename T, int NPAD, bool VEC, bool ZOH>
 __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* smem, const int tid, const int b,
-                                           const int d0, const int dlim, const int bar0) {
+                                           const int d0, const int dlim, const int bar0, volatile int* abort) {
   using Cfg = ScanCfg<T, NPAD>;
   constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, RS = Cfg::RS, VPR = Cfg::VPR;
   constexpr int NT = Cfg::NT, PT = Cfg::PT, ROWS = Cfg::ROWS, PSS = Cfg::PSS, DSS = Cfg::DSS, OPL = Cfg::OPL;
-  constexpr int UPB = Cfg::UPB, CWARPS = Cfg::CWARPS;
+  constexpr int CWARPS = Cfg::CWARPS;
 
   T* raw = reinterpret_cast<T*>(smem);
   unsigned char* tab = smem + Cfg::kRaw;
-  float4* red = reinterpret_cast<float4*>(smem + Cfg::kRaw + Cfg::kTab);
   auto tabBs = [&](int s) { return reinterpret_cast<float*>(tab + s * Cfg::kTabStage); };
   auto tabCs = [&](int s) { return reinterpret_cast<float*>(tab + s * Cfg::kTabStage) + Cfg::kCOfs; };
   auto tabPs = [&](int s) { return reinterpret_cast<float2*>(tab + s * Cfg::kTabStage + Cfg::kBCStage); };
@@ -201,11 +202,21 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
     return reinterpret_cast<float2*>(tab + s * Cfg::kTabStage + Cfg::kBCStage + Cfg::kPStage);
   };
 
-  const int bFull0 = kBarFull0 + bar0, bEmpty0 = kBarEmpty0 + bar0, bPrep = kBarPrep + bar0;
+  const int bPrep = kBarPrep + bar0;
   const int warp = tid >> 5, lane = tid & 31;
   const int L = a.seqlen, N = a.dstate;
   const bool has_z = a.z != nullptr;
   const int nchunks = (L + kChunk - 1) / kChunk;
+
+  // mbarriers: FULL[s] completes when all PT prep threads have written table stage s, EMPTY[s]
+  // when every lane of the recurrence warps holding a channel of the group is done reading it
+  uint64_t* mb = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOfs);
+  const int rec_warps = min(CWARPS, (dlim - d0 + CPW - 1) / CPW);
+  if (tid == 0) {
+    mbar_init(&mb[0], PT), mbar_init(&mb[1], PT);
+    mbar_init(&mb[2], 32 * rec_warps), mbar_init(&mb[3], 32 * rec_warps);
+  }
+  bar_sync(kBarInit + bar0, NT);  // the group's mbarriers are initialised before anyone uses them
 
   if (warp >= CWARPS) {
     // ================================ prep warps ================================
@@ -320,8 +331,11 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
       const int s = k & 1;
       const int t0 = k * kChunk;
       cp_async_wait<1>();           // this thread's copies of chunk k have landed
-      bar_sync(bPrep, PT);          // ... and every prep thread's
-      if (k >= 2) bar_sync(bEmpty0 + s, NT);  // the recurrence warps are done with table stage s
+      // the recurrence warps are done with table stage s (their reads of chunk k - 2): one prep warp
+      // waits, the others learn it from the named barrier below
+      if (k >= 2 && pw == 0)
+        mbar_wait(&mb[2 + s], ((k - 2) >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
+      bar_sync(bPrep, PT);          // every prep thread's copies have landed, and stage s is free
 
       const T* st = raw + size_t(s) * ROWS * RS;
       float* BCs = tabBs(s);
@@ -360,7 +374,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
           // Bbar factor needs Delta and A together and is formed in the recurrence)
           const float2 du = ZOH ? uu : __fmul2_rn(dl, uu);
           const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
-          const float2 sg = has_z ? f2(silu_f32(zz.x), silu_f32(zz.y)) : f2(1.0f, 1.0f);
+          const float2 sg = has_z ? silu2<std::is_same<T, __nv_bfloat16>::value>(zz) : f2(1.0f, 1.0f);
           Ps[ps_ofs + o * PSS] = f2(dl.x, du.x);
           Ps[ps_ofs + (o + 1) * PSS] = f2(dl.y, du.y);
           *reinterpret_cast<float4*>(DS + ds_ofs + o) = make_float4(Du.x, sg.x, Du.y, sg.y);
@@ -372,13 +386,11 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
         items(std::true_type{});
 
       bar_sync(bPrep, PT);               // every prep thread is done reading raw stage s
-      bar_arrive(bFull0 + s, NT);        // table stage s is ready
+      mbar_arrive(&mb[s]);               // this thread's part of table stage s is written
       if (k + 2 < nchunks) stage_load(s, t0 + 2 * kChunk);
       cp_async_commit();
     }
     cp_async_wait<0>();
-    // match the recurrence warps' last arrivals so that no barrier is left half-arrived
-    for (int k = max(0, nchunks - 2); k < nchunks; ++k) bar_sync(bEmpty0 + (k & 1), NT);
     return;
   }
 
@@ -390,14 +402,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
   const int cl = warp * CPW + cw;  // this lane's channel within the CTA
   const int d = d0 + cl;
   const bool ch_ok = d < dlim;
-  if (d0 + warp * CPW >= dlim) {
-    // none of this warp's channels is in the group: keep the table hand-off, skip the work
-    for (int k = 0; k < nchunks; ++k) {
-      bar_sync(bFull0 + (k & 1), NT);
-      bar_arrive(bEmpty0 + (k & 1), NT);
-    }
-    return;
-  }
+  if (warp >= rec_warps) return;  // none of this warp's channels is in the group (not counted in EMPTY)
 
   float2 A01, A23, h01, h23, iA01, iA23;
   {
@@ -428,7 +433,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
       for (int i = 0; i < 4; ++i)
         if (4 * g + i < N) cp[4 * g + i] = hv[i];
     }
-    bar_sync(bFull0 + s, NT);
+    mbar_wait(&mb[s], (k >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kRecBackoff);
     const float* Bs = tabBs(s);
     const float* Cs = tabCs(s);
     const float2* Ps = tabPs(s);
@@ -460,37 +465,44 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
         }
         acc[j] = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
       }
-      // sums over the R lanes of the channel and the pair halves; lane (g, cw) finishes the OPL
-      // steps w + g*OPL ... of channel cl
+      // sums over the R lanes of the channel (lanes cw, cw + CPW, ...) and the pair halves, by a
+      // reduce-scatter of warp shuffles (which take no shared-memory bandwidth, the kernel's
+      // tightest resource): in each round the lanes whose state-group bit is set keep the later
+      // half of their steps and send the earlier half, the others the reverse.  Lane (g, cw) ends
+      // with OPL consecutive steps of channel cl, starting at window step tb - w.
+      float pv[kWin];
+#pragma unroll
+      for (int j = 0; j < kWin; ++j) pv[j] = acc[j].x + acc[j].y;
       float yv[OPL];
+      int tb = w;  // first step (within the chunk) this lane finishes
       if constexpr (R == 1) {
 #pragma unroll
-        for (int j = 0; j < kWin; ++j) yv[j] = acc[j].x + acc[j].y;
+        for (int j = 0; j < kWin; ++j) yv[j] = pv[j];
       } else {
-        float4* rb = red + size_t(warp) * 32 * UPB;
+        const bool b0 = g & 1;
+        float k8[kWin / 2];
 #pragma unroll
-        for (int i = 0; i < UPB; ++i)
-          rb[lane * UPB + red_rot(cw, i)] = make_float4(acc[4 * i].x + acc[4 * i].y, acc[4 * i + 1].x + acc[4 * i + 1].y,
-                                                        acc[4 * i + 2].x + acc[4 * i + 2].y,
-                                                        acc[4 * i + 3].x + acc[4 * i + 3].y);
-        __syncwarp();
-#pragma unroll
-        for (int u = 0; u < OPL / 4; ++u) {
-          const int i = g * (OPL / 4) + u;
-          float4 sm = rb[cw * UPB + red_rot(cw, i)];
-#pragma unroll
-          for (int gp = 1; gp < R; ++gp) {
-            const float4 o = rb[(gp * CPW + cw) * UPB + red_rot(cw, i)];
-            const float2 lo = __fadd2_rn(f2(sm.x, sm.y), f2(o.x, o.y));
-            const float2 hi = __fadd2_rn(f2(sm.z, sm.w), f2(o.z, o.w));
-            sm = make_float4(lo.x, lo.y, hi.x, hi.y);
-          }
-          yv[4 * u] = sm.x, yv[4 * u + 1] = sm.y, yv[4 * u + 2] = sm.z, yv[4 * u + 3] = sm.w;
+        for (int i = 0; i < kWin / 2; ++i) {
+          const float snd = b0 ? pv[i] : pv[i + kWin / 2];
+          const float kp = b0 ? pv[i + kWin / 2] : pv[i];
+          k8[i] = kp + __shfl_xor_sync(0xffffffffu, snd, CPW);
         }
-        __syncwarp();
+        tb += b0 ? kWin / 2 : 0;
+        if constexpr (R == 2) {
+#pragma unroll
+          for (int i = 0; i < OPL; ++i) yv[i] = k8[i];
+        } else {
+          const bool b1 = (g >> 1) & 1;
+#pragma unroll
+          for (int i = 0; i < OPL; ++i) {
+            const float snd = b1 ? k8[i] : k8[i + OPL];
+            const float kp = b1 ? k8[i + OPL] : k8[i];
+            yv[i] = kp + __shfl_xor_sync(0xffffffffu, snd, 2 * CPW);
+          }
+          tb += b1 ? OPL : 0;
+        }
       }
       // epilogue: (y + D u) * silu(z) -> io type, straight to HBM
-      const int tb = w + g * OPL;  // first step (within the chunk) this lane finishes
       float ov[OPL];
 #pragma unroll
       for (int j = 0; j < OPL; j += 2) {
@@ -501,7 +513,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
       const int tg = t0 + tb;  // first global step
       if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, L - tg);
     }
-    bar_arrive(bEmpty0 + s, NT);  // table stage s may be refilled
+    mbar_arrive(&mb[2 + s]);  // this lane is done reading table stage s
   }
 
   if (a.last_state && ch_ok) {
@@ -523,7 +535,10 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   const int nblk_d = (a.dim + CPB - 1) / CPB;
   const int b = blockIdx.x / nblk_d;
   const int d0 = (blockIdx.x % nblk_d) * CPB;
-  scan_group<T, NPAD, VEC, ZOH>(a, smem, threadIdx.x, b, d0, a.dim, 0);
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
+  scan_group<T, NPAD, VEC, ZOH>(a, smem, threadIdx.x, b, d0, a.dim, 0, &abort_flag);
 }
 
 // The balanced form: one CTA per SM holding kFusedGroups groups, each on a channel range (8 to 32
@@ -542,13 +557,16 @@ __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
     scan_fwd_fused_kernel(const ScanArgs a, const FusedPlan plan) {
   extern __shared__ __align__(16) unsigned char smem[];
   using Cfg = ScanCfg<T, NPAD>;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) abort_flag = 0;
+  __syncthreads();
   const int grp = threadIdx.x / Cfg::NT;
   const uint32_t e = plan.e[blockIdx.x * kFusedGroups + grp];
   const int nch = int(e & 15u) * 8;
   if (nch == 0) return;  // an empty group: its warps leave, the other groups do not wait on them
   const int b = int(e >> 16), d0 = int((e >> 4) & 0xfffu) * 8;
   scan_group<T, NPAD, VEC, ZOH>(a, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0,
-                                min(a.dim, d0 + nch), 5 * grp);
+                                min(a.dim, d0 + nch), 5 * grp, &abort_flag);
 }
 
 // Host plan for the balanced form: units of 8 channels, groups of at most 4 units inside one batch
@@ -582,43 +600,60 @@ int make_fused_plan(const ScanArgs& a, int sms, FusedPlan& plan) {
   return (left == 0 && worst < plain_max) ? ctas : 0;
 }
 
-// Launches the balanced form when its plan applies (bf16, dstate 9..16: three groups' shared
-// memory fit one CTA); returns false when the plain kernel should run instead.
+// Once per device: the balanced kernel's shared-memory opt-in, and whether the build has the
+// register count its setmaxnreg split was sized for (if not, the plain kernel runs).  Returns
+// whether the balanced kernel may launch; err reports a failing CUDA call.
+template <typename T, int NPAD, bool VEC, bool ZOH>
+bool fused_ready(int dev, cudaError_t& err) {
+  using Cfg = ScanCfg<T, NPAD>;
+  auto kernel = scan_fwd_fused_kernel<T, NPAD, VEC, ZOH>;
+  constexpr size_t kSmem = kFusedGroups * Cfg::kSmem;
+  static std::atomic<uint64_t> configured{0}, usable{0};
+  const uint64_t bit = uint64_t(1) << (dev & 63);
+  if (!(configured.load(std::memory_order_acquire) & bit)) {
+    if ((err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem))) != cudaSuccess)
+      return false;
+    cudaFuncAttributes fa{};
+    if ((err = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return false;
+    if (fa.numRegs == kLaunchRegs) usable.fetch_or(bit, std::memory_order_acq_rel);
+    configured.fetch_or(bit, std::memory_order_acq_rel);
+  }
+  return (usable.load(std::memory_order_acquire) & bit) != 0;
+}
+
+// CTAs of the balanced form for `a` (bf16, dstate 9..16: three groups' shared memory fit one CTA),
+// or 0 when the plain kernel runs instead (no plan, SSM_SCAN_VARIANT=quad_plain, or a build
+// whose register count does not match the split).
+template <typename T, int NPAD, bool VEC, bool ZOH>
+int fused_ctas(const ScanArgs& a, FusedPlan& plan, int& dev, cudaError_t& err) {
+  if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
+    return 0;
+  } else {
+    const char* force = std::getenv("SSM_SCAN_VARIANT");
+    if (force && std::strcmp(force, "quad_plain") == 0) return 0;
+    int sms = 0;
+    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
+    const int ctas = make_fused_plan(a, sms, plan);
+    if (ctas == 0) return 0;
+    return fused_ready<T, NPAD, VEC, ZOH>(dev, err) ? ctas : 0;
+  }
+}
+
+// Launches the balanced form when its plan applies; returns false when the plain kernel should run.
 template <typename T, int NPAD, bool VEC, bool ZOH>
 bool launch_fused(const ScanArgs& a, cudaStream_t stream, cudaError_t& err) {
   using Cfg = ScanCfg<T, NPAD>;
-  if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
-    return false;
-  } else {
-    const char* force = std::getenv("SSM_SCAN_VARIANT");
-    if (force && std::strcmp(force, "quad") == 0) return false;
-    int dev = 0, sms = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return true;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return true;
-    FusedPlan plan;
-    const int ctas = make_fused_plan(a, sms, plan);
-    if (ctas == 0) return false;
-    auto kernel = scan_fwd_fused_kernel<T, NPAD, VEC, ZOH>;
-    constexpr size_t kSmem = kFusedGroups * Cfg::kSmem;
-    // once per device: the shared-memory opt-in, and whether the build has the register count the
-    // setmaxnreg split was sized for (if not, the plain kernel runs)
-    static std::atomic<uint64_t> configured{0}, usable{0};
-    const uint64_t bit = uint64_t(1) << (dev & 63);
-    if (!(configured.load(std::memory_order_acquire) & bit)) {
-      if ((err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmem))) != cudaSuccess)
-        return true;
-      cudaFuncAttributes fa{};
-      if ((err = cudaFuncGetAttributes(&fa, kernel)) != cudaSuccess) return true;
-      if (fa.numRegs == kLaunchRegs) usable.fetch_or(bit, std::memory_order_acq_rel);
-      configured.fetch_or(bit, std::memory_order_acq_rel);
-    }
-    if (!(usable.load(std::memory_order_acquire) & bit)) return false;
-    ScanArgs args = a;
-    void* params[] = {&args, &plan};
-    err = cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(unsigned(ctas)), dim3(kFusedGroups * Cfg::NT),
-                           params, kSmem, stream);
-    return true;
-  }
+  FusedPlan plan;
+  int dev = 0;
+  const int ctas = fused_ctas<T, NPAD, VEC, ZOH>(a, plan, dev, err);
+  if (err != cudaSuccess) return true;
+  if (ctas == 0) return false;
+  ScanArgs args = a;
+  void* params[] = {&args, &plan};
+  err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_fwd_fused_kernel<T, NPAD, VEC, ZOH>), dim3(unsigned(ctas)),
+                         dim3(kFusedGroups * Cfg::NT), params, kFusedGroups * Cfg::kSmem, stream);
+  return true;
 }
 
 template <typename T, int NPAD, bool VEC, bool ZOH>
@@ -685,16 +720,31 @@ cudaError_t launch_scan_fwd_quad(const ScanArgs& a, bool vec, cudaStream_t strea
   return vec ? dispatch_disc<__nv_bfloat16, true>(a, stream) : dispatch_disc<__nv_bfloat16, false>(a, stream);
 }
 
+cudaError_t scan_fwd_form(const ScanArgs& a, bool vec, int& form, int& ctas) {
+  cudaError_t err = cudaSuccess;
+  int c = 0, dev = 0;
+  if (a.io == kBF16 && a.dstate > 8) {
+    FusedPlan plan;
+    c = vec ? (a.zoh ? fused_ctas<__nv_bfloat16, 16, true, true>(a, plan, dev, err)
+                     : fused_ctas<__nv_bfloat16, 16, true, false>(a, plan, dev, err))
+            : (a.zoh ? fused_ctas<__nv_bfloat16, 16, false, true>(a, plan, dev, err)
+                     : fused_ctas<__nv_bfloat16, 16, false, false>(a, plan, dev, err));
+    if (err != cudaSuccess) return err;
+  }
+  form = c > 0 ? kFormBalanced : kFormPlain;
+  ctas = c > 0 ? c : int(std::min<long long>(0x7fffffffLL, (long long)((a.dim + 31) / 32) * a.batch));
+  return cudaSuccess;
+}
+
+cudaError_t scan_wait_timeouts(unsigned long long& count) {
+  cudaError_t err = cudaDeviceSynchronize();
+  if (err != cudaSuccess) return err;
+  return cudaMemcpyFromSymbol(&count, g_scan_wait_timeouts, sizeof(count));
+}
+
 cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream) {
   const bool vec = a.io == kF32 ? rows_vectorisable<float>(a) : rows_vectorisable<__nv_bfloat16>(a);
-  // The four-lanes-per-channel form is the default at every size: measured on B300 it is 1.45x
-  // faster than the lane-per-channel form even with 27-69 channel warps per SM (batch x dim of
-  // 82k-131k channels).  The lane form runs only when SSM_SCAN_VARIANT=lane asks for it.  Within
-  // the four-lanes form the balanced layout runs wherever its plan applies, the plain 32-channel
-  // CTAs elsewhere or when SSM_SCAN_VARIANT=quad asks for them.
-  const char* force = std::getenv("SSM_SCAN_VARIANT");
-  const bool lane = force && std::strcmp(force, "lane") == 0;
-  return (lane && !a.zoh && !a.ckpt) ? launch_scan_fwd_lane(a, vec, stream) : launch_scan_fwd_quad(a, vec, stream);
+  return launch_scan_fwd_quad(a, vec, stream);
 }
 
 }  // namespace ssm

@@ -33,7 +33,7 @@ def test_header_declares_the_boundary():
         ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_scan_fwd_ex", "ssm_state_update",
          "ssm_state_update_ex", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update",
          "ssm_scan_num_checkpoints", "ssm_scan_fwd_train", "ssm_scan_fwd_train_ex", "ssm_scan_bwd",
-         "ssm_scan_bwd_ex", "ssm_probe_cycles", "ssm_probe_ops_per_cta"])
+         "ssm_scan_bwd_ex", "ssm_probe_cycles", "ssm_probe_ops_per_cta", "ssm_scan_fwd_form", "ssm_wait_timeouts"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.ssm_abi_version() == 3
+    assert lib.ssm_abi_version() == 5
     for code in range(-8, 1):
         s = lib.ssm_status_string(code).decode()
         assert s and s != "unknown status"
@@ -249,14 +249,16 @@ def test_bwd_ex_rejects_unknown_discretization(lib, disc):
 
 
 def test_probe_validation(lib):
-    assert lib.ssm_probe_cycles(3, P, 4, None) == _native.SSM_ERR_ARG
+    assert lib.ssm_probe_cycles(6, P, 4, None) == _native.SSM_ERR_ARG
     assert lib.ssm_probe_cycles(-1, P, 4, None) == _native.SSM_ERR_ARG
     assert lib.ssm_probe_cycles(0, None, 4, None) == _native.SSM_ERR_NULL
     assert lib.ssm_probe_cycles(1, P + 4, 4, None) == _native.SSM_ERR_ALIGN
     assert lib.ssm_probe_cycles(2, None, 0, None) == _native.SSM_OK
     assert lib.ssm_probe_cycles(0, P, -1, None) == _native.SSM_ERR_SHAPE
-    ops = [lib.ssm_probe_ops_per_cta(k) for k in (0, 1, 2)]
-    assert ops[0] == ops[1] > 0 and ops[2] == 2 * ops[1]
+    assert lib.ssm_probe_ops_per_cta(5) == 0.0  # the bounded-wait probe counts no operations
+    ops = [lib.ssm_probe_ops_per_cta(k) for k in (0, 1, 2, 3, 4)]
+    # lane-operations (f32x2 counts twice), ex2 operations of the mix, state-steps (two per pair)
+    assert ops[0] == ops[1] == ops[3] > 0 and ops[2] == 2 * ops[1] and ops[4] == 2 * ops[1]
     assert lib.ssm_probe_ops_per_cta(7) == 0.0
 
 
@@ -269,3 +271,35 @@ def test_grid_overflow_is_refused_before_any_launch(lib):
     assert lib.ssm_scan_bwd(*bwd_args(batch=big, dim=64)) == _native.SSM_ERR_UNSUPPORTED
     assert lib.ssm_scan_bwd_ex(*bwd_args(batch=big, dim=64)[:-1], _native.SSM_DISC_ZOH, None) == \
         _native.SSM_ERR_UNSUPPORTED
+
+
+def test_form_query_validation(lib):
+    """The form query rejects bad sizes on the host; without a device it reports SSM_ERR_LAUNCH."""
+    n = ctypes.c_int(-1)
+    assert lib.ssm_scan_fwd_form(-1, 4, 16, 8, 1, 0, 1, ctypes.byref(n)) == _native.SSM_ERR_SHAPE
+    assert lib.ssm_scan_fwd_form(1, 4, 0, 8, 1, 0, 1, ctypes.byref(n)) == _native.SSM_ERR_SHAPE
+    assert lib.ssm_scan_fwd_form(1, 4, 17, 8, 1, 0, 1, ctypes.byref(n)) == _native.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_scan_fwd_form(1, 4, 16, 8, 7, 0, 1, ctypes.byref(n)) == _native.SSM_ERR_DTYPE
+    assert lib.ssm_scan_fwd_form(1, 4, 16, 8, 1, 5, 1, ctypes.byref(n)) == _native.SSM_ERR_ARG
+    st = lib.ssm_scan_fwd_form(1, 4, 16, 8, 1, 0, 1, ctypes.byref(n))
+    assert st in (_native.SSM_ERR_LAUNCH, 0, 1)
+
+
+def test_wait_timeouts_validation(lib):
+    assert lib.ssm_wait_timeouts(None) == _native.SSM_ERR_NULL
+
+
+def test_scan_output_may_not_overlap_an_input(lib):
+    """y overlapping u, delta, z, B or C is refused on the host; disjoint buffers pass validation
+    (and then fail to launch on a machine without a GPU)."""
+    MB = 1 << 20
+    disjoint = dict(u=P, delta=P + MB, z=P + 2 * MB, B=P + 3 * MB, C=P + 4 * MB, y=P + 5 * MB, last=P + 6 * MB,
+                    A=P + 7 * MB, D=P + 8 * MB, dt_bias=P + 9 * MB)
+    st = lib.ssm_scan_fwd(*scan_args(**disjoint))
+    assert st in (_native.SSM_OK, _native.SSM_ERR_LAUNCH)
+    for k in ("u", "delta", "z", "B", "C"):
+        assert lib.ssm_scan_fwd(*scan_args(**{**disjoint, "y": disjoint[k]})) == _native.SSM_ERR_ARG, k
+    # a partial overlap: y starting inside u's last element of float32
+    n = 2 * 3 * 5 * 4
+    assert lib.ssm_scan_fwd(*scan_args(**{**disjoint, "y": P + n - 4})) == _native.SSM_ERR_ARG
+    assert lib.ssm_scan_fwd(*scan_args(**{**disjoint, "y": P + n})) in (_native.SSM_OK, _native.SSM_ERR_LAUNCH)
