@@ -342,6 +342,70 @@ def weak_scaling_value(elements_per_rank: int, world: int, ms: float) -> float:
     return elements_per_rank * world / (ms * 1e-3)
 
 
+def partition_boxes(batch: int, dim: int, world: int, rank: int, block: int = 32):
+    """This rank's share of one scan workload when `world` ranks split it (no collective: every
+    (batch, channel) runs its own recurrence).  The units are (batch row, `block`-channel block),
+    batch * ceil(dim / block) of them in row-major order; rank r takes the contiguous range
+    [floor(r U / world), floor((r + 1) U / world)), so shares differ by at most one unit.  The range
+    is returned as boxes (b0, b1, d0, d1): whole rows [b0, b1) x [0, dim), or one row b0 = b1 - 1
+    with channels [d0, d1), each a single contiguous scan call."""
+    per_row = (dim + block - 1) // block
+    units = batch * per_row
+    u0, u1 = units * rank // world, units * (rank + 1) // world
+    boxes = []
+    u = u0
+    while u < u1:
+        b, k = divmod(u, per_row)
+        if k == 0 and u + per_row <= u1:  # whole rows
+            nrows = (u1 - u) // per_row
+            boxes.append((b, b + nrows, 0, dim))
+            u += nrows * per_row
+        else:  # part of row b
+            k1 = min(per_row, k + (u1 - u))
+            boxes.append((b, b + 1, k * block, min(dim, k1 * block)))
+            u += k1 - k
+    return boxes
+
+
+def strong_scaling_value(total_elements: int, ms: float) -> float:
+    """Whole-job throughput when the ranks split one workload: its elements over the slowest rank's time."""
+    return total_elements / (ms * 1e-3)
+
+
+class PartitionRun:
+    """This rank's boxes of the scan workload, each a prepared C-ABI call on its own copy of the
+    box's inputs (whole rows, or one row's channel range: contiguous in the [batch][dim][L]
+    layout).  The rank's inputs are cloned into enough rotating copies that consecutive steps read
+    more than three times the L2 size, so no step finds its inputs in L2."""
+
+    def __init__(self, w: wl.ScanWorkload, device, world: int, rank: int):
+        import math
+        import selective_state_space_155_b300 as ssm
+        self.boxes = partition_boxes(w.batch, w.dim, world, rank)
+        base = wl.scan_inputs(w, device=device)
+        self.elements = sum((b1 - b0) * (d1 - d0) * w.seqlen for b0, b1, d0, d1 in self.boxes)
+        rank_bytes = max(1, w.algorithmic_bytes() * self.elements // max(1, w.elements))
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.copies = max(ROTATING_COPIES, math.ceil(3 * l2 / rank_bytes))
+        self.steps = []
+        for _ in range(self.copies):
+            calls = []
+            for b0, b1, d0, d1 in self.boxes:
+                sub = lambda k: base[k][b0:b1, d0:d1].clone() if base[k] is not None else None
+                bc = lambda k: base[k][b0:b1].clone()
+                u = sub("u")
+                calls.append(ssm.prepare_scan_fwd(
+                    u, sub("delta"), base["A"][d0:d1], bc("B"), bc("C"), base["D"][d0:d1], sub("z"),
+                    base["dt_bias"][d0:d1], delta_softplus=True, y=torch.empty_like(u),
+                    last_state=torch.empty((b1 - b0, d1 - d0, w.dstate), dtype=torch.float32, device=device)))
+            self.steps.append(calls)
+        del base
+
+    def step(self, i: int):
+        for c in self.steps[i % len(self.steps)]:
+            c()
+
+
 # ----------------------------------------------------------------------------------------------
 # CPU baseline (the float64 oracle)
 # ----------------------------------------------------------------------------------------------
@@ -744,6 +808,9 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-long", action="store_true")
+    ap.add_argument("--partition", action="store_true",
+                    help="under torchrun, split one workload over the ranks (strong scaling) instead of running a "
+                         "replica per rank (weak scaling)")
     ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-train", action="store_true")
@@ -784,15 +851,27 @@ def main(argv=None):
     w = wl.MID
     import selective_state_space_155_b300 as ssm
     rates = ssm.probe_unit_rates(device)
-    run = ScanRun(w, device)
     sampler = ClockSampler(local)
-    ms = timed(run.step, args.steps, args.warmup, dist, sampler)
-    ms = max_over_ranks(ms, dist)
-    host_us = {"prepared_call": host_us_per_call(run.step), "binding_call": host_us_per_call(run.step_binding),
-               "how": "host time per enqueue while a spin kernel holds the GPU (the calls only queue)"}
-    elems = w.elements * world
-    value = weak_scaling_value(w.elements, world, ms)
-    bytes_launch = w.algorithmic_bytes()
+    if args.partition:
+        # the ranks split one workload: strong scaling, no collective on the data path
+        run = PartitionRun(w, device, world, rank)
+        ms = max_over_ranks(timed(run.step, args.steps, args.warmup, dist, sampler), dist)
+        host_us = {"prepared_call": host_us_per_call(run.step),
+                   "how": "host time per step's enqueues while a spin kernel holds the GPU"}
+        elems = w.elements
+        value = strong_scaling_value(w.elements, ms)
+        bytes_launch = w.algorithmic_bytes() * run.elements // w.elements  # this rank's share
+        scaling, parallelism = "strong", f"partition of one workload over {world} GPU(s): " \
+            f"(batch row, 32-channel block) units, rank 0's share {run.boxes}"
+    else:
+        run = ScanRun(w, device)
+        ms = max_over_ranks(timed(run.step, args.steps, args.warmup, dist, sampler), dist)
+        host_us = {"prepared_call": host_us_per_call(run.step), "binding_call": host_us_per_call(run.step_binding),
+                   "how": "host time per enqueue while a spin kernel holds the GPU (the calls only queue)"}
+        elems = w.elements * world
+        value = weak_scaling_value(w.elements, world, ms)
+        bytes_launch = w.algorithmic_bytes()
+        scaling, parallelism = "weak", "independent replica per GPU"
     hbm, src = measured_peaks()
     achieved = bytes_launch / (ms * 1e-3) / 1e9
     kernel = "scan_fwd_fused_kernel"  # the balanced layout: the mid workload's plan applies
@@ -802,8 +881,9 @@ def main(argv=None):
 
     res = {
         "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32", "data": "synthetic (seeded N(0,1) bf16 activations, S4D-real A)", "config": workload_config(w),
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": scaling, "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded N(0,1) bf16 activations, S4D-real A)",
+        "config": {**workload_config(w), "parallelism": parallelism},
         "hbm_gbs": achieved, "pct_hbm_roofline": 100.0 * achieved / hbm,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                      "traffic": traffic, "kernel": kernel, "peak_source": f"{src} (MEASURED_PEAKS.json hbm_gbs)"
@@ -817,7 +897,7 @@ def main(argv=None):
         "roofline_alu": alu_roofline(w, ms, rates),
         "unit_rates": {"unit": "lane-operations per clock per SM", **rates},
     }
-    if not args.no_e2e:
+    if not args.no_e2e and not args.partition:
         e2e_ms, h2d, d2h, nsl = run_e2e(w, device, max(3, min(args.steps, 20)), 2, dist)
         res["e2e"] = {"value": elems / (e2e_ms * 1e-3), "unit": "elements/s", "h2d_bytes_per_step": h2d,
                       "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,

@@ -82,7 +82,8 @@ def _load():
             lib.oracle_scan_tree_f64.restype = ctypes.c_int
             lib.oracle_scan_tree_f64.argtypes = [_DP] * 8 + [ctypes.c_int, _DP, _DP] + [ctypes.c_int] * 4
             lib.oracle_scan_bwd_f64.restype = ctypes.c_int
-            lib.oracle_scan_bwd_f64.argtypes = [_DP] * 8 + [ctypes.c_int, ctypes.c_int] + [_DP] * 11 + [ctypes.c_int] * 4
+            lib.oracle_scan_bwd_f64.argtypes = ([_DP] * 8 + [ctypes.c_int, ctypes.c_int] + [_DP] * 11 +
+                                                [ctypes.c_int] * 4 + [_DP] * 5)
             lib.oracle_causal_conv1d_f64.restype = ctypes.c_int
             lib.oracle_causal_conv1d_f64.argtypes = [_DP] * 6 + [ctypes.c_int] * 5
             lib.oracle_softplus_f64.restype = ctypes.c_double
@@ -188,11 +189,14 @@ def scan_tree(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=Tr
     return y, last
 
 
-def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, zoh=False):
+def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softplus=True, h0=None, zoh=False,
+             abs_sums=False):
     """Gradients of the scan (Delta*B form, or the exact zero-order hold with zoh) for the output
     gradient dout [batch, dim, L].
     Returns a dict with du, ddelta, dA, dB, dC and, where the input is given, dD, dz,
-    ddt_bias, dh0 (float64 arrays shaped like their inputs)."""
+    ddt_bias, dh0 (float64 arrays shaped like their inputs).  With abs_sums it also has abs_dA,
+    abs_dB, abs_dC (and abs_dD, abs_ddt_bias where D, dt_bias are given): the sum of the absolute
+    values of the terms each summed gradient adds up."""
     u = _f64(u)
     batch, dim, seqlen = u.shape
     A = _f64(A)
@@ -211,11 +215,15 @@ def scan_bwd(u, delta, A, B, C, dout, D=None, z=None, dt_bias=None, delta_softpl
     g["dz"] = np.zeros_like(u) if z is not None else None
     g["ddt_bias"] = np.zeros(dim) if dt_bias is not None else None
     g["dh0"] = np.zeros((batch, dim, dstate)) if h0 is not None else None
+    for k in ("dA", "dB", "dC", "dD", "ddt_bias"):
+        g["abs_" + k] = np.zeros_like(g[k]) if abs_sums and g[k] is not None else None
     rc = _load().oracle_scan_bwd_f64(_ptr(u), _ptr(delta), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
                                      _ptr(dt_bias), int(bool(delta_softplus)), int(bool(zoh)), _ptr(h0), _ptr(dout),
                                      _ptr(g["du"]),
                                      _ptr(g["ddelta"]), _ptr(g["dA"]), _ptr(g["dB"]), _ptr(g["dC"]), _ptr(g["dD"]),
-                                     _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dh0"]), batch, dim, dstate, seqlen)
+                                     _ptr(g["dz"]), _ptr(g["ddt_bias"]), _ptr(g["dh0"]), batch, dim, dstate, seqlen,
+                                     _ptr(g["abs_dA"]), _ptr(g["abs_dB"]), _ptr(g["abs_dC"]), _ptr(g["abs_dD"]),
+                                     _ptr(g["abs_ddt_bias"]))
     if rc != 0:
         raise RuntimeError(f"oracle_scan_bwd_f64 failed: {rc}")
     return {k: v for k, v in g.items() if v is not None}

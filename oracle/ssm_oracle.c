@@ -193,12 +193,17 @@ static double dsilu_f64(double z) {
  *   dD, ddt_bias          [dim]                  (summed over batch and time; NULL skips)
  *   dh0                   [batch][dim][dstate]   (gradient of the initial state; NULL skips)
  * ddelta is with respect to the raw delta (before dt_bias and softplus).
+ * abs_dA, abs_dB, abs_dC, abs_dD, abs_ddt_bias (each nullable, shaped like its gradient) receive
+ * the sum of the absolute values of the terms that the gradient sums (for dA and d dt_bias, of
+ * each term's parts): the scale that floating-point summation error is proportional to, which
+ * lets a float32 result be held to a bound per element.  They do not change the gradients.
  */
 int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, const double* B, const double* C,
                         const double* D, const double* z, const double* dt_bias, int delta_softplus, int zoh,
                         const double* h0, const double* dout, double* du, double* ddelta, double* dA, double* dB,
                         double* dC, double* dD, double* dz, double* ddt_bias, double* dh0, int batch, int dim,
-                        int dstate, int seqlen) {
+                        int dstate, int seqlen, double* abs_dA, double* abs_dB, double* abs_dC, double* abs_dD,
+                        double* abs_ddt_bias) {
   if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC) return -1;
   if (batch < 0 || dim < 0 || dstate < 1 || seqlen < 0) return -2;
   long N = dstate, L = seqlen;
@@ -206,6 +211,11 @@ int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, c
   for (long i = 0; i < (long)batch * N * L; ++i) dB[i] = dC[i] = 0.0;
   if (dD) for (int i = 0; i < dim; ++i) dD[i] = 0.0;
   if (ddt_bias) for (int i = 0; i < dim; ++i) ddt_bias[i] = 0.0;
+  if (abs_dA) for (long i = 0; i < (long)dim * N; ++i) abs_dA[i] = 0.0;
+  if (abs_dB) for (long i = 0; i < (long)batch * N * L; ++i) abs_dB[i] = 0.0;
+  if (abs_dC) for (long i = 0; i < (long)batch * N * L; ++i) abs_dC[i] = 0.0;
+  if (abs_dD) for (int i = 0; i < dim; ++i) abs_dD[i] = 0.0;
+  if (abs_ddt_bias) for (int i = 0; i < dim; ++i) abs_ddt_bias[i] = 0.0;
   double* hs = (double*)malloc(sizeof(double) * (size_t)((L + 1) * N + 1)); /* hs[(t+1)*N + n] = h_t */
   double* carry = (double*)malloc(sizeof(double) * (size_t)N);
   double* ys = (double*)malloc(sizeof(double) * (size_t)(L + 1));
@@ -239,8 +249,9 @@ int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, c
       double dy = zr ? gr[t] * silu_f64(zr[t]) : gr[t];
       if (zr && dz) dz[ch * L + t] = gr[t] * ys[t] * dsilu_f64(zr[t]);
       if (D && dD) dD[d] += dy * ur[t];
+      if (D && abs_dD) abs_dD[d] += fabs(dy * ur[t]);
       double dut = D ? dy * D[d] : 0.0;
-      double ddt = 0.0;
+      double ddt = 0.0, ddt_abs = 0.0;
       for (long n = 0; n < N; ++n) {
         double an = A[(long)d * N + n];
         double a = exp(dt * an);
@@ -262,12 +273,17 @@ int oracle_scan_bwd_f64(const double* u, const double* delta, const double* A, c
         ddt += lam * (an * a * hp + dc_ddt * bn * ur[t]);
         dA[(long)d * N + n] += lam * (dt * a * hp + dc_da * bn * ur[t]);
         carry[n] = lam * a;
+        if (abs_dC) abs_dC[((long)b * N + n) * L + t] += fabs(dy * hs[(t + 1) * N + n]);
+        if (abs_dB) abs_dB[((long)b * N + n) * L + t] += fabs(lam * c * ur[t]);
+        if (abs_dA) abs_dA[(long)d * N + n] += fabs(lam * (dt * a * hp)) + fabs(lam * (dc_da * bn * ur[t]));
+        ddt_abs += fabs(lam * an * a * hp) + fabs(lam * dc_ddt * bn * ur[t]);
       }
       du[ch * L + t] = dut;
       double raw = dr[t] + (dt_bias ? dt_bias[d] : 0.0);
       double dd = delta_softplus ? ddt / (1.0 + exp(-raw)) : ddt; /* softplus' = sigmoid */
       ddelta[ch * L + t] = dd;
       if (ddt_bias && dt_bias) ddt_bias[d] += dd;
+      if (abs_ddt_bias && dt_bias) abs_ddt_bias[d] += delta_softplus ? ddt_abs / (1.0 + exp(-raw)) : ddt_abs;
     }
     if (dh0)
       for (long n = 0; n < N; ++n) dh0[ch * N + n] = carry[n];

@@ -540,6 +540,38 @@ def test_backward_prefix_sum_closed_form():
     np.testing.assert_allclose(g["ddelta"][0, 0], tail * u[0, 0, :], rtol=1e-12, atol=1e-14)
 
 
+SUMMED = ("dA", "dB", "dC", "dD", "ddt_bias")
+
+
+@pytest.mark.parametrize("zoh", [False, True])
+def test_backward_abs_sums_bound_the_gradients(zoh):
+    """The absolute-term sums are the magnitude scale of each summed gradient (triangle inequality)
+    and leave the gradients themselves bitwise unchanged."""
+    case, dout = _bwd_case(5)
+    kw = dict(D=case["D"], z=case["z"], dt_bias=case["dt_bias"], h0=case["h0"], zoh=zoh)
+    g = oracle.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dout, **kw)
+    ga = oracle.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dout, abs_sums=True, **kw)
+    for k in g:
+        np.testing.assert_array_equal(g[k], ga[k])
+    for k in SUMMED:
+        assert np.all(ga["abs_" + k] >= np.abs(ga[k]) * (1 - 1e-14)), k
+        assert np.any(ga["abs_" + k] > np.abs(ga[k]) * (1 + 1e-6)), k  # mixed signs in a generic case
+
+
+def test_backward_abs_sums_equal_the_gradients_when_every_term_is_nonnegative():
+    """With u, B, C, D, h0, dout >= 0, A < 0, Delta > 0 and no gate every term of dA, dB, dC and
+    dD is >= 0 (the adjoint stays >= 0), so each absolute-term sum is its gradient exactly: the
+    sums add up the very terms the gradients do, in the same order."""
+    case, dout = _bwd_case(6, gate=False)
+    for k in ("u", "B", "C", "D", "h0"):
+        case[k] = np.abs(case[k])
+    dout = np.abs(dout)
+    ga = oracle.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], dout, D=case["D"],
+                         dt_bias=case["dt_bias"], h0=case["h0"], abs_sums=True)
+    for k in ("dA", "dB", "dC", "dD"):
+        np.testing.assert_array_equal(ga["abs_" + k], ga[k])
+
+
 @pytest.mark.parametrize("softplus", [True, False])
 @pytest.mark.parametrize("name", sorted(GRAD_OF))
 def test_zoh_backward_matches_finite_differences(name, softplus):
