@@ -115,12 +115,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return done != 0;
 }
+// Arrive on `bar` and add `bytes` to the transaction count its current phase waits for (the bytes a
+// tensor copy issued next will deliver).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+// Make the mbarrier initialisations visible to the tensor-copy unit before its first completion.
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
+// Tensor copy (TMA) of the 2-D box at (x = column, y = row) of the tensor map into shared memory
+// at dst (128-byte aligned), completing `bytes` of the transaction count of `bar`.  Columns past the
+// tensor's extent and rows past its end are filled with zeros.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+// The same for a 3-D box at (x, y, z).
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* tmap, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // Wait until `bar` completes the phase of the given parity.  The wait is bounded: it gives up after
 // `limit` clock cycles, or at once when *abort (a CTA-wide flag in shared memory) is set; giving up
 // sets *abort, adds one to *timeouts for the wait that ran out, and returns false, so that a broken
 // hand-off ends the kernel (with garbage outputs and a counted timeout) instead of hanging it.
 // Between tests the warp sleeps for `backoff_ns` nanoseconds, so that a waiting warp takes almost
-// no issue slots from the warps doing the work.
+// no issue slots from the warps doing the work.  With abort == nullptr the wait runs to its limit
+// regardless of any flag (used to drain copies still in flight before a CTA exits).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, long long limit,
                                           unsigned long long* timeouts, unsigned backoff_ns) {
   if (mbar_try_wait(bar, parity)) return true;
@@ -128,9 +154,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   while (true) {
     __nanosleep(backoff_ns);
     if (mbar_try_wait(bar, parity)) return true;
-    if (*abort) return false;
+    if (abort && *abort) return false;
     if (clock64() - t0 > limit) {
-      *abort = 1;
+      if (abort) *abort = 1;
       atomicAdd(timeouts, 1ull);
       return false;
     }

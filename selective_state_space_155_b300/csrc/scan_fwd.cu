@@ -38,8 +38,10 @@
 //    Delta = 0.  Both leave the state unchanged, so one code path serves every size.
 //  * With a checkpoint buffer (the training forward), the recurrence lanes also store the state
 //    at the start of every chunk, which is what the backward pass restarts from.
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
+#include <cudaTypedefs.h>
 #include <stdint.h>
 
 #include <algorithm>
@@ -57,6 +59,7 @@ namespace {
 constexpr int kChunk = kScanChunk;  // steps per chunk (the checkpoint interval)
 constexpr int kWin = 16;    // steps per recurrence window (readout partials held in registers)
 constexpr int kPrepWarps = 4;
+constexpr int kUnitRows = 8;  // channels per balanced-plan unit (and per small tensor-copy box)
 
 // Register split of the four-recurrence-warp layout (dstate 9..16): the kernel is launched with
 // kLaunchRegs per thread; the prep warpgroup gives registers back and the recurrence warpgroup,
@@ -81,6 +84,17 @@ __device__ unsigned long long g_scan_wait_timeouts;
 
 namespace {
 
+// Tensor maps (TMA descriptors) of the five streamed inputs: u, delta, z with rows batch*dim in
+// boxes of 32 channels, B and C with rows batch*dstate in boxes of NPAD states.  With `pair` set
+// (the sequence a whole number of chunks), each is a 3-D view [chunk][row][step of the chunk]
+// and one copy brings two chunks, landing chunk-major ([chunk][row][step]); otherwise a 2-D view
+// [row][step] with one chunk per copy (steps past the end read as zeros).  Passed by value as a
+// kernel parameter; the z map is unused (zero) when there is no gate.
+struct alignas(64) TmaMaps {
+  CUtensorMap u, delta, z, B, C;
+  int pair;
+};
+
 template <typename T, int NPAD>
 struct ScanCfg {
   static constexpr int R = NPAD / 4;                  // lanes per channel
@@ -90,34 +104,41 @@ struct ScanCfg {
   static constexpr int CPW = 32 / R;                  // channels per recurrence warp
   static constexpr int CPB = CPW * CWARPS;            // channels per CTA (32)
   static constexpr int EPV = 16 / sizeof(T);          // elements per 16-byte vector
-  static constexpr int RS = kChunk + EPV;             // padded row stride (elements) of staged rows
   static constexpr int VPR = kChunk / EPV;            // 16-byte vectors per staged row
   static constexpr int ROWS = 3 * CPB + 2 * NPAD;     // u, delta, z rows, then B rows, then C rows
-  static constexpr int PSS = CPB + 4;                 // row stride (float2) of the (Delta, Delta*u) table
+  static constexpr int PSS = kChunk + 2;              // row stride (float2) of the (Delta, Delta*u) table
   static constexpr int DSS = kChunk + 2;              // row stride (float2) of the (D*u, silu z) table
   static constexpr int OPL = kWin / R;                // outputs each lane finishes per window
+  // raw stage: room for SLOTS chunks as five tiles [slot][rows][kChunk] (u, delta, z, B, C); the
+  // element offsets of the tiles and of one chunk slot within a tile
+  static constexpr int SLOTS = sizeof(T) == 2 ? 2 : 1;
+  static constexpr int kUTile = 0, kDTile = SLOTS * CPB * kChunk, kZTile = 2 * SLOTS * CPB * kChunk,
+                       kBTile = 3 * SLOTS * CPB * kChunk, kCTile = kBTile + SLOTS * NPAD * kChunk;
+  static constexpr int kXSlot = CPB * kChunk, kBCSlot = NPAD * kChunk;
+  static constexpr uint32_t kXBytes = CPB * kChunk * sizeof(T), kBBytes = NPAD * kChunk * sizeof(T);
   // shared memory map (bytes)
-  static constexpr size_t kRawStage = size_t(ROWS) * RS * sizeof(T);
+  static constexpr size_t kRawStage = size_t(SLOTS) * ROWS * kChunk * sizeof(T);
   static constexpr int kCOfs = kChunk * NPAD + 16;    // float offset of the C table after the B table
   static constexpr size_t kBCStage = size_t(kCOfs + kChunk * NPAD) * sizeof(float);  // Bs, Cs [CHUNK][NPAD]
-  static constexpr size_t kPStage = size_t(kChunk) * PSS * sizeof(float2);      // Ps [CHUNK][PSS]
+  static constexpr size_t kPStage = size_t(CPB) * PSS * sizeof(float2);         // Ps [CPB][PSS]
   static constexpr size_t kDSStage = size_t(CPB) * DSS * sizeof(float2);        // DS [CPB][DSS]
   static constexpr size_t kTabStage = kBCStage + kPStage + kDSStage;
   static constexpr size_t kRaw = 2 * kRawStage;
   static constexpr size_t kTab = 2 * kTabStage;
-  static constexpr size_t kBarOfs = kRaw + kTab;                 // FULL0, FULL1, EMPTY0, EMPTY1 mbarriers
-  static constexpr size_t kSmem = kBarOfs + 4 * sizeof(uint64_t);
+  // mbarriers: FULL0, FULL1 (tables written), EMPTY0, EMPTY1 (tables read), RAW0, RAW1 (raw chunk
+  // landed); then the prep's copy decision word
+  static constexpr size_t kBarOfs = kRaw + kTab;
+  static constexpr size_t kSmem = (kBarOfs + 6 * sizeof(uint64_t) + 16 + 127) / 128 * 128;
+  static_assert(kRawStage % 128 == 0 && kXBytes % 128 == 0 && kBBytes % 128 == 0,
+                "tensor-copy destinations are 128-byte aligned");
   static_assert(kRawStage % 16 == 0 && kBCStage % 16 == 0 && kPStage % 16 == 0 && kDSStage % 16 == 0, "align");
   static_assert(OPL % 4 == 0 && kChunk % kWin == 0, "each lane finishes whole 16-byte units of the window");
-  static_assert((RS * sizeof(T)) % 16 == 0 && kChunk % 8 == 0, "staged rows hold whole 16-byte vectors");
+  static_assert((kChunk * sizeof(T)) % 16 == 0, "staged rows hold whole 16-byte vectors");
 };
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 
 __device__ __forceinline__ void bar_sync(int id, int n) { asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory"); }
-__device__ __forceinline__ void bar_arrive(int id, int n) {
-  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 
 template <typename T>
 __device__ __forceinline__ float2 load2(const T* p);  // two consecutive io elements as float32
@@ -186,10 +207,11 @@ __device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) 
 // barriers bar0 + 1 .. bar0 + 5; tid is the thread's index within the group, abort the CTA's
 // give-up flag.  A CTA of the plain kernel is one group.
 template <typename T, int NPAD, bool VEC, bool ZOH>
-__device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* smem, const int tid, const int b,
-                                           const int d0, const int dlim, const int bar0, volatile int* abort) {
+__device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& maps, unsigned char* smem, const int tid,
+                                           const int b, const int d0, const int dlim, const int bar0,
+                                           volatile int* abort) {
   using Cfg = ScanCfg<T, NPAD>;
-  constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, RS = Cfg::RS, VPR = Cfg::VPR;
+  constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, VPR = Cfg::VPR;
   constexpr int NT = Cfg::NT, PT = Cfg::PT, ROWS = Cfg::ROWS, PSS = Cfg::PSS, DSS = Cfg::DSS, OPL = Cfg::OPL;
   constexpr int CWARPS = Cfg::CWARPS;
 
@@ -215,6 +237,8 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
   if (tid == 0) {
     mbar_init(&mb[0], PT), mbar_init(&mb[1], PT);
     mbar_init(&mb[2], 32 * rec_warps), mbar_init(&mb[3], 32 * rec_warps);
+    mbar_init(&mb[4], 1), mbar_init(&mb[5], 1);  // RAW: one expect-tx arrival each
+    fence_mbar_init();
   }
   bar_sync(kBarInit + bar0, NT);  // the group's mbarriers are initialised before anyone uses them
 
@@ -225,119 +249,153 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
     const int pw = warp - CWARPS;
     const int dim = a.dim;
     const bool softplus = a.softplus != 0;
-    const T* __restrict__ gu = static_cast<const T*>(a.u);
-    const T* __restrict__ gd = static_cast<const T*>(a.delta);
-    const T* __restrict__ gz = static_cast<const T*>(a.z);
-    const T* __restrict__ gB = static_cast<const T*>(a.B);
-    const T* __restrict__ gC = static_cast<const T*>(a.C);
 
-    // Global start of staged row r (u, delta, z rows by channel, then B and C rows by state);
-    // ok = the row exists.  Rows of channels past dim and z rows without a gate are never used
-    // by another channel, so they are not copied; B and C rows past dstate are zero-filled
-    // (every channel reads them).
-    auto row_src = [&](int r, bool& ok, bool& fill) -> const T* {
-      if (r < 3 * CPB) {
-        const int which = r / CPB, c = r % CPB;
-        const T* base = which == 0 ? gu : (which == 1 ? gd : gz);
-        ok = (d0 + c < dlim) && (which < 2 || has_z);
-        fill = false;
-        return ok ? base + (size_t(b) * dim + (d0 + c)) * L : gu;
+    // A raw stage holds G chunks (G = 2 with paired copies, else 1) as five dense tiles: u, delta,
+    // z rows of the group's 32 channel slots, then the NPAD B and C rows of batch row b.  On the
+    // 16-byte path they arrive by tensor copies (TMA), whose completion the stage's RAW mbarrier
+    // counts; rows past a tensor's end and steps past the sequence end arrive as zeros.  Channel
+    // slots past the group's range hold other channels' rows and are ignored (their Delta and D
+    // are 0 and their lanes store nothing); B and C rows past dstate are set to 0 in the
+    // conversion.  A copy takes its issuing thread a few hundred cycles (the SM's copy unit takes
+    // instructions one at a time), so the five copies of a stage are spread over the prep warps'
+    // lane 0: warp 0 copies B and C, warps 1, 2, 3 copy u, delta and z.  Before any of them is
+    // issued, ptid 0 has arrived on the stage's RAW barrier with the stage's byte count, so the
+    // barrier's transaction count never runs ahead of its arrival.
+    const bool pair = VEC && Cfg::SLOTS == 2 && maps.pair != 0;
+    const int lg = pair ? 1 : 0;  // log2 of the chunks per raw stage
+    const uint32_t stage_bytes = uint32_t((has_z ? 3 : 2) * Cfg::kXBytes + 2 * Cfg::kBBytes) << lg;
+    auto issue_copies = [&](int stage, int t0) {  // lane 0 of every prep warp
+      T* dst = raw + size_t(stage) * Cfg::SLOTS * ROWS * kChunk;
+      uint64_t* rb = &mb[4 + stage];
+      const int c0 = t0 / kChunk;
+      if (pw == 0) {
+        if (pair) {
+          tma_load_3d(dst + Cfg::kBTile, &maps.B, 0, b * N, c0, rb);
+          tma_load_3d(dst + Cfg::kCTile, &maps.C, 0, b * N, c0, rb);
+        } else {
+          tma_load_2d(dst + Cfg::kBTile, &maps.B, t0, b * N, rb);
+          tma_load_2d(dst + Cfg::kCTile, &maps.C, t0, b * N, rb);
+        }
+      } else if (pw < 3 || has_z) {
+        const CUtensorMap* m = pw == 1 ? &maps.u : (pw == 2 ? &maps.delta : &maps.z);
+        T* tile = dst + (pw - 1) * Cfg::SLOTS * CPB * kChunk;
+        if (pair)
+          tma_load_3d(tile, m, 0, b * dim + d0, c0, rb);
+        else
+          tma_load_2d(tile, m, t0, b * dim + d0, rb);
       }
-      const int rr = r - 3 * CPB;
-      const int which = rr / NPAD, n = rr % NPAD;
-      ok = n < N;
-      fill = true;
-      return ok ? (which == 0 ? gB : gC) + (size_t(b) * N + n) * L : gu;
     };
-
-    // Each prep thread owns the same SLOTS 16-byte copy slots (row, column) in every chunk, so
-    // their addresses are worked out once.
-    constexpr int NV = ROWS * VPR;
-    constexpr int SLOTS = (NV + PT - 1) / PT;
-    const T* s_src[SLOTS];  // global address of the slot's first element in chunk 0
-    int s_dst[SLOTS];       // element offset within a raw stage, -1 = nothing to copy
-    int s_col[SLOTS];       // first step of the slot within a chunk
-    bool s_ok[SLOTS];
-    if constexpr (VEC) {
-#pragma unroll
-      for (int i = 0; i < SLOTS; ++i) {
-        const int v = ptid + i * PT;
-        const int r = v / VPR, j = v % VPR;
-        bool ok = false, fill = false;
-        const T* src = v < NV ? row_src(r, ok, fill) : gu;
-        s_src[i] = ok ? src + j * EPV : gu;
-        s_dst[i] = (v < NV && (ok || fill)) ? r * RS + j * EPV : -1;
-        s_col[i] = j * EPV;
-        s_ok[i] = ok;
-      }
-    }
-    auto stage_load = [&](int stage, int t0) {
-      T* dst = raw + size_t(stage) * ROWS * RS;
-      if constexpr (VEC) {
-#pragma unroll
-        for (int i = 0; i < SLOTS; ++i) {
-          if (s_dst[i] < 0) continue;
-          // rows are 16-byte multiples, so a vector is wholly inside or wholly past the end;
-          // a zero-byte copy only zero-fills, but its source must still be a valid address
-          const bool in = s_ok[i] && t0 + s_col[i] < L;
-          cp_async_16(dst + s_dst[i], in ? static_cast<const void*>(s_src[i] + t0) : gu, in ? 16 : 0);
+    // element-wise copy of one chunk into slot 0 of a stage by every prep thread (rows not 16-byte
+    // aligned)
+    auto stage_copy = [&](int stage, int t0) {
+      T* dst = raw + size_t(stage) * Cfg::SLOTS * ROWS * kChunk;
+      const T* gu = static_cast<const T*>(a.u);
+      const T* gd = static_cast<const T*>(a.delta);
+      const T* gz = static_cast<const T*>(a.z);
+      const T* gB = static_cast<const T*>(a.B);
+      const T* gC = static_cast<const T*>(a.C);
+      for (int e = ptid; e < ROWS * kChunk; e += PT) {
+        const int r = e / kChunk, j = e % kChunk, t = t0 + j;
+        T v = from_f32<T>(0.0f);
+        int o;
+        if (r < 3 * CPB) {
+          const int which = r / CPB, c = r % CPB;
+          const T* base = which == 0 ? gu : (which == 1 ? gd : gz);
+          if (d0 + c < dlim && (which < 2 || has_z) && t < L) v = base[(size_t(b) * dim + d0 + c) * L + t];
+          o = which * Cfg::SLOTS * CPB * kChunk + c * kChunk + j;
+        } else {
+          const int rr = r - 3 * CPB, which = rr / NPAD, n = rr % NPAD;
+          if (n < N && t < L) v = (which == 0 ? gB : gC)[(size_t(b) * N + n) * L + t];
+          o = (which == 0 ? Cfg::kBTile : Cfg::kCTile) + n * kChunk + j;
         }
-      } else {
-        for (int e = ptid; e < ROWS * kChunk; e += PT) {
-          const int r = e / kChunk, j = e % kChunk;
-          bool ok, fill;
-          const T* src = row_src(r, ok, fill);
-          if (!ok && !fill) continue;
-          const int t = t0 + j;
-          dst[r * RS + j] = (ok && t < L) ? src[t] : from_f32<T>(0.0f);
-        }
+        dst[o] = v;
       }
     };
 
-    // B, C conversion items: one item = 8 steps of one row.  Lanes 0..NPAD-1 of a group take the
-    // B rows and the next NPAD lanes the C rows of the same steps; the C table is offset by 16
-    // words so that both halves land in different banks.
-    constexpr int SPI = 8;
-    constexpr int NITEM = 2 * NPAD * (kChunk / SPI);
+    // B, C conversion items: one 16-byte vector (EPV steps) of one row.  Lanes 0..NPAD-1 take the B
+    // rows and the next NPAD lanes the C rows; each lane reads vector (q + rotation) of its row, a
+    // rotation by row that puts the eight rows of a quarter-warp on different banks of the dense
+    // stage (bf16 rows are 64 bytes, two to a bank line).
+    constexpr int NITEM = 2 * NPAD * VPR;
     constexpr int IPT = (NITEM + PT - 1) / PT;
     int c_src[IPT], c_dst[IPT];
+    bool c_ok[IPT];
 #pragma unroll
     for (int m = 0; m < IPT; ++m) {
       const int e = ptid + m * PT;
       const int n = e % NPAD, which = (e / NPAD) % 2, q = e / (2 * NPAD);
-      c_src[m] = e < NITEM ? (3 * CPB + which * NPAD + n) * RS + q * SPI : -1;
-      c_dst[m] = which * Cfg::kCOfs + (q * SPI) * NPAD + n;
+      const int qr = (q + (sizeof(T) == 2 ? (n >> 1) : n)) & (VPR - 1);
+      c_src[m] = e < NITEM ? (which == 0 ? Cfg::kBTile : Cfg::kCTile) + n * kChunk + qr * EPV : -1;
+      c_dst[m] = which * Cfg::kCOfs + (qr * EPV) * NPAD + n;
+      c_ok[m] = n < N;
     }
 
-    // prologue mapping: prep warp pw handles channels PCW*pw + (lane % PCW); the lanes lane/PCW +
-    // PPL*i walk the step pairs of the chunk (conflict-free reads of the staged rows)
-    constexpr int PCW = CPB / kPrepWarps;  // channels per prep warp (8)
-    constexpr int PPL = 32 / PCW;          // step-pair lanes per channel (4)
-    const int pcl = pw * PCW + (lane % PCW);
-    const int tq = lane / PCW;
-    const bool pch_ok = d0 + pcl < dlim;
-    const float p_bias = (pch_ok && a.dt_bias) ? a.dt_bias[d0 + pcl] : 0.0f;
-    const float p_D = (pch_ok && a.D) ? a.D[d0 + pcl] : 0.0f;
-    const int r_ofs = pcl * RS + 2 * tq;     // element offset of this lane's first step pair in a row
-    const int ps_ofs = 2 * tq * PSS + pcl;   // float2 offset of its first (Delta, Delta*u) entry
-    const int ds_ofs = pcl * DSS + 2 * tq;   // float2 offset of its first (D*u, silu z) entry
+    // Element items: (channel, step pair), item e = ptid + PT i covering channel e / 16 and steps
+    // 2 (e % 16), 2 (e % 16) + 1, so that a warp reads two channels' rows of one chunk: 32 lanes on 32
+    // different banks.  Each thread keeps the same step pair and IPE channels.
+    constexpr int IPE = CPB * (kChunk / 2) / PT;
+    static_assert(IPE * PT == CPB * (kChunk / 2), "whole element items per prep thread");
+    const int ep = ptid % (kChunk / 2);  // step pair
+    const int ech0 = ptid / (kChunk / 2);  // first channel; item i takes channel ech0 + i * PT / 16
+    constexpr int ECH = PT / (kChunk / 2);
+    float e_bias[IPE], e_D[IPE];
+#pragma unroll
+    for (int i = 0; i < IPE; ++i) {
+      const int c = d0 + ech0 + i * ECH;
+      e_bias[i] = (c < dlim && a.dt_bias) ? a.dt_bias[c] : 0.0f;
+      e_D[i] = (c < dlim && a.D) ? a.D[c] : 0.0f;
+    }
 
-    if (nchunks > 0) stage_load(0, 0);
-    cp_async_commit();
-    if (nchunks > 1) stage_load(1, kChunk);
-    cp_async_commit();
+    // Copies in flight, tracked by ptid 0: the raw-stage use (chunk >> lg) whose copies into raw
+    // stage 0 / 1 have been issued but not yet seen complete, or -1.  Whether a stage is refilled
+    // is decided once, by ptid 0 before the closing barrier of the stage's last chunk, and read by
+    // every issuing lane after it: only after the stage's last copies were seen complete and
+    // while no wait has given up, so that no copy lands on one still in flight and every issued
+    // copy belongs to a counted phase.  Before the CTA exits, ptid 0 waits once more for copies
+    // still in flight.
+    volatile int* decide = reinterpret_cast<volatile int*>(smem + Cfg::kBarOfs + 6 * sizeof(uint64_t));
+    const bool tma_ok = (smem_u32(raw) & 127u) == 0;  // tensor copies need a 128-byte aligned destination
+    const int nstages = (nchunks + (1 << lg) - 1) >> lg;  // raw-stage uses
+    int pend0 = -1, pend1 = -1;
+    if (VEC && !tma_ok && ptid == 0) {
+      *abort = 1;  // give up at once rather than copy
+      atomicAdd(&g_scan_wait_timeouts, 1ull);
+    }
+    if (VEC && tma_ok) {
+      if (ptid == 0) {
+        if (nstages > 0) mbar_arrive_expect_tx(&mb[4], stage_bytes), pend0 = 0;
+        if (nstages > 1) mbar_arrive_expect_tx(&mb[5], stage_bytes), pend1 = 1;
+      }
+      bar_sync(bPrep, PT);
+      if (lane == 0) {
+        if (nstages > 0) issue_copies(0, 0);
+        if (nstages > 1) issue_copies(1, kChunk << lg);
+      }
+    }
 
     for (int k = 0; k < nchunks; ++k) {
       const int s = k & 1;
       const int t0 = k * kChunk;
-      cp_async_wait<1>();           // this thread's copies of chunk k have landed
-      // the recurrence warps are done with table stage s (their reads of chunk k - 2): one prep warp
-      // waits, the others learn it from the named barrier below
-      if (k >= 2 && pw == 0)
-        mbar_wait(&mb[2 + s], ((k - 2) >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
-      bar_sync(bPrep, PT);          // every prep thread's copies have landed, and stage s is free
+      const int su = k >> lg, rs = su & 1;   // raw-stage use and raw stage of chunk k
+      const int slot = k & ((1 << lg) - 1);  // its slot within the stage
+      if (VEC) {
+        // one prep warp waits for the raw chunk and for a free table stage; the others learn both
+        // from the named barrier below (waiting warps there take no issue slots)
+        if (pw == 0) {
+          if (slot == 0 && mbar_wait(&mb[4 + rs], (su >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff))
+            (rs ? pend1 : pend0) = -1;
+          if (k >= 2)
+            mbar_wait(&mb[2 + s], ((k - 2) >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
+        }
+      } else {
+        stage_copy(rs, t0);
+        if (pw == 0 && k >= 2)
+          mbar_wait(&mb[2 + s], ((k - 2) >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
+      }
+      bar_sync(bPrep, PT);  // raw chunk k is in its stage for every prep thread, and table stage s is free
 
-      const T* st = raw + size_t(s) * ROWS * RS;
+      const T* st = raw + size_t(rs) * Cfg::SLOTS * ROWS * kChunk;
+      const int xo = slot * Cfg::kXSlot, bo = slot * Cfg::kBCSlot;  // this chunk's slot in the tiles
       float* BCs = tabBs(s);
       float2* Ps = tabPs(s);
       float2* DS = tabDS(s);
@@ -345,52 +403,58 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
 #pragma unroll
       for (int m = 0; m < IPT; ++m) {
         if (c_src[m] < 0) continue;
-        float v[SPI];
-        load8<T>(st + c_src[m], v);
+        float v[EPV];
+        if constexpr (sizeof(T) == 2) {
+          float w8[8];
+          load8<T>(st + bo + c_src[m], w8);
+#pragma unroll
+          for (int j = 0; j < EPV; ++j) v[j] = w8[j];
+        } else {
+          const float4 w4 = *reinterpret_cast<const float4*>(st + bo + c_src[m]);
+          v[0] = w4.x, v[1] = w4.y, v[2] = w4.z, v[3] = w4.w;
+        }
         float* dst = BCs + c_dst[m];
 #pragma unroll
-        for (int j = 0; j < SPI; ++j) dst[j * NPAD] = v[j];
+        for (int j = 0; j < EPV; ++j) dst[j * NPAD] = c_ok[m] ? v[j] : 0.0f;
       }
 
-      // per-element work: Delta, Delta*u, D*u, silu(z), two steps per item.  Steps past the end
-      // (and channels past dim) get Delta = 0, which leaves the state unchanged.
-      const int lim = pch_ok ? L - t0 : 0;
-      auto items = [&](auto masked) {
+      // per-element work: Delta, Delta*u (u alone for the zero-order hold, whose Bbar factor needs
+      // Delta and A together and is formed in the recurrence), D*u, silu(z).  Steps past the end
+      // and channels past the group's range get Delta = 0, which leaves the state unchanged.
+      const int lim = L - t0;
 #pragma unroll
-        for (int i = 0; i < kChunk / 2 / PPL; ++i) {
-          const int o = 2 * PPL * i;
-          const float2 uu = load2<T>(st + r_ofs + o);
-          const float2 dr = load2<T>(st + CPB * RS + r_ofs + o);
-          const float2 zz = load2<T>(st + 2 * CPB * RS + r_ofs + o);
-          const float2 dx = __fadd2_rn(dr, f2(p_bias, p_bias));
-          const float2 sp = softplus2(dx);
-          float2 dl = softplus ? sp : dx;
-          if constexpr (decltype(masked)::value) {
-            const int t = 2 * tq + o;
-            dl.x = t < lim ? dl.x : 0.0f;
-            dl.y = t + 1 < lim ? dl.y : 0.0f;
-          }
-          // the recurrence's input factor: Delta*u, or u alone for the zero-order hold (whose
-          // Bbar factor needs Delta and A together and is formed in the recurrence)
-          const float2 du = ZOH ? uu : __fmul2_rn(dl, uu);
-          const float2 Du = __fmul2_rn(f2(p_D, p_D), uu);
-          const float2 sg = has_z ? silu2<std::is_same<T, __nv_bfloat16>::value>(zz) : f2(1.0f, 1.0f);
-          Ps[ps_ofs + o * PSS] = f2(dl.x, du.x);
-          Ps[ps_ofs + (o + 1) * PSS] = f2(dl.y, du.y);
-          *reinterpret_cast<float4*>(DS + ds_ofs + o) = make_float4(Du.x, sg.x, Du.y, sg.y);
-        }
-      };
-      if (lim >= kChunk)
-        items(std::false_type{});
-      else
-        items(std::true_type{});
+      for (int i = 0; i < IPE; ++i) {
+        const int ch = ech0 + i * ECH;
+        const int o = ch * kChunk + 2 * ep;
+        const float2 uu = load2<T>(st + Cfg::kUTile + xo + o);
+        const float2 dr = load2<T>(st + Cfg::kDTile + xo + o);
+        const float2 dx = __fadd2_rn(dr, f2(e_bias[i], e_bias[i]));
+        float2 dl = softplus ? softplus2(dx) : dx;
+        const int lim_c = d0 + ch < dlim ? lim : 0;
+        dl.x = 2 * ep < lim_c ? dl.x : 0.0f;
+        dl.y = 2 * ep + 1 < lim_c ? dl.y : 0.0f;
+        const float2 du = ZOH ? uu : __fmul2_rn(dl, uu);
+        const float2 Du = __fmul2_rn(f2(e_D[i], e_D[i]), uu);
+        const float2 sg = has_z ? silu2<std::is_same<T, __nv_bfloat16>::value>(load2<T>(st + Cfg::kZTile + xo + o))
+                                : f2(1.0f, 1.0f);
+        *reinterpret_cast<float4*>(Ps + ch * PSS + 2 * ep) = make_float4(dl.x, du.x, dl.y, du.y);
+        *reinterpret_cast<float4*>(DS + ch * DSS + 2 * ep) = make_float4(Du.x, sg.x, Du.y, sg.y);
+      }
 
-      bar_sync(bPrep, PT);               // every prep thread is done reading raw stage s
-      mbar_arrive(&mb[s]);               // this thread's part of table stage s is written
-      if (k + 2 < nchunks) stage_load(s, t0 + 2 * kChunk);
-      cp_async_commit();
+      const bool last_of_stage = slot == (1 << lg) - 1 || k == nchunks - 1;
+      if (VEC && ptid == 0 && last_of_stage) {
+        const bool refill = su + 2 < nstages && (rs ? pend1 : pend0) < 0 && !*abort;
+        if (refill) mbar_arrive_expect_tx(&mb[4 + rs], stage_bytes), (rs ? pend1 : pend0) = su + 2;
+        *decide = refill ? 1 : 0;
+      }
+      bar_sync(bPrep, PT);  // every prep thread is done reading chunk k; the decision is visible
+      mbar_arrive(&mb[s]);  // this thread's part of table stage s is written
+      if (VEC && lane == 0 && last_of_stage && *decide) issue_copies(rs, (su + 2) * (kChunk << lg));
     }
-    cp_async_wait<0>();
+    if (VEC && ptid == 0) {  // these last waits ignore the CTA's give-up flag
+      if (pend0 >= 0) mbar_wait(&mb[4], (pend0 >> 1) & 1, nullptr, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
+      if (pend1 >= 0) mbar_wait(&mb[5], (pend1 >> 1) & 1, nullptr, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
+    }
     return;
   }
 
@@ -445,7 +509,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
 #pragma unroll
       for (int j = 0; j < kWin; ++j) {
         const int t = w + j;
-        const float2 p = Ps[t * PSS + cl];
+        const float2 p = Ps[cl * PSS + t];
         const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
         const float4 cc = *reinterpret_cast<const float4*>(Cs + t * NPAD + 4 * g);
         const float2 dd = f2(p.x, p.x), uu = f2(p.y, p.y);
@@ -529,8 +593,9 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, unsigned char* sme
 // The plain kernel: CTA blockIdx.x scans 32-channel block (blockIdx.x % blocks per row) of batch
 // row blockIdx.x / blocks per row.
 template <typename T, int NPAD, bool VEC, bool ZOH>
-__global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const ScanArgs a) {
-  extern __shared__ __align__(16) unsigned char smem[];
+__global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3)
+    scan_fwd_kernel(const ScanArgs a, const __grid_constant__ TmaMaps maps) {
+  extern __shared__ __align__(128) unsigned char smem[];
   constexpr int CPB = ScanCfg<T, NPAD>::CPB;
   const int nblk_d = (a.dim + CPB - 1) / CPB;
   const int b = blockIdx.x / nblk_d;
@@ -538,7 +603,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3) scan_fwd_kernel(const
   __shared__ int abort_flag;
   if (threadIdx.x == 0) abort_flag = 0;
   __syncthreads();
-  scan_group<T, NPAD, VEC, ZOH>(a, smem, threadIdx.x, b, d0, a.dim, 0, &abort_flag);
+  scan_group<T, NPAD, VEC, ZOH>(a, maps, smem, threadIdx.x, b, d0, a.dim, 0, &abort_flag);
 }
 
 // The balanced form: one CTA per SM holding kFusedGroups groups, each on a channel range (8 to 32
@@ -554,8 +619,8 @@ struct FusedPlan {
 
 template <typename T, int NPAD, bool VEC, bool ZOH>
 __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
-    scan_fwd_fused_kernel(const ScanArgs a, const FusedPlan plan) {
-  extern __shared__ __align__(16) unsigned char smem[];
+    scan_fwd_fused_kernel(const ScanArgs a, const __grid_constant__ TmaMaps maps, const FusedPlan plan) {
+  extern __shared__ __align__(128) unsigned char smem[];
   using Cfg = ScanCfg<T, NPAD>;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) abort_flag = 0;
@@ -565,7 +630,7 @@ __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
   const int nch = int(e & 15u) * 8;
   if (nch == 0) return;  // an empty group: its warps leave, the other groups do not wait on them
   const int b = int(e >> 16), d0 = int((e >> 4) & 0xfffu) * 8;
-  scan_group<T, NPAD, VEC, ZOH>(a, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0,
+  scan_group<T, NPAD, VEC, ZOH>(a, maps, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0,
                                 min(a.dim, d0 + nch), 5 * grp, &abort_flag);
 }
 
@@ -598,6 +663,69 @@ int make_fused_plan(const ScanArgs& a, int sms, FusedPlan& plan) {
     ctas = c + 1;
   }
   return (left == 0 && worst < plain_max) ? ctas : 0;
+}
+
+// The driver's tensor-map encoder, looked up once through the runtime (no link against the
+// driver library); null if the driver does not offer it.
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      p = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }();
+  return fn;
+}
+
+// One map of io type T over a tensor [rows][L] with boxes of box_rows rows.  pair == false: a 2-D
+// view [rows][L] with boxes of kChunk steps (steps and rows outside the tensor read as zeros).
+// pair == true (L a multiple of kChunk): a 3-D view [L / kChunk][rows][kChunk] (the chunk axis
+// strides kChunk elements, the row axis L), so that one box of two chunks lands chunk-major.
+// The 128-byte L2 promotion brings in whole lines of which a chunk reads part, so the next chunk
+// of the same rows finds them in L2.
+template <typename T>
+cudaError_t encode_map(CUtensorMap& m, const void* base, long long rows, int L, int box_rows, bool pair) {
+  const PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return cudaErrorNotSupported;
+  const CUtensorMapDataType dt = sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const cuuint32_t elem[3] = {1, 1, 1};
+  CUresult r;
+  if (pair) {
+    const cuuint64_t dims[3] = {cuuint64_t(kChunk), cuuint64_t(rows), cuuint64_t(L / kChunk)};
+    const cuuint64_t strides[2] = {cuuint64_t(L) * sizeof(T), cuuint64_t(kChunk) * sizeof(T)};
+    const cuuint32_t box[3] = {cuuint32_t(kChunk), cuuint32_t(box_rows), 2};
+    r = enc(&m, dt, 3, const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    const cuuint64_t dims[2] = {cuuint64_t(L), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(L) * sizeof(T)};
+    const cuuint32_t box[2] = {cuuint32_t(kChunk), cuuint32_t(box_rows)};
+    r = enc(&m, dt, 2, const_cast<void*>(base), dims, strides, box, elem, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The five maps of a call on the 16-byte path (rows 16-byte aligned, row counts below 2^31):
+// paired two-chunk copies when the io type is bf16 and the sequence a whole number of chunks,
+// else one chunk per copy.
+template <typename T, int NPAD>
+cudaError_t encode_maps(const ScanArgs& a, TmaMaps& m) {
+  const long long rows = (long long)a.batch * a.dim, brows = (long long)a.batch * a.dstate;
+  const int xr = ScanCfg<T, NPAD>::CPB;
+  for (int pair = ScanCfg<T, NPAD>::SLOTS == 2 && a.seqlen % kChunk == 0 ? 1 : 0; pair >= 0; --pair) {
+    const bool p = pair != 0;
+    m.pair = pair;
+    if (encode_map<T>(m.u, a.u, rows, a.seqlen, xr, p) == cudaSuccess &&
+        encode_map<T>(m.delta, a.delta, rows, a.seqlen, xr, p) == cudaSuccess &&
+        (!a.z || encode_map<T>(m.z, a.z, rows, a.seqlen, xr, p) == cudaSuccess) &&
+        encode_map<T>(m.B, a.B, brows, a.seqlen, NPAD, p) == cudaSuccess &&
+        encode_map<T>(m.C, a.C, brows, a.seqlen, NPAD, p) == cudaSuccess)
+      return cudaSuccess;
+  }
+  return cudaErrorInvalidValue;
 }
 
 // Once per device: the balanced kernel's shared-memory opt-in, and whether the build has the
@@ -642,7 +770,7 @@ int fused_ctas(const ScanArgs& a, FusedPlan& plan, int& dev, cudaError_t& err) {
 
 // Launches the balanced form when its plan applies; returns false when the plain kernel should run.
 template <typename T, int NPAD, bool VEC, bool ZOH>
-bool launch_fused(const ScanArgs& a, cudaStream_t stream, cudaError_t& err) {
+bool launch_fused(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, cudaError_t& err) {
   using Cfg = ScanCfg<T, NPAD>;
   FusedPlan plan;
   int dev = 0;
@@ -650,7 +778,8 @@ bool launch_fused(const ScanArgs& a, cudaStream_t stream, cudaError_t& err) {
   if (err != cudaSuccess) return true;
   if (ctas == 0) return false;
   ScanArgs args = a;
-  void* params[] = {&args, &plan};
+  TmaMaps m = maps;
+  void* params[] = {&args, &m, &plan};
   err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_fwd_fused_kernel<T, NPAD, VEC, ZOH>), dim3(unsigned(ctas)),
                          dim3(kFusedGroups * Cfg::NT), params, kFusedGroups * Cfg::kSmem, stream);
   return true;
@@ -659,9 +788,15 @@ bool launch_fused(const ScanArgs& a, cudaStream_t stream, cudaError_t& err) {
 template <typename T, int NPAD, bool VEC, bool ZOH>
 cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   using Cfg = ScanCfg<T, NPAD>;
+  TmaMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  if constexpr (VEC) {
+    // a shape the tensor-map encoder rejects runs the element-wise staging instead
+    if (encode_maps<T, NPAD>(a, maps) != cudaSuccess) return launch_cfg<T, NPAD, false, ZOH>(a, stream);
+  }
   {
     cudaError_t err = cudaSuccess;
-    if (launch_fused<T, NPAD, VEC, ZOH>(a, stream, err)) return err;
+    if (launch_fused<T, NPAD, VEC, ZOH>(a, maps, stream, err)) return err;
   }
   auto kernel = scan_fwd_kernel<T, NPAD, VEC, ZOH>;
   // The dynamic shared-memory opt-in is a per-device function attribute; set it once per device.
@@ -687,7 +822,7 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   if (nblk <= 0) return cudaSuccess;
   if (nblk > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   ScanArgs args = a;
-  void* params[] = {&args};
+  void* params[] = {&args, &maps};
   return cudaLaunchKernel(reinterpret_cast<const void*>(kernel), dim3(unsigned(nblk)), dim3(Cfg::NT), params,
                           Cfg::kSmem, stream);
 }
@@ -704,11 +839,13 @@ cudaError_t dispatch_disc(const ScanArgs& a, cudaStream_t stream) {
   return a.zoh ? dispatch_npad<T, VEC, true>(a, stream) : dispatch_npad<T, VEC, false>(a, stream);
 }
 
+// The 16-byte path: a non-empty sequence, every row 16-byte aligned (tensor copies in, vector
+// stores out), and row indices that fit the copies' signed 32-bit coordinates.
 template <typename T>
 bool rows_vectorisable(const ScanArgs& a) {
   auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  return (size_t(a.seqlen) * sizeof(T)) % 16 == 0 && al(a.u) && al(a.delta) && al(a.z) && al(a.B) && al(a.C) &&
-         al(a.y);
+  return a.seqlen > 0 && (size_t(a.seqlen) * sizeof(T)) % 16 == 0 && al(a.u) && al(a.delta) && al(a.z) && al(a.B) && al(a.C) &&
+         al(a.y) && (long long)a.batch * a.dim < (1LL << 31) && (long long)a.batch * a.dstate < (1LL << 31);
 }
 
 
