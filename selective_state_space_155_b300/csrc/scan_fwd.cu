@@ -486,6 +486,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   }
   T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L;
 
+#pragma unroll 2  // two chunks per iteration: more independent work for the scheduler around the hand-offs
   for (int k = 0; k < nchunks; ++k) {
     const int s = k & 1;
     const int t0 = k * kChunk;
@@ -503,7 +504,9 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
     const float2* Ps = tabPs(s);
     const float2* DS = tabDS(s);
 
-#pragma unroll 1
+    // both windows of the chunk unrolled: the first window's readout reduction and epilogue (a
+    // chain of dependent shuffles) then overlap the second window's loads and exponentials
+#pragma unroll
     for (int w = 0; w < kChunk; w += kWin) {
       float2 acc[kWin];
 #pragma unroll
