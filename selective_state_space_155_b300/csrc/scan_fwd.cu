@@ -486,7 +486,10 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   }
   T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L;
 
-#pragma unroll 2  // two chunks per iteration: more independent work for the scheduler around the hand-offs
+  // two chunks per iteration: more independent work for the scheduler around the hand-offs (not
+  // with the zero-order hold, whose longer step body would then outgrow the instruction cache)
+  constexpr int kChunkUnroll = ZOH ? 1 : 2;
+#pragma unroll kChunkUnroll
   for (int k = 0; k < nchunks; ++k) {
     const int s = k & 1;
     const int t0 = k * kChunk;
