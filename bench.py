@@ -464,9 +464,12 @@ def gpu_vs_oracle(w: wl.ScanWorkload, small: dict) -> dict:
     y_ref, s_ref = oracle.scan(small["u"], small["delta"], small["A"], small["B"], small["C"], small["D"], small["z"],
                                small["dt_bias"], delta_softplus=True)
     rel = lambda a, b: float(np.max(np.abs(a - b) / (1.0 + np.abs(b))))
+    big = np.abs(s_ref) > 1e-3
+    pure = float(np.max(np.abs(s0 - s_ref)[big] / np.abs(s_ref)[big])) if np.any(big) else 0.0
     return {"channels": f"batch row 0, channels 0..{n - 1}", "max_rel_err_y": rel(y0, y_ref),
             "max_rel_err_state": rel(s0, s_ref), "tolerance_y": 2e-2 if w.io == "bf16" else 1e-4,
-            "tolerance_state": 1e-4}
+            "tolerance_state": 1e-4,
+            "max_pure_rel_err_state": pure, "pure_rel_over": "|s_ref| > 1e-3", "tolerance_pure_rel_state": 1e-3}
 
 
 def cpu_baseline(w: wl.ScanWorkload, target_s: float = 25.0):

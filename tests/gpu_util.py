@@ -28,6 +28,27 @@ def assert_close(got, ref, tol, what):
     return err
 
 
+# Pure-relative bound on the final state where |s_ref| > STATE_REL_FLOOR.  The element-wise check
+# 1e-4 * (1 + |s_ref|) reads "final state within 1e-4 relative" with an absolute part for small
+# states; this one bounds |s - s_ref| / |s_ref| itself.  Measured on B300 over the tiny, small, mid
+# and ragged cases of both discretizations: at most 2.7e-4 (states whose sum over 2048 steps
+# cancels to a few 1e-3), 99.9th percentile 6e-5; the bound leaves ~4x headroom.
+STATE_REL_FLOOR = 1e-3
+STATE_REL_TOL = 1e-3
+
+
+def state_pure_rel(got, ref):
+    """max |got - ref| / |ref| over the elements with |ref| > STATE_REL_FLOOR (0 when there are none)."""
+    m = np.abs(ref) > STATE_REL_FLOOR
+    return float(np.max(np.abs(got - ref)[m] / np.abs(ref)[m])) if np.any(m) else 0.0
+
+
+def assert_state_rel(got, ref, what):
+    err = state_pure_rel(got, ref)
+    assert err <= STATE_REL_TOL, f"{what}: max |s-s_ref|/|s_ref| (|s_ref| > {STATE_REL_FLOOR}) = {err:.3e}"
+    return err
+
+
 def oracle_scan(inp, softplus=True, h0=None, zoh=False):
     f = wl.to_f64
     return oracle.scan(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), f(inp.get("D")),

@@ -4,8 +4,11 @@ through the C-ABI.
 Tolerances: the per-element gradients (du, ddelta, dz) are held element-wise like the forward's
 outputs (1e-4 relative for float32 io, 2e-2 for bf16 io, whose outputs are rounded to bf16).  The
 gradients that are sums over many terms of both signs (dA over batch and time, dB and dC over the
-channels, dD and ddt_bias, dh0) are float32 accumulations whose error scales with the size of
-the terms, not of the result, so they are held norm-wise: max|got - ref| <= 2e-4 * max(1, max|ref|).
+channels, dD and ddt_bias) are float32 accumulations whose error scales with the size of the terms,
+not of the result, so each element is held against the sum of the absolute values of its own terms
+(which the oracle returns beside the gradient): |got - ref| <= KAPPA * sum|terms|.  dh0, the
+adjoint state carried back to t = 0 rather than a sum, keeps the norm-wise form
+max|got - ref| <= 2e-4 * max(1, max|ref|).
 """
 import numpy as np
 import pytest
@@ -20,6 +23,27 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 f = wl.to_f64
 ELEMENTWISE = ("du", "ddelta", "dz")
+
+
+# Per-element bound for the summed gradients, relative to the element's absolute-term sum.  A
+# float32 sum of n terms can be off by up to n * 2^-24 of that sum in the worst case (above 1e-4 for
+# n > 1700, i.e. for every workload here), but the kernel adds at most 32 partials in registers
+# before a float32 atomic across CTAs, so the realized error stays near sqrt(n) * 2^-24; with the
+# forward recomputation's approximate exponentials (a few units in the last place per term) the
+# largest ratio measured on B300 over all cases of this file is 4.2e-6.  KAPPA leaves ~25x headroom.
+KAPPA = 1e-4
+SUMMED = ("dA", "dB", "dC", "dD", "ddt_bias")
+
+
+def term_close(got, ref, abs_sum, what):
+    assert np.all(np.isfinite(got)), f"{what}: non-finite values"
+    err = np.abs(got - ref)
+    bound = KAPPA * abs_sum
+    bad = err > bound
+    if np.any(bad):
+        i = int(np.argmax(err / np.maximum(abs_sum, 1e-300)))
+        raise AssertionError(f"{what}: {int(bad.sum())} elements with |got-ref| > {KAPPA:.0e} * sum|terms|; "
+                             f"worst |got-ref| = {err.flat[i]:.3e}, sum|terms| = {abs_sum.flat[i]:.3e}")
 
 
 def norm_close(got, ref, tol, what):
@@ -50,14 +74,18 @@ def check_bwd(inp, softplus=True, h0=None, seed=0, what="", disc="delta_b"):
     y, last, ck, g = train_step(inp, dout, softplus, h0, need_dh0=h0 is not None, disc=disc)
     ref = oracle.scan_bwd(f(inp["u"]), f(inp["delta"]), f(inp["A"]), f(inp["B"]), f(inp["C"]), f(dout),
                           D=f(inp.get("D")), z=f(inp.get("z")), dt_bias=f(inp.get("dt_bias")),
-                          delta_softplus=softplus, h0=f(h0) if h0 is not None else None, zoh=disc == "zoh")
-    assert set(ref) <= set(g) | ({"dh0"} if h0 is None else set()), (sorted(ref), sorted(g))
-    for k, r in ref.items():
-        if k == "dh0" and h0 is None:
+                          delta_softplus=softplus, h0=f(h0) if h0 is not None else None, zoh=disc == "zoh",
+                          abs_sums=True)
+    grads = {k: v for k, v in ref.items() if not k.startswith("abs_")}
+    assert set(grads) <= set(g) | ({"dh0"} if h0 is None else set()), (sorted(grads), sorted(g))
+    for k, r in grads.items():
+        if r is None or (k == "dh0" and h0 is None):
             continue
         got = f(g[k])
         if k in ELEMENTWISE:
             assert_close(got, r, TOL[io][0], f"{what} {k}")
+        elif k in SUMMED:
+            term_close(got, r, ref["abs_" + k], f"{what} {k}")
         else:
             norm_close(got, r, 2e-4, f"{what} {k}")
     return y, last, ck

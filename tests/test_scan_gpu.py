@@ -5,7 +5,7 @@ import torch
 
 import selective_state_space_155_b300 as ssm
 import ssm_workloads as wl
-from tests.gpu_util import TOL, assert_close, io_name, oracle_scan, to_device
+from tests.gpu_util import assert_state_rel, TOL, assert_close, io_name, oracle_scan, to_device
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
@@ -36,6 +36,7 @@ def check_case(inp, softplus=True, h0=None, what=""):
     y_ref, s_ref = oracle_scan(inp, softplus, h0)
     ey = assert_close(y, y_ref, ty, f"{what} y")
     es = assert_close(last, s_ref, ts, f"{what} last_state")
+    assert_state_rel(last, s_ref, f"{what} last_state")
     return ey, es
 
 
