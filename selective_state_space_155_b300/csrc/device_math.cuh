@@ -165,30 +165,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
 
 // Exact zero-order hold: Bbar = (exp(Delta a) - 1) / a * B for a diagonal A.  This returns the
 // factor Bbar / B from x = Delta*a, abar = exp(x) (already computed by the caller), Delta and
-// inv_a = 1/a.  For |x| >= 1/8 it is (abar - 1) * inv_a, which loses at most a few units in
-// the sixth digit to the rounding of abar.  Below that, abar - 1 would cancel, so it is
-// Delta * (e^x - 1)/x from the Taylor series 1 + x/2 + x^2/6 + ... + x^5/720, whose first
-// omitted term is under 1e-9 relative there; this branch also covers a = 0, where the factor
-// is its limit Delta and inv_a is never used.
+// inv_a = 1/a.  For |x| >= 1/16 it is (abar - 1) * inv_a: abar carries a relative error of a few
+// 2^-23, which against |abar - 1| >= 1 - e^(-1/16) = 0.06 costs at most a few units in the
+// sixth digit.  Below that, abar - 1 would cancel, so it is Delta * (e^x - 1)/x from the Taylor
+// series 1 + x/2 + x^2/6 + x^3/24, whose first omitted term x^4/120 is under 1.3e-7 relative
+// there; this branch also covers a = 0, where the factor is its limit Delta and inv_a is never
+// used.
 __device__ __forceinline__ float zoh_factor(float x, float abar, float delta, float inv_a) {
-  float p = fmaf(x, 1.0f / 720.0f, 1.0f / 120.0f);
-  p = fmaf(x, p, 1.0f / 24.0f);
-  p = fmaf(x, p, 1.0f / 6.0f);
+  float p = fmaf(x, 1.0f / 24.0f, 1.0f / 6.0f);
   p = fmaf(x, p, 0.5f);
   p = fmaf(x, p, 1.0f);
-  return fabsf(x) < 0.125f ? delta * p : (abar - 1.0f) * inv_a;
+  return fabsf(x) < 0.0625f ? delta * p : (abar - 1.0f) * inv_a;
 }
-
 // zoh_factor on a pair of states with packed arithmetic.
 __device__ __forceinline__ float2 zoh_factor2(float2 x, float2 abar, float2 delta, float2 inv_a) {
-  float2 p = __ffma2_rn(x, make_float2(1.0f / 720.0f, 1.0f / 720.0f), make_float2(1.0f / 120.0f, 1.0f / 120.0f));
-  p = __ffma2_rn(x, p, make_float2(1.0f / 24.0f, 1.0f / 24.0f));
-  p = __ffma2_rn(x, p, make_float2(1.0f / 6.0f, 1.0f / 6.0f));
+  float2 p = __ffma2_rn(x, make_float2(1.0f / 24.0f, 1.0f / 24.0f), make_float2(1.0f / 6.0f, 1.0f / 6.0f));
   p = __ffma2_rn(x, p, make_float2(0.5f, 0.5f));
   p = __ffma2_rn(x, p, make_float2(1.0f, 1.0f));
   p = __fmul2_rn(p, delta);
   const float2 q = __fmul2_rn(__fadd2_rn(abar, make_float2(-1.0f, -1.0f)), inv_a);
-  return make_float2(fabsf(x.x) < 0.125f ? p.x : q.x, fabsf(x.y) < 0.125f ? p.y : q.y);
+  return make_float2(fabsf(x.x) < 0.0625f ? p.x : q.x, fabsf(x.y) < 0.0625f ? p.y : q.y);
 }
 
 // d(Bbar/B)/da of the zero-order hold, for the backward pass: with c = zoh_factor(...),

@@ -2,7 +2,7 @@
 with SSM_DISC_ZOH) against the float64 oracle, through the C-ABI.
 
 Bbar = (exp(Delta A) - 1) / A * B: the kernels evaluate it from the exponential they already
-have where |Delta A| >= 1/8 and from a short series below that; the cases here put states on
+have where |Delta A| >= 1/16 and from a short series below that; the cases here put states on
 both sides of that threshold, at A = 0, and at the workload sizes."""
 import numpy as np
 import pytest
