@@ -186,6 +186,19 @@ __device__ __forceinline__ float2 zoh_factor2(float2 x, float2 abar, float2 delt
   const float2 q = __fmul2_rn(__fadd2_rn(abar, make_float2(-1.0f, -1.0f)), inv_a);
   return make_float2(fabsf(x.x) < 0.0625f ? p.x : q.x, fabsf(x.y) < 0.0625f ? p.y : q.y);
 }
+// zoh_factor2 from the base-2 exponent g = x / ln 2 that the recurrence already has (abar =
+// 2^g): the same series and switch point, with the powers of ln 2 folded into the coefficients.
+__device__ __forceinline__ float2 zoh_factor2_log2(float2 g, float2 abar, float2 delta, float2 inv_a) {
+  constexpr double ln2 = 0.6931471805599453;
+  constexpr float c1 = float(ln2 / 2), c2 = float(ln2 * ln2 / 6), c3 = float(ln2 * ln2 * ln2 / 24);
+  constexpr float gmax = float(0.0625 / ln2);
+  float2 p = __ffma2_rn(g, make_float2(c3, c3), make_float2(c2, c2));
+  p = __ffma2_rn(g, p, make_float2(c1, c1));
+  p = __ffma2_rn(g, p, make_float2(1.0f, 1.0f));
+  p = __fmul2_rn(p, delta);
+  const float2 q = __fmul2_rn(__fadd2_rn(abar, make_float2(-1.0f, -1.0f)), inv_a);
+  return make_float2(fabsf(g.x) < gmax ? p.x : q.x, fabsf(g.y) < gmax ? p.y : q.y);
+}
 
 // d(Bbar/B)/da of the zero-order hold, for the backward pass: with c = zoh_factor(...),
 // dc/da = (Delta abar - c) / a = Delta^2 phi(x), phi(x) = (x e^x - e^x + 1) / x^2.  For |x| >= 1/2

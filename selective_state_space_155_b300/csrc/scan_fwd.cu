@@ -523,10 +523,9 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
         const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y));
         const float2 a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
         if constexpr (ZOH) {
-          // p.y is u here; Bbar*u = zoh_factor(Delta*A) * u * B
-          const float2 ln2 = f2(kLn2, kLn2);
-          const float2 c01 = zoh_factor2(__fmul2_rn(g01, ln2), a01, dd, iA01);
-          const float2 c23 = zoh_factor2(__fmul2_rn(g23, ln2), a23, dd, iA23);
+          // p.y is u here; Bbar*u = zoh_factor(Delta*A) * u * B, from the base-2 exponent g
+          const float2 c01 = zoh_factor2_log2(g01, a01, dd, iA01);
+          const float2 c23 = zoh_factor2_log2(g23, a23, dd, iA23);
           h01 = __ffma2_rn(a01, h01, __fmul2_rn(c01, __fmul2_rn(uu, f2(bb.x, bb.y))));
           h23 = __ffma2_rn(a23, h23, __fmul2_rn(c23, __fmul2_rn(uu, f2(bb.z, bb.w))));
         } else {
