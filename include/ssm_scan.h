@@ -86,7 +86,8 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
  */
 typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization;
 
-/* Version of this ABI (bumped when a signature changes or an entry point is added): 5. */
+/* Version of this ABI (bumped when a signature changes, an entry point is added or a layout
+ * changes): 6. */
 int ssm_abi_version(void);
 
 /*
@@ -144,13 +145,16 @@ int ssm_scan_fwd_form(int batch, int dim, int dstate, int seqlen, int io_dtype, 
 
 /*
  * Training forward: ssm_scan_fwd_h0 (Delta*B discretization) that also stores, for the backward
- * pass, the state at the start of every chunk of SSM_SCAN_CHECKPOINT_STEPS steps:
- *   checkpoints : [batch][nchunks][dim][dstate] float32, nchunks = ssm_scan_num_checkpoints(seqlen);
- *                 chunk c holds h_{c*SSM_SCAN_CHECKPOINT_STEPS - 1} (h0, or zero, for c = 0).
+ * pass, the state before every SSM_SCAN_CHECKPOINT_STEPS-th step:
+ *   checkpoints : [batch][ncheck][dim][dstate] float32, ncheck = ssm_scan_num_checkpoints(seqlen)
+ *                 = ceil(seqlen / SSM_SCAN_CHECKPOINT_STEPS); checkpoint c holds
+ *                 h_{c*SSM_SCAN_CHECKPOINT_STEPS - 1} (h0, or zero, for c = 0).  (8 bytes per
+ *                 (batch, channel, step) for dstate 16: the backward restarts every 8-step
+ *                 register sub-chunk from its checkpoint instead of recomputing the chunk.)
  * Required: checkpoints, plus what ssm_scan_fwd_h0 requires.  The lane-per-channel form is not
  * used for this call.  Returns an ssm_status.
  */
-#define SSM_SCAN_CHECKPOINT_STEPS 32
+#define SSM_SCAN_CHECKPOINT_STEPS 8
 int ssm_scan_num_checkpoints(int seqlen);
 int ssm_scan_fwd_train(const void* u, const void* delta, const float* A, const void* B, const void* C,
                        const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,

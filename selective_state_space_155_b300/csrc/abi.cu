@@ -23,7 +23,7 @@ bool overlaps(const void* p, size_t np, const void* q, size_t nq) {
 
 extern "C" {
 
-int ssm_abi_version(void) { return 5; }
+int ssm_abi_version(void) { return 6; }
 
 const char* ssm_status_string(int status) {
   switch (status) {
@@ -72,7 +72,7 @@ int scan_fwd_common(const void* u, const void* delta, const float* A, const void
       overlaps(y, ny, C, nbc))
     return SSM_ERR_ARG;
   if (ckpt) {
-    const size_t nck = size_t(batch) * ((seqlen + 31) / 32) * dim * dstate * 4;
+    const size_t nck = size_t(batch) * ssm_scan_num_checkpoints(seqlen) * dim * dstate * 4;
     if (overlaps(ckpt, nck, y, ny) || overlaps(ckpt, nck, last_state, nst) || overlaps(ckpt, nck, h0, nst) ||
         overlaps(ckpt, nck, u, ny) || overlaps(ckpt, nck, delta, ny))
       return SSM_ERR_ARG;
@@ -110,7 +110,7 @@ int ssm_scan_fwd_train_ex(const void* u, const void* delta, const float* A, cons
                           const float* D, const void* z, const float* dt_bias, int delta_softplus, const float* h0,
                           void* y, float* last_state, float* checkpoints, int batch, int dim, int dstate, int seqlen,
                           int io_dtype, int discretization, void* stream) {
-  static_assert(SSM_SCAN_CHECKPOINT_STEPS == ssm::kScanChunk, "checkpoint interval");
+  static_assert(SSM_SCAN_CHECKPOINT_STEPS == ssm::kCkptSteps, "checkpoint interval");
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
   if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;

@@ -46,11 +46,14 @@ struct ScanArgs {
   int softplus;
   int io;
   int zoh;      // exact zero-order-hold Bbar instead of Delta * B
-  float* ckpt;  // nullable: the state at the start of every kScanChunk-step chunk, for the backward
+  float* ckpt;  // nullable: the state at the start of every kCkptSteps steps, for the backward
 };
 
-// Steps per chunk of the scan kernels; the forward's checkpoints are kScanChunk steps apart.
+// Steps per chunk of the scan kernels, and the interval of the training forward's checkpoints
+// (the backward's register sub-chunk: it restarts each sub-chunk from its checkpoint).
 constexpr int kScanChunk = 32;
+constexpr int kCkptSteps = 8;
+static_assert(kScanChunk % kCkptSteps == 0 && kCkptSteps % 8 == 0, "checkpoints at sub-window boundaries");
 
 // Arguments of one backward pass of the scan; meaning as in ssm_scan.h.
 struct ScanBwdArgs {

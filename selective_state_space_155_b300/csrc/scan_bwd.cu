@@ -19,11 +19,10 @@
 // 32 steps are processed last to first.  For each chunk all 128 threads stage the per-(channel,
 // step) values (Delta, u, dy, the softplus and silu derivatives) and B, C into shared-memory
 // tables from raw input rows that were copied into shared memory (16-byte cp.async when rows are
-// 16-byte aligned) while the previous chunk was being computed;
-// then every lane recomputes the chunk forward from the state the forward pass checkpointed at
-// its start, keeping the state at the start of each 8-step sub-chunk, and walks the sub-chunks
-// last to first: it recomputes the sub-chunk's 8 states and decay factors into registers and
-// runs the adjoint recurrence backwards over them.  Sums over a channel's 4 lanes take two
+// 16-byte aligned) while the previous chunk was being computed, together with the four states the
+// training forward checkpointed at the chunk's 8-step sub-chunk starts; then every lane walks the
+// sub-chunks last to first: from the sub-chunk's checkpoint it recomputes the 8 states (and the
+// readout y that dz needs) into registers, and runs the adjoint recurrence backwards over them.  Sums over a channel's 4 lanes take two
 // shuffles (y) or two shuffles for the du and dDelta sums together (a reduce-scatter that leaves
 // one of them on each lane); dB and dC, shared by all channels, are reduce-scattered over the 8
 // channels of a warp by shuffles; a step's sums wait in registers until its sub-chunk ends, are
@@ -44,9 +43,10 @@ namespace {
 
 __device__ __forceinline__ float2 f2(float x, float y) { return make_float2(x, y); }
 
-constexpr int kK = kScanChunk;  // steps per chunk (the forward's checkpoint interval)
-constexpr int kS = 8;           // steps per register sub-chunk
+constexpr int kK = kScanChunk;  // steps per chunk
+constexpr int kS = kCkptSteps;  // steps per register sub-chunk (the forward's checkpoint interval)
 constexpr int kSub = kK / kS;
+static_assert(kS == 8, "the adjoint's deferred sums are sized for 8-step sub-chunks");
 constexpr int kCPB = 32;        // channels per CTA
 constexpr int kThr = 128;       // four warps; four lanes per channel, four states per lane
 constexpr int kTS = kK + 1;     // padded row stride of the per-(channel, step) tables
@@ -73,9 +73,9 @@ struct __align__(16) BwdRaw {
   static constexpr int kEPV = 16 / int(sizeof(T));  // elements per 16-byte copy
   static constexpr int kPPR = kK / kEPV;            // 16-byte copies per 32-step row
   static constexpr int kRSBC = kK + kEPV;           // B/C row stride, padded against bank conflicts
-  T x[4][kCPB][kK];    // u, delta, z, dout
-  T bc[2][16][kRSBC];  // B, C
-  float ck[kCPB][16];  // the state at the chunk's start
+  T x[4][kCPB][kK];          // u, delta, z, dout
+  T bc[2][16][kRSBC];        // B, C
+  float ck[kSub][kCPB][16];  // the states at the chunk's sub-chunk starts
 };
 
 template <typename T>
@@ -94,7 +94,8 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
   const int nblk_d = (dim + kCPB - 1) / kCPB;
   const int b = blockIdx.x / nblk_d;
   const int d0 = (blockIdx.x % nblk_d) * kCPB;
-  const int nck = (L + kK - 1) / kK;
+  const int nchunks = (L + kK - 1) / kK;
+  const int nck = (L + kS - 1) / kS;  // checkpoints per batch row
   const T* gu_ = static_cast<const T*>(a.u);
   const T* gdl = static_cast<const T*>(a.delta);
   const T* gz = static_cast<const T*>(a.z);
@@ -183,22 +184,27 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
         if (n < N && tg < L) raw.bc[which][n][t] = (which ? gC : gB)[(size_t(b) * N + n) * L + tg];
       }
     }
-    const float* ck = a.ckpt + (size_t(b) * nck + k) * dim * size_t(N);
-    if (ck_vec) {
-      // one 16-byte copy per (channel, 4 states): 32 x 4 = kThr copies
-      const int c = tid >> 2, q = tid & 3;
-      if (d0 + c < dim && 4 * q < N) cp_async_16(&raw.ck[c][4 * q], ck + size_t(d0 + c) * N + 4 * q, 16);
-    } else {
-      for (int e = tid; e < kCPB * 16; e += kThr) {
-        const int c = e >> 4, n = e & 15;
-        if (d0 + c < dim && n < N) raw.ck[c][n] = ck[size_t(d0 + c) * N + n];
+#pragma unroll
+    for (int sb = 0; sb < kSub; ++sb) {
+      const int ci = k * kSub + sb;  // checkpoint index; sub-chunks past the sequence have none
+      if (ci >= nck) continue;
+      const float* ck = a.ckpt + (size_t(b) * nck + ci) * dim * size_t(N);
+      if (ck_vec) {
+        // one 16-byte copy per (channel, 4 states): 32 x 4 = kThr copies
+        const int c = tid >> 2, q = tid & 3;
+        if (d0 + c < dim && 4 * q < N) cp_async_16(&raw.ck[sb][c][4 * q], ck + size_t(d0 + c) * N + 4 * q, 16);
+      } else {
+        for (int e = tid; e < kCPB * 16; e += kThr) {
+          const int c = e >> 4, n = e & 15;
+          if (d0 + c < dim && n < N) raw.ck[sb][c][n] = ck[size_t(d0 + c) * N + n];
+        }
       }
     }
     cp_async_commit();
   };
-  issue(nck - 1);
+  issue(nchunks - 1);
 
-  for (int k = nck - 1; k >= 0; --k) {
+  for (int k = nchunks - 1; k >= 0; --k) {
     const int t0 = k * kK;
     cp_async_wait<0>();  // this thread's copies of chunk k have landed
     __syncthreads();     // everyone's have, and the previous chunk is finished with every table
@@ -240,46 +246,18 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
       }
     }
     for (int e = tid; e < kK * 2 * 16; e += kThr) (&sm.acc[0][0][0])[e] = 0.0f;
-    float ck0[4];
-    {
-      const float4 c4 = *reinterpret_cast<const float4*>(&raw.ck[cl][4 * g]);  // conflict-free
-      const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+    // the sub-chunks' starting states, from the checkpoints (zero past the sequence's end)
+    float hs[kSub][4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ck0[i] = (ch_ok && 4 * g + i < N) ? cv[i] : 0.0f;
+    for (int sb = 0; sb < kSub; ++sb) {
+      const float4 c4 = *reinterpret_cast<const float4*>(&raw.ck[sb][cl][4 * g]);  // conflict-free
+      const float cv[4] = {c4.x, c4.y, c4.z, c4.w};
+      const bool in = ch_ok && t0 + sb * kS < L;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hs[sb][i] = (in && 4 * g + i < N) ? cv[i] : 0.0f;
     }
     __syncthreads();     // tables written; the raw rows are free
     if (k > 0) issue(k - 1);  // in flight while this chunk is computed
-
-    // ---- recurrence role: forward recompute of the chunk, keeping each sub-chunk's start ----
-    float hs[kSub][4];
-    {
-      float h[4] = {ck0[0], ck0[1], ck0[2], ck0[3]};
-#pragma unroll
-      for (int sb = 0; sb < kSub; ++sb) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) hs[sb][i] = h[i];
-#pragma unroll
-        for (int j = 0; j < kS; ++j) {
-          const int t = sb * kS + j;
-          const float dl = sm.dl[cl][t], du = ZOH ? sm.uu[cl][t] : dl * sm.uu[cl][t];
-          const float4 bb = *reinterpret_cast<const float4*>(&sm.Bs[t][4 * g]);
-          const float4 cc = *reinterpret_cast<const float4*>(&sm.Cs[t][4 * g]);
-          const float2 dl2 = f2(dl, dl), du2 = f2(du, du);
-          const float2 g01 = __fmul2_rn(dl2, f2(An2[0], An2[1])), g23 = __fmul2_rn(dl2, f2(An2[2], An2[3]));
-          const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y)), a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
-          const float2 h01 = __ffma2_rn(a01, f2(h[0], h[1]), bbar_u(dl2, g01, a01, 0, __fmul2_rn(du2, f2(bb.x, bb.y))));
-          const float2 h23 = __ffma2_rn(a23, f2(h[2], h[3]), bbar_u(dl2, g23, a23, 1, __fmul2_rn(du2, f2(bb.z, bb.w))));
-          h[0] = h01.x, h[1] = h01.y, h[2] = h23.x, h[3] = h23.y;
-          const float2 yp2 = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
-          float yp = yp2.x + yp2.y;
-          if (has_z) {
-            yp += __shfl_xor_sync(0xffffffffu, yp, 8);
-            yp += __shfl_xor_sync(0xffffffffu, yp, 16);
-            if (g == 0) sm.yv[cl][t] = yp;
-          }
-        }
-      }
-    }
 
     // ---- recurrence role: sub-chunks last to first, adjoint recurrence backwards ----
     const int k1 = (cw >> 2) & 1, k2 = (cw >> 1) & 1, k3 = cw & 1;
@@ -299,6 +277,14 @@ __global__ void __launch_bounds__(kThr, 3) scan_bwd_kernel(const ScanBwdArgs a) 
           h01 = __ffma2_rn(a01, h01, bbar_u(dl2, g01, a01, 0, __fmul2_rn(du2, f2(bb.x, bb.y))));
           h23 = __ffma2_rn(a23, h23, bbar_u(dl2, g23, a23, 1, __fmul2_rn(du2, f2(bb.z, bb.w))));
           ht[j][0] = h01, ht[j][1] = h23;
+          if (has_z) {  // y before the gate, for dz: the readout summed over the channel's 4 lanes
+            const float4 cc = *reinterpret_cast<const float4*>(&sm.Cs[t][4 * g]);
+            const float2 yp2 = __ffma2_rn(f2(cc.z, cc.w), h23, __fmul2_rn(f2(cc.x, cc.y), h01));
+            float yp = yp2.x + yp2.y;
+            yp += __shfl_xor_sync(0xffffffffu, yp, 8);
+            yp += __shfl_xor_sync(0xffffffffu, yp, 16);
+            if (g == 0) sm.yv[cl][t] = yp;
+          }
         }
       }
       // Each step's dB/dC sum (and, in the Delta*B form, its du/dDelta sums) is kept in registers

@@ -206,7 +206,7 @@ __device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) 
 // most CPB of them, with its own shared-memory block `smem` (mbarriers included) and the named
 // barriers bar0 + 1 .. bar0 + 5; tid is the thread's index within the group, abort the CTA's
 // give-up flag.  A CTA of the plain kernel is one group.
-template <typename T, int NPAD, bool VEC, bool ZOH>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& maps, unsigned char* smem, const int tid,
                                            const int b, const int d0, const int dlim, const int bar0,
                                            volatile int* abort) {
@@ -489,18 +489,32 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   // two chunks per iteration: more independent work for the scheduler around the hand-offs (not
   // with the zero-order hold, whose longer step body would then outgrow the instruction cache)
   constexpr int kChunkUnroll = ZOH ? 1 : 2;
+  // checkpoints for the backward pass, [batch][ceil(L / kCkptSteps)][dim][dstate]: the state
+  // before every kCkptSteps-th step (null when not requested, or for a lane without a channel)
+  const int nck = (L + kCkptSteps - 1) / kCkptSteps;
+  float* const ckrow = (CK && ch_ok) ? a.ckpt + (size_t(b) * nck * a.dim + d) * N + 4 * g : nullptr;
+  const size_t ckstride = size_t(a.dim) * N;  // between consecutive checkpoints of this channel
+  const int nst = min(4, N - 4 * g);          // this lane's real states
+  // one 16-byte store per lane when its four states are real and the rows 16-byte aligned
+  const bool ck16 = CK && nst == 4 && N % 4 == 0 && (reinterpret_cast<uintptr_t>(a.ckpt) & 15u) == 0;
+  auto checkpoint = [&](int tg) {
+    if (ckrow != nullptr && tg < L) {
+      float* cp = ckrow + size_t(tg / kCkptSteps) * ckstride;
+      if (ck16) {
+        *reinterpret_cast<float4*>(cp) = make_float4(h01.x, h01.y, h23.x, h23.y);
+      } else {
+        const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (i < nst) cp[i] = hv[i];
+      }
+    }
+  };
+
 #pragma unroll kChunkUnroll
   for (int k = 0; k < nchunks; ++k) {
     const int s = k & 1;
     const int t0 = k * kChunk;
-    if (a.ckpt && ch_ok) {
-      // the state at the start of chunk k, for the backward pass: [batch][chunk][dim][dstate]
-      float* cp = a.ckpt + ((size_t(b) * nchunks + k) * a.dim + d) * N;
-      const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (4 * g + i < N) cp[4 * g + i] = hv[i];
-    }
     mbar_wait(&mb[s], (k >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kRecBackoff);
     const float* Bs = tabBs(s);
     const float* Cs = tabCs(s);
@@ -515,6 +529,9 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
 #pragma unroll
       for (int j = 0; j < kWin; ++j) {
         const int t = w + j;
+        if constexpr (CK) {
+          if (j % kCkptSteps == 0) checkpoint(t0 + t);
+        }
         const float2 p = Ps[cl * PSS + t];
         const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
         const float4 cc = *reinterpret_cast<const float4*>(Cs + t * NPAD + 4 * g);
@@ -597,7 +614,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
 
 // The plain kernel: CTA blockIdx.x scans 32-channel block (blockIdx.x % blocks per row) of batch
 // row blockIdx.x / blocks per row.
-template <typename T, int NPAD, bool VEC, bool ZOH>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3)
     scan_fwd_kernel(const ScanArgs a, const __grid_constant__ TmaMaps maps) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -608,7 +625,7 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3)
   __shared__ int abort_flag;
   if (threadIdx.x == 0) abort_flag = 0;
   __syncthreads();
-  scan_group<T, NPAD, VEC, ZOH>(a, maps, smem, threadIdx.x, b, d0, a.dim, 0, &abort_flag);
+  scan_group<T, NPAD, VEC, ZOH, CK>(a, maps, smem, threadIdx.x, b, d0, a.dim, 0, &abort_flag);
 }
 
 // The balanced form: one CTA per SM holding kFusedGroups groups, each on a channel range (8 to 32
@@ -622,7 +639,7 @@ struct FusedPlan {
   uint32_t e[kFusedGroups * kMaxFusedCtas];
 };
 
-template <typename T, int NPAD, bool VEC, bool ZOH>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
     scan_fwd_fused_kernel(const ScanArgs a, const __grid_constant__ TmaMaps maps, const FusedPlan plan) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -635,7 +652,7 @@ __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
   const int nch = int(e & 15u) * 8;
   if (nch == 0) return;  // an empty group: its warps leave, the other groups do not wait on them
   const int b = int(e >> 16), d0 = int((e >> 4) & 0xfffu) * 8;
-  scan_group<T, NPAD, VEC, ZOH>(a, maps, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0,
+  scan_group<T, NPAD, VEC, ZOH, CK>(a, maps, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0,
                                 min(a.dim, d0 + nch), 5 * grp, &abort_flag);
 }
 
@@ -736,10 +753,10 @@ cudaError_t encode_maps(const ScanArgs& a, TmaMaps& m) {
 // Once per device: the balanced kernel's shared-memory opt-in, and whether the build has the
 // register count its setmaxnreg split was sized for (if not, the plain kernel runs).  Returns
 // whether the balanced kernel may launch; err reports a failing CUDA call.
-template <typename T, int NPAD, bool VEC, bool ZOH>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 bool fused_ready(int dev, cudaError_t& err) {
   using Cfg = ScanCfg<T, NPAD>;
-  auto kernel = scan_fwd_fused_kernel<T, NPAD, VEC, ZOH>;
+  auto kernel = scan_fwd_fused_kernel<T, NPAD, VEC, ZOH, CK>;
   constexpr size_t kSmem = kFusedGroups * Cfg::kSmem;
   static std::atomic<uint64_t> configured{0}, usable{0};
   const uint64_t bit = uint64_t(1) << (dev & 63);
@@ -757,7 +774,7 @@ bool fused_ready(int dev, cudaError_t& err) {
 // CTAs of the balanced form for `a` (bf16, dstate 9..16: three groups' shared memory fit one CTA),
 // or 0 when the plain kernel runs instead (no plan, SSM_SCAN_VARIANT=quad_plain, or a build
 // whose register count does not match the split).
-template <typename T, int NPAD, bool VEC, bool ZOH>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 int fused_ctas(const ScanArgs& a, FusedPlan& plan, int& dev, cudaError_t& err) {
   if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
     return 0;
@@ -769,41 +786,41 @@ int fused_ctas(const ScanArgs& a, FusedPlan& plan, int& dev, cudaError_t& err) {
     if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
     const int ctas = make_fused_plan(a, sms, plan);
     if (ctas == 0) return 0;
-    return fused_ready<T, NPAD, VEC, ZOH>(dev, err) ? ctas : 0;
+    return fused_ready<T, NPAD, VEC, ZOH, CK>(dev, err) ? ctas : 0;
   }
 }
 
 // Launches the balanced form when its plan applies; returns false when the plain kernel should run.
-template <typename T, int NPAD, bool VEC, bool ZOH>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 bool launch_fused(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, cudaError_t& err) {
   using Cfg = ScanCfg<T, NPAD>;
   FusedPlan plan;
   int dev = 0;
-  const int ctas = fused_ctas<T, NPAD, VEC, ZOH>(a, plan, dev, err);
+  const int ctas = fused_ctas<T, NPAD, VEC, ZOH, CK>(a, plan, dev, err);
   if (err != cudaSuccess) return true;
   if (ctas == 0) return false;
   ScanArgs args = a;
   TmaMaps m = maps;
   void* params[] = {&args, &m, &plan};
-  err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_fwd_fused_kernel<T, NPAD, VEC, ZOH>), dim3(unsigned(ctas)),
+  err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_fwd_fused_kernel<T, NPAD, VEC, ZOH, CK>), dim3(unsigned(ctas)),
                          dim3(kFusedGroups * Cfg::NT), params, kFusedGroups * Cfg::kSmem, stream);
   return true;
 }
 
-template <typename T, int NPAD, bool VEC, bool ZOH>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   using Cfg = ScanCfg<T, NPAD>;
   TmaMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   if constexpr (VEC) {
     // a shape the tensor-map encoder rejects runs the element-wise staging instead
-    if (encode_maps<T, NPAD>(a, maps) != cudaSuccess) return launch_cfg<T, NPAD, false, ZOH>(a, stream);
+    if (encode_maps<T, NPAD>(a, maps) != cudaSuccess) return launch_cfg<T, NPAD, false, ZOH, CK>(a, stream);
   }
   {
     cudaError_t err = cudaSuccess;
-    if (launch_fused<T, NPAD, VEC, ZOH>(a, maps, stream, err)) return err;
+    if (launch_fused<T, NPAD, VEC, ZOH, CK>(a, maps, stream, err)) return err;
   }
-  auto kernel = scan_fwd_kernel<T, NPAD, VEC, ZOH>;
+  auto kernel = scan_fwd_kernel<T, NPAD, VEC, ZOH, CK>;
   // The dynamic shared-memory opt-in is a per-device function attribute; set it once per device.
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -832,16 +849,19 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
                           Cfg::kSmem, stream);
 }
 
-template <typename T, bool VEC, bool ZOH>
+template <typename T, bool VEC, bool ZOH, bool CK>
 cudaError_t dispatch_npad(const ScanArgs& a, cudaStream_t stream) {
-  if (a.dstate <= 4) return launch_cfg<T, 4, VEC, ZOH>(a, stream);
-  if (a.dstate <= 8) return launch_cfg<T, 8, VEC, ZOH>(a, stream);
-  return launch_cfg<T, 16, VEC, ZOH>(a, stream);
+  if (a.dstate <= 4) return launch_cfg<T, 4, VEC, ZOH, CK>(a, stream);
+  if (a.dstate <= 8) return launch_cfg<T, 8, VEC, ZOH, CK>(a, stream);
+  return launch_cfg<T, 16, VEC, ZOH, CK>(a, stream);
 }
 
+// The training forward (checkpoints requested) is its own instantiation, so that the inference
+// kernels carry no checkpoint code in their unrolled windows.
 template <typename T, bool VEC>
 cudaError_t dispatch_disc(const ScanArgs& a, cudaStream_t stream) {
-  return a.zoh ? dispatch_npad<T, VEC, true>(a, stream) : dispatch_npad<T, VEC, false>(a, stream);
+  if (a.ckpt) return a.zoh ? dispatch_npad<T, VEC, true, true>(a, stream) : dispatch_npad<T, VEC, false, true>(a, stream);
+  return a.zoh ? dispatch_npad<T, VEC, true, false>(a, stream) : dispatch_npad<T, VEC, false, false>(a, stream);
 }
 
 // The 16-byte path: a non-empty sequence, every row 16-byte aligned (tensor copies in, vector
@@ -867,10 +887,10 @@ cudaError_t scan_fwd_form(const ScanArgs& a, bool vec, int& form, int& ctas) {
   int c = 0, dev = 0;
   if (a.io == kBF16 && a.dstate > 8) {
     FusedPlan plan;
-    c = vec ? (a.zoh ? fused_ctas<__nv_bfloat16, 16, true, true>(a, plan, dev, err)
-                     : fused_ctas<__nv_bfloat16, 16, true, false>(a, plan, dev, err))
-            : (a.zoh ? fused_ctas<__nv_bfloat16, 16, false, true>(a, plan, dev, err)
-                     : fused_ctas<__nv_bfloat16, 16, false, false>(a, plan, dev, err));
+    c = vec ? (a.zoh ? fused_ctas<__nv_bfloat16, 16, true, true, false>(a, plan, dev, err)
+                     : fused_ctas<__nv_bfloat16, 16, true, false, false>(a, plan, dev, err))
+            : (a.zoh ? fused_ctas<__nv_bfloat16, 16, false, true, false>(a, plan, dev, err)
+                     : fused_ctas<__nv_bfloat16, 16, false, false, false>(a, plan, dev, err));
     if (err != cudaSuccess) return err;
   }
   form = c > 0 ? kFormBalanced : kFormPlain;

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.ssm_abi_version() == 5
+    assert lib.ssm_abi_version() == 6
     for code in range(-8, 1):
         s = lib.ssm_status_string(code).decode()
         assert s and s != "unknown status"
@@ -198,7 +198,8 @@ def test_conv_update_validation(lib, over, expected):
 
 
 def test_num_checkpoints(lib):
-    assert [lib.ssm_scan_num_checkpoints(L) for L in (0, 1, 31, 32, 33, 2048, 65536)] == [0, 1, 1, 1, 2, 64, 2048]
+    # one checkpoint before every 8th step (SSM_SCAN_CHECKPOINT_STEPS)
+    assert [lib.ssm_scan_num_checkpoints(L) for L in (0, 1, 7, 8, 9, 2048, 65536)] == [0, 1, 1, 1, 2, 256, 8192]
 
 
 def test_train_forward_validation(lib):

@@ -23,6 +23,7 @@ pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda:0") if torch.cuda.is_available() else None
 f = wl.to_f64
 ELEMENTWISE = ("du", "ddelta", "dz")
+CKPT = 8  # SSM_SCAN_CHECKPOINT_STEPS: steps between the training forward's checkpoints
 
 
 # Per-element bound for the summed gradients, relative to the element's absolute-term sum.  A
@@ -132,7 +133,7 @@ def test_initial_state_gradient():
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_training_forward_matches_forward_and_checkpoints(io):
     """The training forward returns the same y and last_state as the plain forward, and its
-    checkpoint c is the oracle's state after the first 32c steps."""
+    checkpoint c is the oracle's state after the first CKPT * c steps."""
     inp = to_device(wl.random_scan_case(2, 40, 16, 200, io=io, seed=9, h0=True), DEV)
     dout = torch.zeros_like(inp["u"])
     y, last, ck, _ = train_step(inp, dout, h0=inp["h0"])
@@ -143,7 +144,7 @@ def test_training_forward_matches_forward_and_checkpoints(io):
     ckn = f(ck)
     np.testing.assert_array_equal(ckn[:, 0], f(inp["h0"]))
     for c in range(1, ckn.shape[1]):
-        pre = {k: (v[..., :32 * c].contiguous() if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
+        pre = {k: (v[..., :CKPT * c].contiguous() if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
         _, s_ref = oracle_scan(pre, h0=inp["h0"])
         assert_close(ckn[:, c], s_ref, 1e-4, f"checkpoint {c}")
 
@@ -204,7 +205,7 @@ def test_zoh_backward_decay_regimes(regime):
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_zoh_training_forward_matches_forward_and_checkpoints(io):
     """The training forward under the hold returns the plain hold forward's y and last_state, and
-    its checkpoint c is the oracle's hold state after the first 32c steps."""
+    its checkpoint c is the oracle's hold state after the first CKPT * c steps."""
     inp = to_device(wl.random_scan_case(2, 40, 16, 200, io=io, seed=10, h0=True), DEV)
     dout = torch.zeros_like(inp["u"])
     y, last, ck, _ = train_step(inp, dout, h0=inp["h0"], disc="zoh")
@@ -215,6 +216,6 @@ def test_zoh_training_forward_matches_forward_and_checkpoints(io):
     ckn = f(ck)
     np.testing.assert_array_equal(ckn[:, 0], f(inp["h0"]))
     for c in range(1, ckn.shape[1]):
-        pre = {k: (v[..., :32 * c].contiguous() if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
+        pre = {k: (v[..., :CKPT * c].contiguous() if k in ("u", "delta", "z", "B", "C") else v) for k, v in inp.items()}
         _, s_ref = oracle_scan(pre, h0=inp["h0"], zoh=True)
         assert_close(ckn[:, c], s_ref, 1e-4, f"zoh checkpoint {c}")
