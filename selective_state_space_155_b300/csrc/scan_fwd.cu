@@ -10,19 +10,22 @@
 // its time in a chain of latency-bound phases (wait for the chunk, convert, per-element prologue,
 // barrier, recurrence, readout reduction, epilogue) that one set of warps walks in turn.  This
 // kernel gives the phases to different warps so that they overlap:
-//  * PREP warps (4) own the HBM traffic and all per-element work.  They stream chunks of 32 steps
-//    of u, delta, z, B, C with 16-byte cp.async into a two-stage raw ring (zero-filled past the
-//    sequence end), convert B and C into float32 [t][n] tables, and compute, once per element,
-//    Delta = softplus(delta + dt_bias), Delta*u, D*u and silu(z) into a two-stage table ring.
+//  * PREP warps (4) own the HBM traffic and all per-element work.  Tensor copies (TMA) bring u,
+//    delta, z, B, C into a two-stage raw ring, two 32-step chunks per copy when the sequence is a
+//    whole number of chunks (zero-filled past the sequence end); the prep converts B and C into
+//    float32 [t][n] tables and computes, once per element, Delta = softplus(delta + dt_bias),
+//    Delta*u, D*u and silu(z) into a two-stage table ring.
 //  * RECURRENCE warps (R = NPAD/4) each own 32/R channels, four states per lane (lanes of a
 //    quarter-warp share one n-group, so their B/C loads hit one address).  The float32 state lives
 //    in registers for the whole sequence.  Per 16-step window the recurrence runs on float2 pairs
 //    (mul/fma.f32x2) keeping the readout partials C.h in registers; the sum over the R lanes of a
-//    channel is a reduce-scatter of warp shuffles (no shared-memory traffic: the kernel is bound by
-//    the shared-memory data path, which its B, C and step-table loads already fill); lane (g, c)
-//    then finishes 16/R consecutive steps of channel c, (y + D u) * silu(z), stored straight to HBM.
+//    channel is a reduce-scatter of warp shuffles (no shared-memory traffic: the shared-memory data
+//    path is the recurrence's busiest, its B, C and step-table loads already fill most of it);
+//    lane (g, c) then finishes 16/R consecutive steps of channel c, (y + D u) * silu(z), stored
+//    straight to HBM.
 //  * Hand-off is by mbarriers in shared memory: table stage s is FULL once every prep thread has
-//    arrived on it, EMPTY once every lane of the group's recurrence warps has.  Each recurrence
+//    arrived on it, EMPTY once every recurrence warp of the group has (one arrival per warp, after
+//    the warp's lanes have synchronised).  Each recurrence
 //    warp waits for FULL on its own, so the warps of a group are not re-aligned at every chunk
 //    (aligned warps reach their window-end readouts together and leave the schedulers idle).  The
 //    prep, which runs ahead and waits at almost every chunk, waits for EMPTY in one warp while the
@@ -36,8 +39,8 @@
 //    pole; the kernel is launched at 80 registers per thread and the shares add up to that.
 //  * Padded states (n >= dstate) have A = 0 and B = C = 0; padded steps (t >= seqlen) have
 //    Delta = 0.  Both leave the state unchanged, so one code path serves every size.
-//  * With a checkpoint buffer (the training forward), the recurrence lanes also store the state
-//    at the start of every chunk, which is what the backward pass restarts from.
+//  * With a checkpoint buffer (the training forward, its own instantiation), the recurrence lanes
+//    also store the state before every 8th step, which is what the backward pass restarts from.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -231,12 +234,12 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   const int nchunks = (L + kChunk - 1) / kChunk;
 
   // mbarriers: FULL[s] completes when all PT prep threads have written table stage s, EMPTY[s]
-  // when every lane of the recurrence warps holding a channel of the group is done reading it
+  // when every recurrence warp holding a channel of the group is done reading it
   uint64_t* mb = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOfs);
   const int rec_warps = min(CWARPS, (dlim - d0 + CPW - 1) / CPW);
   if (tid == 0) {
     mbar_init(&mb[0], PT), mbar_init(&mb[1], PT);
-    mbar_init(&mb[2], 32 * rec_warps), mbar_init(&mb[3], 32 * rec_warps);
+    mbar_init(&mb[2], rec_warps), mbar_init(&mb[3], rec_warps);  // EMPTY: one arrival per recurrence warp
     mbar_init(&mb[4], 1), mbar_init(&mb[5], 1);  // RAW: one expect-tx arrival each
     fence_mbar_init();
   }
@@ -599,7 +602,8 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       const int tg = t0 + tb;  // first global step
       if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, L - tg);
     }
-    mbar_arrive(&mb[2 + s]);  // this lane is done reading table stage s
+    __syncwarp();  // every lane of the warp is done reading table stage s ...
+    if (lane == 0) mbar_arrive(&mb[2 + s]);  // ... which one arrival (release) then reports
   }
 
   if (a.last_state && ch_ok) {
