@@ -23,9 +23,9 @@
 //    path is the recurrence's busiest, its B, C and step-table loads already fill most of it);
 //    lane (g, c) then finishes 16/R consecutive steps of channel c, (y + D u) * silu(z), stored
 //    straight to HBM.
-//  * Hand-off is by mbarriers in shared memory: table stage s is FULL once every prep thread has
-//    arrived on it, EMPTY once every recurrence warp of the group has (one arrival per warp, after
-//    the warp's lanes have synchronised).  Each recurrence
+//  * Hand-off is by mbarriers in shared memory: table stage s is FULL once the prep has written it
+//    (one arrival after the prep threads' closing barrier), EMPTY once every recurrence warp of the
+//    group has read it (one arrival per warp, after the warp's lanes have synchronised).  Each recurrence
 //    warp waits for FULL on its own, so the warps of a group are not re-aligned at every chunk
 //    (aligned warps reach their window-end readouts together and leave the schedulers idle).  The
 //    prep, which runs ahead and waits at almost every chunk, waits for EMPTY in one warp while the
@@ -233,12 +233,13 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   const bool has_z = a.z != nullptr;
   const int nchunks = (L + kChunk - 1) / kChunk;
 
-  // mbarriers: FULL[s] completes when all PT prep threads have written table stage s, EMPTY[s]
-  // when every recurrence warp holding a channel of the group is done reading it
+  // mbarriers: FULL[s] completes when the prep threads have written table stage s (one arrival
+  // after their closing barrier), EMPTY[s] when every recurrence warp holding a channel of the
+  // group is done reading it
   uint64_t* mb = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOfs);
   const int rec_warps = min(CWARPS, (dlim - d0 + CPW - 1) / CPW);
   if (tid == 0) {
-    mbar_init(&mb[0], PT), mbar_init(&mb[1], PT);
+    mbar_init(&mb[0], 1), mbar_init(&mb[1], 1);  // FULL: one arrival after the prep's closing barrier
     mbar_init(&mb[2], rec_warps), mbar_init(&mb[3], rec_warps);  // EMPTY: one arrival per recurrence warp
     mbar_init(&mb[4], 1), mbar_init(&mb[5], 1);  // RAW: one expect-tx arrival each
     fence_mbar_init();
@@ -451,7 +452,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
         *decide = refill ? 1 : 0;
       }
       bar_sync(bPrep, PT);  // every prep thread is done reading chunk k; the decision is visible
-      mbar_arrive(&mb[s]);  // this thread's part of table stage s is written
+      if (ptid == 0) mbar_arrive(&mb[s]);  // table stage s is written (the barrier above ordered every prep write)
       if (VEC && lane == 0 && last_of_stage && *decide) issue_copies(rs, (su + 2) * (kChunk << lg));
     }
     if (VEC && ptid == 0) {  // these last waits ignore the CTA's give-up flag
