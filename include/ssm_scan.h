@@ -298,9 +298,9 @@ double ssm_probe_ops_per_cta(int kind);
 
 /*
  * Inside the forward kernels the warps that load and prepare each chunk hand it to the warps that
- * run the recurrence through shared-memory barriers.  Every wait on them is bounded (about a
- * second); a wait that gives up ends the kernel early, leaving y and the states undefined, and is
- * counted.  This writes the number of such waits since the library was loaded to *count (after
+ * run the recurrence through shared-memory barriers, and the decode step's bulk-copy form waits on
+ * a barrier for each tile's copies.  Every such wait is bounded (about a second); a wait that gives
+ * up ends the kernel early, leaving its outputs and states undefined, and is counted.  This writes the number of such waits since the library was loaded to *count (after
  * synchronising the device).  A correct build never gives up: non-zero means a defect or a device
  * that stopped a kernel's warps for over a second.  Returns SSM_OK, SSM_ERR_NULL or SSM_ERR_LAUNCH.
  */

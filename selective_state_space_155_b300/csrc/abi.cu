@@ -300,9 +300,9 @@ int ssm_causal_conv1d_update(void* state, const void* x, const float* weight, co
 
 int ssm_wait_timeouts(unsigned long long* count) {
   if (!count) return SSM_ERR_NULL;
-  unsigned long long n = 0;
-  if (ssm::scan_wait_timeouts(n) != cudaSuccess) return SSM_ERR_LAUNCH;
-  *count = n;
+  unsigned long long n = 0, m = 0;
+  if (ssm::scan_wait_timeouts(n) != cudaSuccess || ssm::decode_wait_timeouts(m) != cudaSuccess) return SSM_ERR_LAUNCH;
+  *count = n + m;
   return SSM_OK;
 }
 

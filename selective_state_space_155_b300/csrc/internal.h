@@ -147,6 +147,10 @@ cudaError_t scan_wait_timeouts(unsigned long long& count);
 // Enqueue one decode step on `stream`.  Arguments are already validated.
 cudaError_t launch_state_update(const UpdateArgs& a, cudaStream_t stream);
 
+// Stage waits of the bulk-copy decode kernel that gave up since the library was loaded
+// (synchronises the device first).
+cudaError_t decode_wait_timeouts(unsigned long long& count);
+
 // Enqueue the backward pass of the scan on `stream` (scan_bwd.cu): zero the accumulated
 // gradients, then one launch.  Arguments are already validated.
 cudaError_t launch_scan_bwd(const ScanBwdArgs& a, cudaStream_t stream);

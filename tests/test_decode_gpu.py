@@ -95,19 +95,23 @@ def test_decode_workload_1024_steps_sampled():
         assert_close(f(run.state[bs[i], ds[i]]), s_ref.ravel(), ts, f"final state of channel ({bs[i]}, {ds[i]})")
 
 
-# The persistent tiled form serves dstate 16 from 65536 channels up: tiles of 128 channels, a
+# The persistent tiled forms serve dstate 16 from 65536 channels up: tiles of 128 channels, a
 # partial last tile when batch*dim is not a multiple of 128, and tiles that straddle batch rows
-# when dim is not; when dim is, the tiles also stage dt_bias, D and the row's B, C.
+# when dim is not; when dim is, the tiles also stage dt_bias, D and the row's B, C, and the
+# library's choice is the bulk-copy form (one bulk copy per operand range, one bulk store of the
+# new states); SSM_DECODE_VARIANT=tiled forces the per-thread-copy tiled form.
 TILED = [(37, 1800, "bf16"), (16, 4096, "f32"), (64, 1032, "bf16"), (32, 2048, "bf16")]
 
 
 @pytest.mark.parametrize("shape", TILED, ids=lambda s: "b{}_d{}_{}".format(*s))
 @pytest.mark.parametrize("opts", [(True, True, True), (False, False, False)])
 @pytest.mark.parametrize("disc", ["delta_b", "zoh"])
-@pytest.mark.parametrize("variant", ["tiled", "thread"])
+@pytest.mark.parametrize("variant", ["auto", "tiled", "thread"])
 def test_large_batch_step(shape, opts, disc, variant, monkeypatch):
-    if variant == "thread":
-        monkeypatch.setenv("SSM_DECODE_VARIANT", "thread")
+    if variant == "auto":
+        monkeypatch.delenv("SSM_DECODE_VARIANT", raising=False)
+    else:
+        monkeypatch.setenv("SSM_DECODE_VARIANT", variant)
     batch, dim, io = shape
     inp = random_step(batch, dim, 16, io, seed=batch + dim, gate=opts[0], use_D=opts[1], use_bias=opts[2])
     d = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
@@ -124,16 +128,17 @@ def test_large_batch_step(shape, opts, disc, variant, monkeypatch):
 
 
 def test_tiled_and_thread_forms_agree():
-    """Both decode forms on the same large batch: the states agree to float32 rounding (the
-    readout sums run in different orders, the state update is the same arithmetic)."""
+    """The decode forms on the same large batch: the bulk-copy and tiled forms run the same
+    per-channel arithmetic (bitwise equal); against the per-thread form the states are equal and
+    the outputs agree to a bf16 rounding step (the readout sums run in different orders)."""
     inp = random_step(40, 2048, 16, "bf16", seed=77)
     d = {k: (v.to(DEV) if v is not None else None) for k, v in inp.items()}
     res = {}
-    for variant in ("tiled", "thread"):
+    for variant in ("bulk", "tiled", "thread"):
         import os
         old = os.environ.pop("SSM_DECODE_VARIANT", None)
-        if variant == "thread":
-            os.environ["SSM_DECODE_VARIANT"] = "thread"
+        if variant != "bulk":
+            os.environ["SSM_DECODE_VARIANT"] = variant
         try:
             st = d["state"].clone()
             out = ssm.ssm_state_update(st, d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"])
@@ -143,6 +148,7 @@ def test_tiled_and_thread_forms_agree():
             os.environ.pop("SSM_DECODE_VARIANT", None)
             if old is not None:
                 os.environ["SSM_DECODE_VARIANT"] = old
+    assert torch.equal(res["bulk"][0], res["tiled"][0]) and torch.equal(res["bulk"][1], res["tiled"][1])
     assert torch.equal(res["tiled"][0], res["thread"][0])  # the update itself is identical per state
     a, b = res["tiled"][1].float(), res["thread"][1].float()
     assert float(((a - b).abs() / (1.0 + b.abs())).max()) <= 1e-2  # a bf16 rounding step at most
