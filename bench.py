@@ -655,6 +655,37 @@ def run_long(device, steps=6, warmup=3):
             "l2": "one input set of 2.0 GB (far above L2)"}
 
 
+def run_long_narrow(device, steps=10, warmup=3):
+    """The long sequence with few channels (batch 1, d_inner 1536, d_state 16, L 65536, bf16), which
+    the library scans in its split form (segments side by side, linked by a carry pass); timed the
+    same way with the split switched off (SSM_SCAN_SPLIT=off) for comparison."""
+    import selective_state_space_155_b300 as ssm
+    w = wl.LONG_NARROW
+    inp = wl.scan_inputs(w, device=device)
+    call = ssm.prepare_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                inp["dt_bias"], delta_softplus=True)
+    form = ssm.scan_fwd_form(w.batch, w.dim, w.dstate, w.seqlen)[0]
+    ms = timed(lambda i: call(), steps, warmup)
+    prev = os.environ.get("SSM_SCAN_SPLIT")
+    os.environ["SSM_SCAN_SPLIT"] = "off"
+    try:
+        ms_off = timed(lambda i: call(), steps, warmup)
+    finally:
+        if prev is None:
+            os.environ.pop("SSM_SCAN_SPLIT", None)
+        else:
+            os.environ["SSM_SCAN_SPLIT"] = prev
+    del inp, call
+    torch.cuda.empty_cache()
+    hbm, _ = measured_peaks()
+    nbytes = w.algorithmic_bytes()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "form": form, "us_per_step": ms * 1e3, "elements_per_s": w.elements / (ms * 1e-3),
+            "algorithmic_bytes_per_launch": nbytes, "hbm_gbs": gbs, "frac_of_hbm": gbs / hbm,
+            "unsplit_us_per_step": ms_off * 1e3, "split_speedup": ms_off / ms, "steps": steps,
+            "l2": "one input set of 0.6 GB (above L2)"}
+
+
 def run_train(w: wl.ScanWorkload, device, steps=50, warmup=3, copies=ROTATING_COPIES, discretization="delta_b"):
     """The training pair on the scan workload: the forward that keeps chunk checkpoints, then the
     backward pass from them and a synthetic dout (rotating input copies, as for the forward)."""
@@ -766,13 +797,17 @@ def run_decode(device, steps_graph=3, warmup=1):
 
 def profile_mode(which: str) -> int:
     """A few launches of one kernel for an ncu capture: the mid-size scan with either
-    discretisation (about 0.6 GB on the device), the causal conv1d on the same activation shape
+    discretisation (about 0.6 GB on the device), the long scan (about 2.7 GB; with its split
+    form, three launches per step), the causal conv1d on the same activation shape
     (about 0.1 GB), or decode steps of the decode workload without a graph (about 0.2 GB)."""
     from selective_state_space_155_b300 import build as _build
     _build.build()
     device = torch.device("cuda", 0)
     if which == "scan":
         run = ScanRun(wl.MID, device, copies=1)
+        fn = run.step
+    elif which == "long":
+        run = ScanRun(wl.LONG, device, copies=1)
         fn = run.step
     elif which == "zoh":
         run = ScanRun(wl.MID, device, copies=1, discretization="zoh")
@@ -823,7 +858,7 @@ def main(argv=None):
     ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-train", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "zoh", "bwd", "bwd_zoh", "conv", "decode"], default=None,
+    ap.add_argument("--profile", choices=["scan", "zoh", "long", "bwd", "bwd_zoh", "conv", "decode"], default=None,
                     help="run 2 warm-up and 3 profiled launches of one kernel on its workload and exit "
                          "(a small command for ncu; prints no JSON line)")
     args = ap.parse_args(argv)
@@ -913,6 +948,7 @@ def main(argv=None):
                       "pipeline": f"{nsl} batch-row slices over three streams (H2D, scan, D2H)"}
     if rank == 0 and not args.no_long:
         res["long"] = run_long(device)
+        res["long_narrow"] = run_long_narrow(device)
     if rank == 0 and not args.no_decode:
         res["decode"] = run_decode(device)
     if rank == 0 and not args.no_zoh:

@@ -34,8 +34,12 @@
  *                    input, over whole rows and as a decode step.
  *
  * Conventions shared by every entry point
- *  - Every pointer is a DEVICE pointer owned by the caller.  The library never
- *    allocates, never frees and keeps no global state between calls.
+ *  - Every pointer is a DEVICE pointer owned by the caller.  The library keeps no
+ *    global state between calls and allocates nothing, with one exception: a scan
+ *    that runs split (SSM_FORM_SPLIT below) takes its carry buffers (about
+ *    4 * (dstate + 1) bytes per batch row, channel and carry segment) from the
+ *    device's default memory pool with cudaMallocAsync on `stream` and returns them
+ *    with cudaFreeAsync on the same stream after its last launch.
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  Kernel-time errors surface on the caller's next
  *    synchronisation of that stream.
@@ -129,17 +133,29 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void
 
 /*
  * Which kernel form a scan of these sizes launches on the current device, without launching it.
- * Both forms compute the same recurrence in the same order per state, so their results are
- * bitwise equal; they differ in how channels are spread over SMs:
+ * The plain and balanced forms compute the same recurrence in the same order per state, so their
+ * results are bitwise equal; they differ in how channels are spread over SMs:
  *   SSM_FORM_PLAIN     one CTA per 32-channel block of a batch row;
  *   SSM_FORM_BALANCED  one CTA per SM holding up to three warp groups on host-planned channel
  *                      ranges (bf16, dstate 9..16, dim a multiple of 8, where the plan lowers the
  *                      busiest SM's load; SSM_SCAN_VARIANT=quad_plain in the environment turns it off).
+ *   SSM_FORM_SPLIT     the balanced form with the sequence split into segments scanned side by
+ *                      side, for few channels and long sequences (four segments fit the SMs'
+ *                      warp groups at once: at most 3 eight-channel units per SM; seqlen >= 8192,
+ *                      16-byte aligned rows, no checkpoints, last_state not overlapping h0).  A carry pass scans each carry segment from a zero
+ *                      state (the first from h0) for its end state and step-size sum; a combine
+ *                      folds them with the associative pair operator (a1, b1) o (a2, b2) =
+ *                      (a1 a2, a2 b1 + b2), a segment's decay a = exp(A * sum of its Delta) (53ai.com
+ *                      Mamba article, section 3.3 "Parallel Associative Scan"; gsyq.cn page,
+ *                      "硬件优化并行扫描算法"); the full pass scans every segment from its combined
+ *                      carry.  Results equal the unsplit scan's up to float32 rounding (the decay
+ *                      of a segment is one exponential of a sum instead of a product of per-step
+ *                      exponentials).  SSM_SCAN_SPLIT=off in the environment turns it off.
  * aligned_rows: non-zero when u, delta, z, B, C and y will be 16-byte aligned.  *ctas (nullable)
- * receives the grid size.  Returns the form (>= 0) or a negative ssm_status (SSM_ERR_LAUNCH when
- * no device can be queried).
+ * receives the grid size (of the full pass, for the split form).  Returns the form (>= 0) or a
+ * negative ssm_status (SSM_ERR_LAUNCH when no device can be queried).
  */
-typedef enum { SSM_FORM_PLAIN = 0, SSM_FORM_BALANCED = 1 } ssm_scan_form;
+typedef enum { SSM_FORM_PLAIN = 0, SSM_FORM_BALANCED = 1, SSM_FORM_SPLIT = 2 } ssm_scan_form;
 int ssm_scan_fwd_form(int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization, int aligned_rows,
                       int* ctas);
 

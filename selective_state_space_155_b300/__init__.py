@@ -168,8 +168,9 @@ def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_soft
 def scan_fwd_form(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bfloat16, discretization="delta_b",
                   aligned_rows: bool = True) -> tuple[str, int]:
     """(form name, CTAs) of the kernel a scan of these sizes launches on the current device
-    (``ssm_scan_fwd_form``): "plain" (one CTA per 32-channel block) or "balanced" (one CTA per SM
-    with up to three warp groups on planned channel ranges)."""
+    (``ssm_scan_fwd_form``): "plain" (one CTA per 32-channel block), "balanced" (one CTA per SM
+    with up to three warp groups on planned channel ranges) or "split" (the balanced form over
+    segments of the sequence, linked by a carry pass; few channels and long sequences)."""
     import ctypes
     n = ctypes.c_int(0)
     st = lib().ssm_scan_fwd_form(int(batch), int(dim), int(dstate), int(seqlen), io_dtype_code(dtype),

@@ -29,7 +29,8 @@ SSM_DISC_ZOH = 1
 
 SSM_FORM_PLAIN = 0
 SSM_FORM_BALANCED = 1
-FORM_NAMES = {0: "plain", 1: "balanced"}
+SSM_FORM_SPLIT = 2
+FORM_NAMES = {0: "plain", 1: "balanced", 2: "split"}
 
 SSM_PROBE_EX2 = 0
 SSM_PROBE_FFMA = 1

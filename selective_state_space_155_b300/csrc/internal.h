@@ -47,6 +47,15 @@ struct ScanArgs {
   int io;
   int zoh;      // exact zero-order-hold Bbar instead of Delta * B
   float* ckpt;  // nullable: the state at the start of every kCkptSteps steps, for the backward
+  // Sequence split (set by the launcher, zero otherwise): the steps of a row are cut into segments
+  // of seg_len steps (a multiple of 2 * kScanChunk).  The carry pass scans every carry segment but
+  // the last scan segment's from a zero state (the first from h0) and stores its end state and its
+  // step-size sum; the full pass scans every segment from the state its carries combine to,
+  // seg_carries carry segments per segment.
+  int seg_len;
+  int seg_carries;
+  float* carry_h;  // [carry segment][batch][dim][dstate]
+  float* carry_d;  // [carry segment][batch][dim]
 };
 
 // Steps per chunk of the scan kernels, and the interval of the training forward's checkpoints
@@ -137,8 +146,17 @@ cudaError_t launch_scan_fwd(const ScanArgs& a, cudaStream_t stream);
 cudaError_t launch_scan_fwd_quad(const ScanArgs& a, bool vec, cudaStream_t stream);
 
 // The form launch_scan_fwd runs for `a` (vec: rows take the 16-byte copy path) and its grid size.
-enum ScanForm { kFormPlain = 0, kFormBalanced = 1 };
+enum ScanForm { kFormPlain = 0, kFormBalanced = 1, kFormSplit = 2 };
 cudaError_t scan_fwd_form(const ScanArgs& a, bool vec, int& form, int& ctas);
+
+// The sequence split the balanced form uses for `a` on the current device: segments, carry
+// segments per segment, their lengths in steps, and the carry buffers' size in bytes; segs = 0
+// when the scan is not split.
+struct SplitPlan {
+  int segs, carries_per_seg, seg_len, carry_len, ncarry;
+  size_t workspace_bytes;
+};
+cudaError_t scan_fwd_split(const ScanArgs& a, bool vec, SplitPlan& p);
 
 // Hand-off waits of the forward kernels that gave up since the library was loaded (synchronises
 // the device first).

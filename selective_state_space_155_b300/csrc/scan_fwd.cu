@@ -49,6 +49,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <type_traits>
@@ -206,13 +207,16 @@ __device__ __forceinline__ void store_out(T* dst, const float (&v)[OPL], int n) 
 }
 
 // One group of warps (4 prep + R recurrence) scanning the channels [d0, dlim) of batch row b, at
-// most CPB of them, with its own shared-memory block `smem` (mbarriers included) and the named
-// barriers bar0 + 1 .. bar0 + 5; tid is the thread's index within the group, abort the CTA's
-// give-up flag.  A CTA of the plain kernel is one group.
-template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
+// most CPB of them, over the chunks [kc0, kc1) of segment seg, with its own shared-memory block
+// `smem` (mbarriers included) and the named barriers bar0 + 1 .. bar0 + 5; tid is the thread's index
+// within the group, abort the CTA's give-up flag.  A CTA of the plain kernel is one group over the
+// whole sequence.  SEGS: the group's range is a segment of a split sequence ([kc0, kc1), seg);
+// otherwise the whole row (seg 0).  CARRY: the carry pass of a split sequence (state and
+// step-size sum only: no C, z, readout or output).
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK, bool SEGS = false, bool CARRY = false>
 __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& maps, unsigned char* smem, const int tid,
-                                           const int b, const int d0, const int dlim, const int bar0,
-                                           volatile int* abort) {
+                                           const int b, const int d0, const int dlim, const int seg, const int kc0,
+                                           const int kc1, const int bar0, volatile int* abort) {
   using Cfg = ScanCfg<T, NPAD>;
   constexpr int R = Cfg::R, CPW = Cfg::CPW, CPB = Cfg::CPB, EPV = Cfg::EPV, VPR = Cfg::VPR;
   constexpr int NT = Cfg::NT, PT = Cfg::PT, ROWS = Cfg::ROWS, PSS = Cfg::PSS, DSS = Cfg::DSS, OPL = Cfg::OPL;
@@ -230,8 +234,9 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   const int bPrep = kBarPrep + bar0;
   const int warp = tid >> 5, lane = tid & 31;
   const int L = a.seqlen, N = a.dstate;
-  const bool has_z = a.z != nullptr;
-  const int nchunks = (L + kChunk - 1) / kChunk;
+  const bool has_z = !CARRY && a.z != nullptr;
+  const int nchunks = SEGS ? kc1 - kc0 : (L + kChunk - 1) / kChunk;  // chunks of the group's range
+  const int T0 = SEGS ? kc0 * kChunk : 0;                              // its first step
 
   // mbarriers: FULL[s] completes when the prep threads have written table stage s (one arrival
   // after their closing barrier), EMPTY[s] when every recurrence warp holding a channel of the
@@ -267,7 +272,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
     // barrier's transaction count never runs ahead of its arrival.
     const bool pair = VEC && Cfg::SLOTS == 2 && maps.pair != 0;
     const int lg = pair ? 1 : 0;  // log2 of the chunks per raw stage
-    const uint32_t stage_bytes = uint32_t((has_z ? 3 : 2) * Cfg::kXBytes + 2 * Cfg::kBBytes) << lg;
+    const uint32_t stage_bytes = uint32_t((has_z ? 3 : 2) * Cfg::kXBytes + (CARRY ? 1 : 2) * Cfg::kBBytes) << lg;
     auto issue_copies = [&](int stage, int t0) {  // lane 0 of every prep warp
       T* dst = raw + size_t(stage) * Cfg::SLOTS * ROWS * kChunk;
       uint64_t* rb = &mb[4 + stage];
@@ -275,10 +280,10 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       if (pw == 0) {
         if (pair) {
           tma_load_3d(dst + Cfg::kBTile, &maps.B, 0, b * N, c0, rb);
-          tma_load_3d(dst + Cfg::kCTile, &maps.C, 0, b * N, c0, rb);
+          if (!CARRY) tma_load_3d(dst + Cfg::kCTile, &maps.C, 0, b * N, c0, rb);
         } else {
           tma_load_2d(dst + Cfg::kBTile, &maps.B, t0, b * N, rb);
-          tma_load_2d(dst + Cfg::kCTile, &maps.C, t0, b * N, rb);
+          if (!CARRY) tma_load_2d(dst + Cfg::kCTile, &maps.C, t0, b * N, rb);
         }
       } else if (pw < 3 || has_z) {
         const CUtensorMap* m = pw == 1 ? &maps.u : (pw == 2 ? &maps.delta : &maps.z);
@@ -329,7 +334,8 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       const int e = ptid + m * PT;
       const int n = e % NPAD, which = (e / NPAD) % 2, q = e / (2 * NPAD);
       const int qr = (q + (sizeof(T) == 2 ? (n >> 1) : n)) & (VPR - 1);
-      c_src[m] = e < NITEM ? (which == 0 ? Cfg::kBTile : Cfg::kCTile) + n * kChunk + qr * EPV : -1;
+      c_src[m] = e < NITEM && (!CARRY || which == 0) ? (which == 0 ? Cfg::kBTile : Cfg::kCTile) + n * kChunk + qr * EPV
+                                                     : -1;
       c_dst[m] = which * Cfg::kCOfs + (qr * EPV) * NPAD + n;
       c_ok[m] = n < N;
     }
@@ -347,7 +353,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
     for (int i = 0; i < IPE; ++i) {
       const int c = d0 + ech0 + i * ECH;
       e_bias[i] = (c < dlim && a.dt_bias) ? a.dt_bias[c] : 0.0f;
-      e_D[i] = (c < dlim && a.D) ? a.D[c] : 0.0f;
+      e_D[i] = (!CARRY && c < dlim && a.D) ? a.D[c] : 0.0f;
     }
 
     // Copies in flight, tracked by ptid 0: the raw-stage use (chunk >> lg) whose copies into raw
@@ -372,14 +378,14 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       }
       bar_sync(bPrep, PT);
       if (lane == 0) {
-        if (nstages > 0) issue_copies(0, 0);
-        if (nstages > 1) issue_copies(1, kChunk << lg);
+        if (nstages > 0) issue_copies(0, T0);
+        if (nstages > 1) issue_copies(1, T0 + (kChunk << lg));
       }
     }
 
     for (int k = 0; k < nchunks; ++k) {
       const int s = k & 1;
-      const int t0 = k * kChunk;
+      const int t0 = T0 + k * kChunk;
       const int su = k >> lg, rs = su & 1;   // raw-stage use and raw stage of chunk k
       const int slot = k & ((1 << lg) - 1);  // its slot within the stage
       if (VEC) {
@@ -438,11 +444,13 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
         dl.x = 2 * ep < lim_c ? dl.x : 0.0f;
         dl.y = 2 * ep + 1 < lim_c ? dl.y : 0.0f;
         const float2 du = ZOH ? uu : __fmul2_rn(dl, uu);
-        const float2 Du = __fmul2_rn(f2(e_D[i], e_D[i]), uu);
-        const float2 sg = has_z ? silu2<std::is_same<T, __nv_bfloat16>::value>(load2<T>(st + Cfg::kZTile + xo + o))
-                                : f2(1.0f, 1.0f);
         *reinterpret_cast<float4*>(Ps + ch * PSS + 2 * ep) = make_float4(dl.x, du.x, dl.y, du.y);
-        *reinterpret_cast<float4*>(DS + ch * DSS + 2 * ep) = make_float4(Du.x, sg.x, Du.y, sg.y);
+        if constexpr (!CARRY) {
+          const float2 Du = __fmul2_rn(f2(e_D[i], e_D[i]), uu);
+          const float2 sg = has_z ? silu2<std::is_same<T, __nv_bfloat16>::value>(load2<T>(st + Cfg::kZTile + xo + o))
+                                  : f2(1.0f, 1.0f);
+          *reinterpret_cast<float4*>(DS + ch * DSS + 2 * ep) = make_float4(Du.x, sg.x, Du.y, sg.y);
+        }
       }
 
       const bool last_of_stage = slot == (1 << lg) - 1 || k == nchunks - 1;
@@ -453,7 +461,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       }
       bar_sync(bPrep, PT);  // every prep thread is done reading chunk k; the decision is visible
       if (ptid == 0) mbar_arrive(&mb[s]);  // table stage s is written (the barrier above ordered every prep write)
-      if (VEC && lane == 0 && last_of_stage && *decide) issue_copies(rs, (su + 2) * (kChunk << lg));
+      if (VEC && lane == 0 && last_of_stage && *decide) issue_copies(rs, T0 + (su + 2) * (kChunk << lg));
     }
     if (VEC && ptid == 0) {  // these last waits ignore the CTA's give-up flag
       if (pend0 >= 0) mbar_wait(&mb[4], (pend0 >> 1) & 1, nullptr, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
@@ -482,13 +490,23 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       const float av = ok ? a.A[size_t(d) * N + n] : 0.0f;
       Av[i] = av * kLog2e;
       iv[i] = zoh_inv(av);
-      hv[i] = (ok && a.h0) ? a.h0[(size_t(b) * a.dim + d) * N + n] : 0.0f;
+      // the state the group starts from: h0 for the first segment; for a later one of a split
+      // sequence, zero in the carry pass and in the full pass the state its carries combined to
+      // (the combine kernel left it in the last carry slot before the segment)
+      float hs = 0.0f;
+      if (ok && seg == 0 && a.h0) hs = a.h0[(size_t(b) * a.dim + d) * N + n];
+      if (!CARRY && ok && seg > 0)
+        hs = a.carry_h[((size_t(seg * a.seg_carries - 1) * a.batch + b) * a.dim + d) * N + n];
+      hv[i] = hs;
     }
     A01 = f2(Av[0], Av[1]), A23 = f2(Av[2], Av[3]);
     iA01 = f2(iv[0], iv[1]), iA23 = f2(iv[2], iv[3]);
     h01 = f2(hv[0], hv[1]), h23 = f2(hv[2], hv[3]);
   }
-  T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L;
+  float dsum = 0.0f;  // the carry pass: sum of this channel's Delta over the segment
+  // the output row from the group's first step on, and the steps left in the row from there
+  T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L + T0;
+  const int Lr = L - T0;
 
   // two chunks per iteration: more independent work for the scheduler around the hand-offs (not
   // with the zero-order hold, whose longer step body would then outgrow the instruction cache)
@@ -518,12 +536,38 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
 #pragma unroll kChunkUnroll
   for (int k = 0; k < nchunks; ++k) {
     const int s = k & 1;
-    const int t0 = k * kChunk;
+    const int t0 = k * kChunk;  // from the group's first step
     mbar_wait(&mb[s], (k >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kRecBackoff);
     const float* Bs = tabBs(s);
     const float* Cs = tabCs(s);
     const float2* Ps = tabPs(s);
     const float2* DS = tabDS(s);
+
+    if constexpr (CARRY) {
+      // state and step-size sum only
+#pragma unroll
+      for (int t = 0; t < kChunk; ++t) {
+        const float2 p = Ps[cl * PSS + t];
+        const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
+        const float2 dd = f2(p.x, p.x), uu = f2(p.y, p.y);
+        const float2 g01 = __fmul2_rn(dd, A01), g23 = __fmul2_rn(dd, A23);
+        const float2 a01 = f2(ex2_approx(g01.x), ex2_approx(g01.y));
+        const float2 a23 = f2(ex2_approx(g23.x), ex2_approx(g23.y));
+        if constexpr (ZOH) {
+          const float2 c01 = zoh_factor2_log2(g01, a01, dd, iA01);
+          const float2 c23 = zoh_factor2_log2(g23, a23, dd, iA23);
+          h01 = __ffma2_rn(a01, h01, __fmul2_rn(c01, __fmul2_rn(uu, f2(bb.x, bb.y))));
+          h23 = __ffma2_rn(a23, h23, __fmul2_rn(c23, __fmul2_rn(uu, f2(bb.z, bb.w))));
+        } else {
+          h01 = __ffma2_rn(a01, h01, __fmul2_rn(uu, f2(bb.x, bb.y)));
+          h23 = __ffma2_rn(a23, h23, __fmul2_rn(uu, f2(bb.z, bb.w)));
+        }
+        dsum += p.x;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&mb[2 + s]);
+      continue;
+    }
 
     // both windows of the chunk unrolled: the first window's readout reduction and epilogue (a
     // chain of dependent shuffles) then overlap the second window's loads and exponentials
@@ -534,7 +578,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       for (int j = 0; j < kWin; ++j) {
         const int t = w + j;
         if constexpr (CK) {
-          if (j % kCkptSteps == 0) checkpoint(t0 + t);
+          if (j % kCkptSteps == 0) checkpoint(T0 + t0 + t);
         }
         const float2 p = Ps[cl * PSS + t];
         const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
@@ -600,15 +644,25 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
         const float2 o = __fmul2_rn(__fadd2_rn(f2(yv[j], yv[j + 1]), f2(ds.x, ds.z)), f2(ds.y, ds.w));
         ov[j] = o.x, ov[j + 1] = o.y;
       }
-      const int tg = t0 + tb;  // first global step
-      if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, L - tg);
+      const int tg = t0 + tb;  // first step, from the group's first
+      if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, Lr - tg);
     }
     __syncwarp();  // every lane of the warp is done reading table stage s ...
     if (lane == 0) mbar_arrive(&mb[2 + s]);  // ... which one arrival (release) then reports
   }
 
-  if (a.last_state && ch_ok) {
-    const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
+  const float hv[4] = {h01.x, h01.y, h23.x, h23.y};
+  if constexpr (CARRY) {
+    if (ch_ok) {
+      const size_t row = (size_t(seg) * a.batch + b) * a.dim + d;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int n = 4 * g + i;
+        if (n < N) a.carry_h[row * N + n] = hv[i];
+      }
+      if (g == 0) a.carry_d[row] = dsum;
+    }
+  } else if (a.last_state && ch_ok && nchunks * kChunk >= Lr) {  // the last segment holds the final state
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int n = 4 * g + i;
@@ -630,21 +684,47 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3)
   __shared__ int abort_flag;
   if (threadIdx.x == 0) abort_flag = 0;
   __syncthreads();
-  scan_group<T, NPAD, VEC, ZOH, CK>(a, maps, smem, threadIdx.x, b, d0, a.dim, 0, &abort_flag);
+  scan_group<T, NPAD, VEC, ZOH, CK>(a, maps, smem, threadIdx.x, b, d0, a.dim, 0, 0, 0, 0, &abort_flag);
+}
+
+// The carry combine of a split sequence, one thread per (batch row, channel, state): carry slot j
+// holds (S_j, h_j), the step-size sum and the end state (from zero; slot 0 from h0) of carry segment
+// j, and the segment's decay is the product of its Abar, exp(A S_j).  Folding the slots left to right
+// with the associative pair operator (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) leaves in slot j the
+// state after carry segment j, from which the next segment starts; only the running state is kept.
+__global__ void __launch_bounds__(256) scan_carry_combine_kernel(const ScanArgs a, int ncarry) {
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long per = (long long)a.batch * a.dim * a.dstate;
+  if (i >= per) return;
+  const long long row = i / a.dstate;  // b * dim + d
+  const int d = int(row % a.dim), n = int(i - row * a.dstate);
+  const float al = a.A[size_t(d) * a.dstate + n] * kLog2e;
+  float h = a.carry_h[i];
+  for (int j = 1; j < ncarry; ++j) {
+    h = __fmaf_rn(ex2_approx(al * a.carry_d[j * ((long long)a.batch * a.dim) + row]), h, a.carry_h[j * per + i]);
+    a.carry_h[j * per + i] = h;
+  }
 }
 
 // The balanced form: one CTA per SM holding kFusedGroups groups, each on a channel range (8 to 32
 // channels of one batch row) from a host plan that evens out the channels per SM.  With 32-channel
 // CTAs an SM carries 64 or 96 channels when the total is not a multiple of 96 per SM; the plan
 // gives every SM within 8 channels of the mean.  Plan entry: b << 16 | (d0 / 8) << 4 | (channels / 8),
-// 0 for an empty group.
+// 0 for an empty group; for the passes of a split sequence b takes 12 bits and the group's segment
+// (it then scans that segment's steps only) the top 4.
 constexpr int kFusedGroups = 3;
 constexpr int kMaxFusedCtas = 160;
+constexpr int kSegShift = 28, kMaxPlanSegs = 16, kMaxSplitBatch = 1 << 12;
 struct FusedPlan {
   uint32_t e[kFusedGroups * kMaxFusedCtas];
 };
 
-template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
+// What one launch of the balanced form scans: whole rows, the segments of a split sequence (full
+// pass), or its carry segments (carry pass).  Whole rows are their own instantiation, without the
+// segment decode, which costs the unsplit kernel registers.
+enum PassMode { kWhole = 0, kSegments = 1, kCarries = 2 };
+
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK, int MODE>
 __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
     scan_fwd_fused_kernel(const ScanArgs a, const __grid_constant__ TmaMaps maps, const FusedPlan plan) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -656,20 +736,29 @@ __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
   const uint32_t e = plan.e[blockIdx.x * kFusedGroups + grp];
   const int nch = int(e & 15u) * 8;
   if (nch == 0) return;  // an empty group: its warps leave, the other groups do not wait on them
-  const int b = int(e >> 16), d0 = int((e >> 4) & 0xfffu) * 8;
-  scan_group<T, NPAD, VEC, ZOH, CK>(a, maps, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0,
-                                min(a.dim, d0 + nch), 5 * grp, &abort_flag);
+  const int d0 = int((e >> 4) & 0xfffu) * 8;
+  int b = int(e >> 16), seg = 0, kc0 = 0, kc1 = 0;
+  if (MODE != kWhole) {
+    const int nck = (a.seqlen + kChunk - 1) / kChunk;
+    seg = int(e >> kSegShift), b &= kMaxSplitBatch - 1;
+    kc0 = seg * (a.seg_len / kChunk), kc1 = min(nck, kc0 + a.seg_len / kChunk);
+  }
+  scan_group<T, NPAD, VEC, ZOH, CK, MODE != kWhole, MODE == kCarries>(
+      a, maps, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0, min(a.dim, d0 + nch), seg, kc0, kc1,
+      5 * grp, &abort_flag);
 }
 
-// Host plan for the balanced form: units of 8 channels, groups of at most 4 units inside one batch
-// row, at most kFusedGroups groups per CTA, CTA c taking ceil(units left / CTAs left) units.
-// Returns the CTA count, or 0 when the plan does not apply or does not lower the busiest SM's load
-// below that of the plain kernel (32-channel CTAs spread over the SMs).
-int make_fused_plan(const ScanArgs& a, int sms, FusedPlan& plan) {
-  if (a.dim % 8 != 0 || a.batch >= (1 << 16) || a.dim / 8 >= (1 << 12) || sms <= 0 || sms > kMaxFusedCtas) return 0;
-  const long long ur = a.dim / 8, units = (long long)a.batch * ur;
+// Host plan for the balanced form over `rows` rows of a.dim channels (the batch rows, or for a
+// split sequence its (segment, batch row) pairs): units of 8 channels, groups of at most 4 units
+// inside one row, at most kFusedGroups groups per CTA, CTA c taking ceil(units left / CTAs left)
+// units.  Returns the CTA count, or 0 when the plan does not apply or (with `against_plain`) does
+// not lower the busiest SM's load below that of the plain kernel (32-channel CTAs spread over the
+// SMs; the passes of a split sequence have no plain alternative).
+int make_fused_plan(const ScanArgs& a, long long rows, int sms, FusedPlan& plan, bool against_plain = true) {
+  if (a.dim % 8 != 0 || rows >= (1 << 16) || a.dim / 8 >= (1 << 12) || sms <= 0 || sms > kMaxFusedCtas) return 0;
+  const long long ur = a.dim / 8, units = rows * ur;
   if (units == 0 || units > (long long)sms * kFusedGroups * 4) return 0;
-  const long long blocks = (long long)a.batch * ((a.dim + 31) / 32);
+  const long long blocks = rows * ((a.dim + 31) / 32);
   const long long plain_max = 4 * ((blocks + sms - 1) / sms);  // units on the busiest SM, plain kernel
   long long left = units, row = 0, pos = 0, worst = 0;
   int ctas = 0;
@@ -678,9 +767,11 @@ int make_fused_plan(const ScanArgs& a, int sms, FusedPlan& plan) {
     long long load = 0;
     for (int g = 0; g < kFusedGroups; ++g) {
       uint32_t entry = 0;
-      if (load < target && row < a.batch) {
+      if (load < target && row < rows) {
         const long long take = std::min(std::min(4LL, target - load), ur - pos);
-        entry = uint32_t(row) << 16 | uint32_t(pos) << 4 | uint32_t(take);
+        // whole rows: row = b; split passes: row = segment * batch + b, segment < 16, batch < 4096
+        entry = uint32_t(row % a.batch) << 16 | uint32_t(row / a.batch) << kSegShift | uint32_t(pos) << 4 |
+                uint32_t(take);
         load += take, pos += take, left -= take;
         if (pos == ur) ++row, pos = 0;
       }
@@ -689,7 +780,7 @@ int make_fused_plan(const ScanArgs& a, int sms, FusedPlan& plan) {
     worst = std::max(worst, load);
     ctas = c + 1;
   }
-  return (left == 0 && worst < plain_max) ? ctas : 0;
+  return (left == 0 && (worst < plain_max || !against_plain)) ? ctas : 0;
 }
 
 // The driver's tensor-map encoder, looked up once through the runtime (no link against the
@@ -758,10 +849,10 @@ cudaError_t encode_maps(const ScanArgs& a, TmaMaps& m) {
 // Once per device: the balanced kernel's shared-memory opt-in, and whether the build has the
 // register count its setmaxnreg split was sized for (if not, the plain kernel runs).  Returns
 // whether the balanced kernel may launch; err reports a failing CUDA call.
-template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK, int MODE>
 bool fused_ready(int dev, cudaError_t& err) {
   using Cfg = ScanCfg<T, NPAD>;
-  auto kernel = scan_fwd_fused_kernel<T, NPAD, VEC, ZOH, CK>;
+  auto kernel = scan_fwd_fused_kernel<T, NPAD, VEC, ZOH, CK, MODE>;
   constexpr size_t kSmem = kFusedGroups * Cfg::kSmem;
   static std::atomic<uint64_t> configured{0}, usable{0};
   const uint64_t bit = uint64_t(1) << (dev & 63);
@@ -776,40 +867,161 @@ bool fused_ready(int dev, cudaError_t& err) {
   return (usable.load(std::memory_order_acquire) & bit) != 0;
 }
 
-// CTAs of the balanced form for `a` (bf16, dstate 9..16: three groups' shared memory fit one CTA),
-// or 0 when the plain kernel runs instead (no plan, SSM_SCAN_VARIANT=quad_plain, or a build
-// whose register count does not match the split).
-template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
-int fused_ctas(const ScanArgs& a, FusedPlan& plan, int& dev, cudaError_t& err) {
+// The current device and its SM count.
+cudaError_t device_sms(int& dev, int& sms) {
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  return cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+bool balanced_allowed() {
+  const char* force = std::getenv("SSM_SCAN_VARIANT");
+  return !(force && std::strcmp(force, "quad_plain") == 0);
+}
+
+// CTAs of the balanced form for `a` over `rows` plan rows (bf16, dstate 9..16: three groups'
+// shared memory fit one CTA), or 0 when it does not run (no plan, SSM_SCAN_VARIANT=quad_plain, or
+// a build whose register count does not match the setmaxnreg split).
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK, int MODE = kWhole>
+int fused_ctas(const ScanArgs& a, long long rows, FusedPlan& plan, int& dev, cudaError_t& err) {
+  static_assert(MODE == kWhole || (VEC && !CK), "the split runs on the 16-byte path without checkpoints");
   if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
     return 0;
   } else {
-    const char* force = std::getenv("SSM_SCAN_VARIANT");
-    if (force && std::strcmp(force, "quad_plain") == 0) return 0;
+    if (!balanced_allowed()) return 0;
     int sms = 0;
-    if ((err = cudaGetDevice(&dev)) != cudaSuccess) return 0;
-    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return 0;
-    const int ctas = make_fused_plan(a, sms, plan);
+    if ((err = device_sms(dev, sms)) != cudaSuccess) return 0;
+    const int ctas = make_fused_plan(a, rows, sms, plan, MODE == kWhole);
     if (ctas == 0) return 0;
-    return fused_ready<T, NPAD, VEC, ZOH, CK>(dev, err) ? ctas : 0;
+    return fused_ready<T, NPAD, VEC, ZOH, CK, MODE>(dev, err) ? ctas : 0;
   }
+}
+
+template <typename T, int NPAD, bool VEC, bool ZOH, bool CK, int MODE>
+cudaError_t launch_fused_plan(const ScanArgs& a, const TmaMaps& maps, FusedPlan& plan, int ctas,
+                              cudaStream_t stream) {
+  using Cfg = ScanCfg<T, NPAD>;
+  ScanArgs args = a;
+  TmaMaps m = maps;
+  void* params[] = {&args, &m, &plan};
+  return cudaLaunchKernel(reinterpret_cast<const void*>(scan_fwd_fused_kernel<T, NPAD, VEC, ZOH, CK, MODE>),
+                          dim3(unsigned(ctas)), dim3(kFusedGroups * Cfg::NT), params, kFusedGroups * Cfg::kSmem,
+                          stream);
 }
 
 // Launches the balanced form when its plan applies; returns false when the plain kernel should run.
 template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
 bool launch_fused(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, cudaError_t& err) {
-  using Cfg = ScanCfg<T, NPAD>;
-  FusedPlan plan;
-  int dev = 0;
-  const int ctas = fused_ctas<T, NPAD, VEC, ZOH, CK>(a, plan, dev, err);
-  if (err != cudaSuccess) return true;
-  if (ctas == 0) return false;
-  ScanArgs args = a;
-  TmaMaps m = maps;
-  void* params[] = {&args, &m, &plan};
-  err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_fwd_fused_kernel<T, NPAD, VEC, ZOH, CK>), dim3(unsigned(ctas)),
-                         dim3(kFusedGroups * Cfg::NT), params, kFusedGroups * Cfg::kSmem, stream);
+  if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
+    return false;  // the balanced form is built for bf16 with dstate 9..16 only
+  } else {
+    FusedPlan plan;
+    int dev = 0;
+    const int ctas = fused_ctas<T, NPAD, VEC, ZOH, CK>(a, a.batch, plan, dev, err);
+    if (err != cudaSuccess) return true;
+    if (ctas == 0) return false;
+    err = launch_fused_plan<T, NPAD, VEC, ZOH, CK, kWhole>(a, maps, plan, ctas, stream);
+    return true;
+  }
+}
+
+// Sequence split for few channels and long sequences.  With few 8-channel units per SM the
+// balanced form leaves each SM one warp group, which is latency-bound, and the split multiplies the
+// groups by scanning segments of the sequence side by side: a carry pass (the recurrence without
+// C, z or output) over the carry segments gives each one's end state from a zero state and its
+// step-size sum, a combine folds them into the state entering each segment, and the full pass
+// scans every segment from it.  The carry pass costs about 0.7 of the full scan per element over
+// (segments - 1) / segments of the sequence, so the split is taken only where kSegs segments fit the
+// SMs' groups at once (at most 3 units per SM); carry segments per segment (at most kMaxCarries) are
+// as many as the groups hold.  Both lengths are multiples of two chunks.
+constexpr int kSplitMinLen = 8192;  // the shortest sequence split (the extra launches must pay)
+constexpr int kSegs = 4, kMaxCarries = 4;
+
+bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
+  p = SplitPlan{};
+  if (a.ckpt || a.dim % 8 != 0 || a.seqlen < kSplitMinLen || sms <= 0) return false;
+  // the full pass reads h0 in one segment while another writes last_state
+  const size_t nst = size_t(a.batch) * a.dim * a.dstate * sizeof(float);
+  const uintptr_t h0 = reinterpret_cast<uintptr_t>(a.h0), ls = reinterpret_cast<uintptr_t>(a.last_state);
+  if (h0 && ls && h0 < ls + nst && ls < h0 + nst) return false;
+  const long long units = (long long)a.batch * (a.dim / 8), cap = (long long)sms * kFusedGroups * 4;
+  if (units == 0) return false;
+  long long segs = kSegs, per = 0;
+  const char* force = std::getenv("SSM_SCAN_SPLIT");
+  if (force && std::strcmp(force, "off") == 0) return false;
+  int fs = 0, fr = 0;
+  if (force && std::sscanf(force, "%d,%d", &fs, &fr) == 2 && fs >= 2 && fr >= 1) {
+    segs = fs, per = fr;  // forced (for measurements and tests)
+    if (units * segs > cap || units * (segs - 1) * per > cap) return false;
+  } else {
+    if (units * segs > cap) return false;
+    per = std::min<long long>(kMaxCarries, cap / (units * (segs - 1)));
+  }
+  const long long step = 2 * kChunk;
+  const long long clen = ((a.seqlen + segs * per - 1) / (segs * per) + step - 1) / step * step;
+  const long long slen = clen * per;
+  const long long nseg = (a.seqlen + slen - 1) / slen;
+  if (nseg < 2 || a.batch >= kMaxSplitBatch || (nseg - 1) * per > kMaxPlanSegs || nseg > kMaxPlanSegs) return false;
+  p.segs = int(nseg), p.carries_per_seg = int(per), p.seg_len = int(slen), p.carry_len = int(clen);
+  p.ncarry = int((nseg - 1) * per);
+  p.workspace_bytes = size_t(p.ncarry) * a.batch * a.dim * (size_t(a.dstate) + 1) * sizeof(float);
   return true;
+}
+
+// The split for `a`, with both passes' plans; false when the scan runs unsplit.
+template <typename T, int NPAD, bool ZOH>
+bool split_plans(const ScanArgs& a, SplitPlan& sp, FusedPlan& p1, int& c1, FusedPlan& p2, int& c2, cudaError_t& err) {
+  if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
+    return false;
+  } else {
+    int dev = 0, sms = 0;
+    if (!balanced_allowed() || (err = device_sms(dev, sms)) != cudaSuccess || !make_split(a, sms, sp)) return false;
+    c1 = fused_ctas<T, NPAD, true, ZOH, false, kCarries>(a, (long long)sp.ncarry * a.batch, p1, dev, err);
+    if (err != cudaSuccess || c1 == 0) return false;
+    c2 = fused_ctas<T, NPAD, true, ZOH, false, kSegments>(a, (long long)sp.segs * a.batch, p2, dev, err);
+    return err == cudaSuccess && c2 > 0;
+  }
+}
+
+// Runs the split scan when it applies (the 16-byte path, no checkpoints), with its carry buffers
+// in `ws` (workspace_bytes of SplitPlan) or, when ws is null, in a stream-ordered allocation freed
+// after the two launches.  Returns false when the scan should run unsplit.
+template <typename T, int NPAD, bool ZOH>
+bool launch_split(const ScanArgs& a, const TmaMaps& maps, void* ws, cudaStream_t stream, cudaError_t& err) {
+  if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
+    return false;
+  } else {
+    SplitPlan sp;
+    FusedPlan p1, p2;
+    int c1 = 0, c2 = 0;
+    if (!split_plans<T, NPAD, ZOH>(a, sp, p1, c1, p2, c2, err)) return err != cudaSuccess;
+    void* buf = ws;
+    if (!buf && cudaMallocAsync(&buf, sp.workspace_bytes, stream) != cudaSuccess) {
+      (void)cudaGetLastError();  // the unsplit scan runs instead
+      return false;
+    }
+    ScanArgs c = a;
+    c.carry_h = static_cast<float*>(buf);
+    c.carry_d = c.carry_h + size_t(sp.ncarry) * a.batch * a.dim * a.dstate;
+    c.seg_len = sp.carry_len, c.seg_carries = 0;
+    err = launch_fused_plan<T, NPAD, true, ZOH, false, kCarries>(c, maps, p1, c1, stream);
+    if (err == cudaSuccess) {
+      const long long per = (long long)a.batch * a.dim * a.dstate;
+      int ncarry = sp.ncarry;
+      void* params[] = {&c, &ncarry};
+      err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_carry_combine_kernel), dim3(unsigned((per + 255) / 256)),
+                             dim3(256), params, 0, stream);
+    }
+    if (err == cudaSuccess) {
+      c.seg_len = sp.seg_len, c.seg_carries = sp.carries_per_seg;
+      err = launch_fused_plan<T, NPAD, true, ZOH, false, kSegments>(c, maps, p2, c2, stream);
+    }
+    if (!ws) {
+      const cudaError_t ferr = cudaFreeAsync(buf, stream);
+      if (err == cudaSuccess) err = ferr;
+    }
+    return true;
+  }
 }
 
 template <typename T, int NPAD, bool VEC, bool ZOH, bool CK>
@@ -823,6 +1035,9 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   }
   {
     cudaError_t err = cudaSuccess;
+    if constexpr (VEC && !CK) {
+      if (launch_split<T, NPAD, ZOH>(a, maps, nullptr, stream, err)) return err;
+    }
     if (launch_fused<T, NPAD, VEC, ZOH, CK>(a, maps, stream, err)) return err;
   }
   auto kernel = scan_fwd_kernel<T, NPAD, VEC, ZOH, CK>;
@@ -878,6 +1093,20 @@ bool rows_vectorisable(const ScanArgs& a) {
          al(a.y) && (long long)a.batch * a.dim < (1LL << 31) && (long long)a.batch * a.dstate < (1LL << 31);
 }
 
+// The split for `a` and the grid of its full pass, or segs = 0.
+cudaError_t split_form(const ScanArgs& a, bool vec, SplitPlan& p, int& ctas) {
+  cudaError_t err = cudaSuccess;
+  p = SplitPlan{};
+  ctas = 0;
+  if (vec && a.io == kBF16 && a.dstate > 8 && !a.ckpt) {
+    FusedPlan p1, p2;
+    int c1 = 0;
+    const bool split = a.zoh ? split_plans<__nv_bfloat16, 16, true>(a, p, p1, c1, p2, ctas, err)
+                             : split_plans<__nv_bfloat16, 16, false>(a, p, p1, c1, p2, ctas, err);
+    if (!split) p = SplitPlan{}, ctas = 0;
+  }
+  return err;
+}
 
 }  // namespace
 
@@ -887,15 +1116,26 @@ cudaError_t launch_scan_fwd_quad(const ScanArgs& a, bool vec, cudaStream_t strea
   return vec ? dispatch_disc<__nv_bfloat16, true>(a, stream) : dispatch_disc<__nv_bfloat16, false>(a, stream);
 }
 
+cudaError_t scan_fwd_split(const ScanArgs& a, bool vec, SplitPlan& p) {
+  int ctas = 0;
+  return split_form(a, vec, p, ctas);
+}
+
 cudaError_t scan_fwd_form(const ScanArgs& a, bool vec, int& form, int& ctas) {
   cudaError_t err = cudaSuccess;
   int c = 0, dev = 0;
   if (a.io == kBF16 && a.dstate > 8) {
+    SplitPlan sp;
+    if ((err = split_form(a, vec, sp, c)) != cudaSuccess) return err;
+    if (sp.segs > 0) {
+      form = kFormSplit, ctas = c;
+      return cudaSuccess;
+    }
     FusedPlan plan;
-    c = vec ? (a.zoh ? fused_ctas<__nv_bfloat16, 16, true, true, false>(a, plan, dev, err)
-                     : fused_ctas<__nv_bfloat16, 16, true, false, false>(a, plan, dev, err))
-            : (a.zoh ? fused_ctas<__nv_bfloat16, 16, false, true, false>(a, plan, dev, err)
-                     : fused_ctas<__nv_bfloat16, 16, false, false, false>(a, plan, dev, err));
+    c = vec ? (a.zoh ? fused_ctas<__nv_bfloat16, 16, true, true, false>(a, a.batch, plan, dev, err)
+                     : fused_ctas<__nv_bfloat16, 16, true, false, false>(a, a.batch, plan, dev, err))
+            : (a.zoh ? fused_ctas<__nv_bfloat16, 16, false, true, false>(a, a.batch, plan, dev, err)
+                     : fused_ctas<__nv_bfloat16, 16, false, false, false>(a, a.batch, plan, dev, err));
     if (err != cudaSuccess) return err;
   }
   form = c > 0 ? kFormBalanced : kFormPlain;

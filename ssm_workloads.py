@@ -85,9 +85,13 @@ SMALL = ScanWorkload("small_f32_b2_d32_n16_l64", 2, 32, 16, 64, "f32", 1, gate=T
 MID = ScanWorkload("mid_bf16_b8_d1536_n16_l2048", 8, 1536, 16, 2048, "bf16", 2, gate=True, D_mode="ones")
 LONG = ScanWorkload("long_bf16_b1_d5120_n16_l65536", 1, 5120, 16, 65536, "bf16", 3, gate=True, D_mode="ones",
                     u_std=0.5, generator="device")
+# One 64K-token document through a layer of the mid workload's width (d_inner 1536): few channels
+# for a long sequence, the case the split scan serves.  Distributions as the long workload.
+LONG_NARROW = ScanWorkload("long_bf16_b1_d1536_n16_l65536", 1, 1536, 16, 65536, "bf16", 5, gate=True,
+                           D_mode="ones", u_std=0.5, generator="device")
 DECODE = DecodeWorkload("decode_bf16_b256_d5120_n16_x1024", 256, 5120, 16, 1024, "bf16", 4)
 
-SCAN_WORKLOADS = {w.name: w for w in (TINY, SMALL, MID, LONG)}
+SCAN_WORKLOADS = {w.name: w for w in (TINY, SMALL, MID, LONG, LONG_NARROW)}
 
 
 def _io_dtype(io: str) -> torch.dtype:
