@@ -36,10 +36,12 @@
  * Conventions shared by every entry point
  *  - Every pointer is a DEVICE pointer owned by the caller.  The library keeps no
  *    global state between calls and allocates nothing, with one exception: a scan
- *    that runs split (SSM_FORM_SPLIT below) takes its carry buffers (about
- *    4 * (dstate + 1) bytes per batch row, channel and carry segment) from the
- *    device's default memory pool with cudaMallocAsync on `stream` and returns them
- *    with cudaFreeAsync on the same stream after its last launch.
+ *    that runs split (SSM_FORM_SPLIT below) through an entry point without a
+ *    workspace argument takes its carry buffers (4 * (dstate + 1) bytes per batch
+ *    row, channel and carry segment) from the device's default memory pool with
+ *    cudaMallocAsync on `stream` and returns them with cudaFreeAsync on the same
+ *    stream after its last launch.  ssm_scan_fwd_ws takes them from the caller
+ *    and never allocates.
  *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream).  Kernel-time errors surface on the caller's next
  *    synchronisation of that stream.
@@ -59,6 +61,8 @@
  */
 #ifndef SSM_SCAN_H_
 #define SSM_SCAN_H_
+
+#include <stddef.h>
 
 #ifdef __cplusplus
 extern "C" {
@@ -91,7 +95,7 @@ typedef enum { SSM_F32 = 0, SSM_BF16 = 1 } ssm_dtype;
 typedef enum { SSM_DISC_DELTA_B = 0, SSM_DISC_ZOH = 1 } ssm_discretization;
 
 /* Version of this ABI (bumped when a signature changes, an entry point is added or a layout
- * changes): 6. */
+ * changes): 7. */
 int ssm_abi_version(void);
 
 /*
@@ -158,6 +162,27 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void
 typedef enum { SSM_FORM_PLAIN = 0, SSM_FORM_BALANCED = 1, SSM_FORM_SPLIT = 2 } ssm_scan_form;
 int ssm_scan_fwd_form(int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization, int aligned_rows,
                       int* ctas);
+
+/*
+ * ssm_scan_fwd_ex with caller-owned scratch: it never allocates.  A scan that runs split
+ * (SSM_FORM_SPLIT) keeps its carry buffers in `workspace`: device memory, 16-byte aligned, of at
+ * least the bytes ssm_scan_fwd_workspace_size reports for these sizes, overlapping no other
+ * argument (SSM_ERR_ALIGN / SSM_ERR_ARG otherwise), and left alone until the scan has completed on
+ * `stream`.  With a NULL workspace or fewer bytes the scan runs unsplit, with the same results as
+ * SSM_SCAN_SPLIT=off.  Other arguments and the return as ssm_scan_fwd_ex.
+ */
+int ssm_scan_fwd_ws(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
+                    void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace a scan of these sizes uses on the current device (0 when it does not run
+ * split); aligned_rows as for ssm_scan_fwd_form.  *bytes is required.  Returns an ssm_status
+ * (SSM_ERR_LAUNCH when no device can be queried).
+ */
+int ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
+                                int aligned_rows, size_t* bytes);
 
 /*
  * Training forward: ssm_scan_fwd_h0 (Delta*B discretization) that also stores, for the backward

@@ -17,7 +17,7 @@ import torch
 from . import _native
 from ._native import SsmError, lib, status_string  # noqa: F401
 
-__all__ = ["ssm_scan_fwd", "prepare_scan_fwd", "scan_fwd_form", "wait_timeouts", "ssm_scan_bwd", "scan_num_checkpoints", "ssm_state_update",
+__all__ = ["ssm_scan_fwd", "prepare_scan_fwd", "scan_fwd_form", "scan_fwd_workspace_size", "wait_timeouts", "ssm_scan_bwd", "scan_num_checkpoints", "ssm_state_update",
            "causal_conv1d_fwd", "causal_conv1d_update", "probe_unit_rates", "SsmError", "lib", "status_string",
            "io_dtype_code"]
 
@@ -63,14 +63,18 @@ def scan_num_checkpoints(seqlen: int) -> int:
 
 
 def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, y=None, last_state=None,
-                 h0=None, return_last_state=True, stream=None, discretization="delta_b", checkpoints=None):
-    """Selective scan forward (``ssm_scan_fwd`` / ``_h0`` / ``_ex`` / ``_train`` of the C-ABI).
+                 h0=None, return_last_state=True, stream=None, discretization="delta_b", checkpoints=None,
+                 workspace=None):
+    """Selective scan forward (``ssm_scan_fwd`` / ``_h0`` / ``_ex`` / ``_ws`` / ``_train`` of the C-ABI).
 
     u, delta, z: [batch, dim, L]; B, C: [batch, dstate, L] (float32 or bfloat16, all the same);
     A: [dim, dstate], D, dt_bias: [dim], h0: [batch, dim, dstate] (float32).
     discretization: "delta_b" (Bbar = Delta B) or "zoh" (exact zero-order hold).
     checkpoints: a float32 [batch, scan_num_checkpoints(L), dim, dstate] tensor to receive the
     chunk-start states for ssm_scan_bwd (training forward, either discretization).
+    workspace: a contiguous CUDA tensor (any dtype) for the carry buffers of the split form
+    (``ssm_scan_fwd_ws``: the library then allocates nothing; ``scan_fwd_workspace_size`` gives
+    the bytes it needs, and with fewer the scan runs unsplit).  Not with checkpoints.
     Returns (y, last_state); y has u's dtype, last_state is float32 (None if not requested).
     """
     disc = _disc(discretization)
@@ -98,7 +102,13 @@ def ssm_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus
         batch, dim, dstate, L, io, _stream(stream),
     ]
     h0p = _ptr(h0, torch.float32, (batch, dim, dstate), "h0")
-    if checkpoints is not None:
+    if workspace is not None:
+        if checkpoints is not None:
+            raise ValueError("workspace and checkpoints do not go together (the training forward does not split)")
+        wsp = _ptr(workspace, None, None, "workspace")
+        nbytes = workspace.numel() * workspace.element_size()
+        _native.check("ssm_scan_fwd_ws", lib().ssm_scan_fwd_ws(*args, h0p, *tail[:-1], disc, wsp, nbytes, tail[-1]))
+    elif checkpoints is not None:
         ck = _ptr(checkpoints, torch.float32, (batch, scan_num_checkpoints(L), dim, dstate), "checkpoints")
         if disc == _native.SSM_DISC_DELTA_B:
             _native.check("ssm_scan_fwd_train", lib().ssm_scan_fwd_train(*args, h0p, tail[0], tail[1], ck, *tail[2:]))
@@ -134,11 +144,12 @@ class PreparedCall:
 
 
 def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_softplus=True, y=None, last_state=None,
-                     h0=None, return_last_state=True, stream=None, discretization="delta_b") -> PreparedCall:
-    """``ssm_scan_fwd_ex`` with every argument checked and marshalled once, for callers that repeat
-    the same scan on the same buffers (a benchmark loop, a fixed serving shape): the returned
-    PreparedCall enqueues it with one foreign call and nothing else.  Arguments as ssm_scan_fwd;
-    ``.outputs`` is (y, last_state)."""
+                     h0=None, return_last_state=True, stream=None, discretization="delta_b",
+                     workspace=None) -> PreparedCall:
+    """``ssm_scan_fwd_ex`` (``ssm_scan_fwd_ws`` with a workspace) with every argument checked and
+    marshalled once, for callers that repeat the same scan on the same buffers (a benchmark loop, a
+    fixed serving shape): the returned PreparedCall enqueues it with one foreign call and nothing
+    else.  Arguments as ssm_scan_fwd; ``.outputs`` is (y, last_state)."""
     disc = _disc(discretization)
     batch, dim, L = u.shape
     dstate = A.shape[1]
@@ -160,9 +171,25 @@ def prepare_scan_fwd(u, delta, A, B, C, D=None, z=None, dt_bias=None, delta_soft
         _ptr(h0, torch.float32, (batch, dim, dstate), "h0"),
         _ptr(y, u.dtype, (batch, dim, L), "y"),
         _ptr(last_state, torch.float32, (batch, dim, dstate), "last_state"),
-        batch, dim, dstate, L, io, disc, _stream(stream),
+        batch, dim, dstate, L, io, disc,
     )
-    return PreparedCall("ssm_scan_fwd_ex", args, (y, last_state))
+    if workspace is not None:
+        nbytes = workspace.numel() * workspace.element_size()
+        return PreparedCall("ssm_scan_fwd_ws", args + (_ptr(workspace, None, None, "workspace"), nbytes,
+                                                       _stream(stream)), (y, last_state))
+    return PreparedCall("ssm_scan_fwd_ex", args + (_stream(stream),), (y, last_state))
+
+
+def scan_fwd_workspace_size(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bfloat16,
+                            discretization="delta_b", aligned_rows: bool = True) -> int:
+    """Bytes of workspace a scan of these sizes uses on the current device (0 when it runs
+    unsplit): ``ssm_scan_fwd_workspace_size``."""
+    import ctypes
+    n = ctypes.c_size_t(0)
+    _native.check("ssm_scan_fwd_workspace_size",
+                  lib().ssm_scan_fwd_workspace_size(int(batch), int(dim), int(dstate), int(seqlen), io_dtype_code(dtype),
+                                                    _disc(discretization), int(bool(aligned_rows)), ctypes.byref(n)))
+    return int(n.value)
 
 
 def scan_fwd_form(batch: int, dim: int, dstate: int, seqlen: int, dtype=torch.bfloat16, discretization="delta_b",

@@ -59,6 +59,9 @@ SIGNATURES = {
     "ssm_scan_bwd_ex": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _vp, _vp, _fp, _fp, _fp, _fp, _vp,
                              _fp, _fp, _i, _i, _i, _i, _i, _i, _vp]),
     "ssm_scan_fwd_form": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_int)]),
+    "ssm_scan_fwd_ws": (_i, [_vp, _vp, _fp, _vp, _vp, _fp, _vp, _fp, _i, _fp, _vp, _fp, _i, _i, _i, _i, _i, _i, _vp,
+                             ctypes.c_size_t, _vp]),
+    "ssm_scan_fwd_workspace_size": (_i, [_i, _i, _i, _i, _i, _i, _i, ctypes.POINTER(ctypes.c_size_t)]),
     "ssm_wait_timeouts": (_i, [ctypes.POINTER(ctypes.c_ulonglong)]),
     "ssm_probe_cycles": (_i, [_i, _vp, _i, _vp]),
     "ssm_probe_ops_per_cta": (ctypes.c_double, [_i]),

@@ -1,5 +1,7 @@
-// extern "C" entry points of the library: host-side validation, then one launch on the caller's
-// stream.  Nothing here allocates, synchronises or keeps state between calls.
+// extern "C" entry points of the library: host-side validation, then the launches on the caller's
+// stream.  Nothing here synchronises or keeps state between calls; the only allocation is the
+// stream-ordered carry buffer of a split scan called without a workspace (ssm_scan_fwd_ws never
+// allocates).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,7 +25,7 @@ bool overlaps(const void* p, size_t np, const void* q, size_t nq) {
 
 extern "C" {
 
-int ssm_abi_version(void) { return 6; }
+int ssm_abi_version(void) { return 7; }
 
 const char* ssm_status_string(int status) {
   switch (status) {
@@ -47,7 +49,8 @@ namespace {
 int scan_fwd_common(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
                     const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
                     float* last_state, float* ckpt, int batch, int dim, int dstate, int seqlen, int io_dtype,
-                    int discretization, void* stream) {
+                    int discretization, void* stream, bool ws_given = false, void* ws = nullptr,
+                    size_t ws_bytes = 0) {
   if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
   if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
   if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
@@ -77,6 +80,16 @@ int scan_fwd_common(const void* u, const void* delta, const float* A, const void
         overlaps(ckpt, nck, u, ny) || overlaps(ckpt, nck, delta, ny))
       return SSM_ERR_ARG;
   }
+  // the workspace is written while every other buffer is in use
+  if (ws_given && ws && ws_bytes > 0) {
+    if (!aligned(ws, 16)) return SSM_ERR_ALIGN;
+    const size_t nA = size_t(dim) * dstate * 4, nd = size_t(dim) * 4;
+    if (overlaps(ws, ws_bytes, u, ny) || overlaps(ws, ws_bytes, delta, ny) || overlaps(ws, ws_bytes, z, ny) ||
+        overlaps(ws, ws_bytes, y, ny) || overlaps(ws, ws_bytes, B, nbc) || overlaps(ws, ws_bytes, C, nbc) ||
+        overlaps(ws, ws_bytes, last_state, nst) || overlaps(ws, ws_bytes, h0, nst) || overlaps(ws, ws_bytes, A, nA) ||
+        overlaps(ws, ws_bytes, D, nd) || overlaps(ws, ws_bytes, dt_bias, nd))
+      return SSM_ERR_ARG;
+  }
 
   ssm::ScanArgs a{};
   a.u = u, a.delta = delta, a.A = A, a.B = B, a.C = C, a.D = D, a.z = z, a.dt_bias = dt_bias, a.h0 = h0;
@@ -86,6 +99,7 @@ int scan_fwd_common(const void* u, const void* delta, const float* A, const void
   a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
   a.zoh = discretization == SSM_DISC_ZOH ? 1 : 0;
   a.ckpt = ckpt;
+  a.ws_given = ws_given ? 1 : 0, a.ws = ws, a.ws_bytes = ws_bytes;
   const cudaError_t err = ssm::launch_scan_fwd(a, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
@@ -100,6 +114,34 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void
                     void* stream) {
   return scan_fwd_common(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, nullptr, batch, dim,
                          dstate, seqlen, io_dtype, discretization, stream);
+}
+
+int ssm_scan_fwd_ws(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* dt_bias, int delta_softplus, const float* h0, void* y,
+                    float* last_state, int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
+                    void* workspace, size_t workspace_bytes, void* stream) {
+  return scan_fwd_common(u, delta, A, B, C, D, z, dt_bias, delta_softplus, h0, y, last_state, nullptr, batch, dim,
+                         dstate, seqlen, io_dtype, discretization, stream, true, workspace, workspace_bytes);
+}
+
+int ssm_scan_fwd_workspace_size(int batch, int dim, int dstate, int seqlen, int io_dtype, int discretization,
+                                int aligned_rows, size_t* bytes) {
+  if (!bytes) return SSM_ERR_NULL;
+  *bytes = 0;
+  if (batch < 0 || dim < 0 || seqlen < 0 || dstate < 1) return SSM_ERR_SHAPE;
+  if (io_dtype != SSM_F32 && io_dtype != SSM_BF16) return SSM_ERR_DTYPE;
+  if (discretization != SSM_DISC_DELTA_B && discretization != SSM_DISC_ZOH) return SSM_ERR_ARG;
+  if (dstate > 16) return SSM_ERR_UNSUPPORTED;
+  if (batch == 0 || dim == 0 || seqlen == 0) return SSM_OK;
+  ssm::ScanArgs a{};
+  a.batch = batch, a.dim = dim, a.dstate = dstate, a.seqlen = seqlen;
+  a.io = io_dtype == SSM_F32 ? ssm::kF32 : ssm::kBF16;
+  a.zoh = discretization == SSM_DISC_ZOH ? 1 : 0;
+  const bool vec = aligned_rows != 0 && (size_t(seqlen) * io_size(io_dtype)) % 16 == 0;
+  ssm::SplitPlan p{};
+  if (ssm::scan_fwd_split(a, vec, p) != cudaSuccess) return SSM_ERR_LAUNCH;
+  *bytes = p.segs > 0 ? p.workspace_bytes : 0;
+  return SSM_OK;
 }
 
 int ssm_scan_num_checkpoints(int seqlen) {

@@ -56,6 +56,11 @@ struct ScanArgs {
   int seg_carries;
   float* carry_h;  // [carry segment][batch][dim][dstate]
   float* carry_d;  // [carry segment][batch][dim]
+  // Caller-owned scratch for the split (ws_given: never allocate; the split runs only when ws holds
+  // its carry buffers).  Without it the launcher takes them from a stream-ordered allocation.
+  void* ws;
+  size_t ws_bytes;
+  int ws_given;
 };
 
 // Steps per chunk of the scan kernels, and the interval of the training forward's checkpoints

@@ -984,10 +984,11 @@ bool split_plans(const ScanArgs& a, SplitPlan& sp, FusedPlan& p1, int& c1, Fused
 }
 
 // Runs the split scan when it applies (the 16-byte path, no checkpoints), with its carry buffers
-// in `ws` (workspace_bytes of SplitPlan) or, when ws is null, in a stream-ordered allocation freed
-// after the two launches.  Returns false when the scan should run unsplit.
+// in the caller's workspace (a.ws_given: the split runs only if a.ws holds SplitPlan's
+// workspace_bytes) or else in a stream-ordered allocation freed after the launches.  Returns false
+// when the scan should run unsplit.
 template <typename T, int NPAD, bool ZOH>
-bool launch_split(const ScanArgs& a, const TmaMaps& maps, void* ws, cudaStream_t stream, cudaError_t& err) {
+bool launch_split(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, cudaError_t& err) {
   if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
     return false;
   } else {
@@ -995,8 +996,11 @@ bool launch_split(const ScanArgs& a, const TmaMaps& maps, void* ws, cudaStream_t
     FusedPlan p1, p2;
     int c1 = 0, c2 = 0;
     if (!split_plans<T, NPAD, ZOH>(a, sp, p1, c1, p2, c2, err)) return err != cudaSuccess;
-    void* buf = ws;
-    if (!buf && cudaMallocAsync(&buf, sp.workspace_bytes, stream) != cudaSuccess) {
+    void* buf = nullptr;
+    if (a.ws_given) {
+      if (!a.ws || a.ws_bytes < sp.workspace_bytes) return false;  // no room: unsplit
+      buf = a.ws;
+    } else if (cudaMallocAsync(&buf, sp.workspace_bytes, stream) != cudaSuccess) {
       (void)cudaGetLastError();  // the unsplit scan runs instead
       return false;
     }
@@ -1016,7 +1020,7 @@ bool launch_split(const ScanArgs& a, const TmaMaps& maps, void* ws, cudaStream_t
       c.seg_len = sp.seg_len, c.seg_carries = sp.carries_per_seg;
       err = launch_fused_plan<T, NPAD, true, ZOH, false, kSegments>(c, maps, p2, c2, stream);
     }
-    if (!ws) {
+    if (!a.ws_given) {
       const cudaError_t ferr = cudaFreeAsync(buf, stream);
       if (err == cudaSuccess) err = ferr;
     }
@@ -1036,7 +1040,7 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t stream) {
   {
     cudaError_t err = cudaSuccess;
     if constexpr (VEC && !CK) {
-      if (launch_split<T, NPAD, ZOH>(a, maps, nullptr, stream, err)) return err;
+      if (launch_split<T, NPAD, ZOH>(a, maps, stream, err)) return err;
     }
     if (launch_fused<T, NPAD, VEC, ZOH, CK>(a, maps, stream, err)) return err;
   }

@@ -33,7 +33,8 @@ def test_header_declares_the_boundary():
         ["ssm_abi_version", "ssm_scan_fwd", "ssm_scan_fwd_h0", "ssm_scan_fwd_ex", "ssm_state_update",
          "ssm_state_update_ex", "ssm_status_string", "ssm_causal_conv1d_fwd", "ssm_causal_conv1d_update",
          "ssm_scan_num_checkpoints", "ssm_scan_fwd_train", "ssm_scan_fwd_train_ex", "ssm_scan_bwd",
-         "ssm_scan_bwd_ex", "ssm_probe_cycles", "ssm_probe_ops_per_cta", "ssm_scan_fwd_form", "ssm_wait_timeouts"])
+         "ssm_scan_bwd_ex", "ssm_probe_cycles", "ssm_probe_ops_per_cta", "ssm_scan_fwd_form", "ssm_wait_timeouts",
+         "ssm_scan_fwd_ws", "ssm_scan_fwd_workspace_size"])
 
 
 def test_library_exports_every_declared_symbol(lib):
@@ -43,7 +44,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_status_strings(lib):
-    assert lib.ssm_abi_version() == 6
+    assert lib.ssm_abi_version() == 7
     for code in range(-8, 1):
         s = lib.ssm_status_string(code).decode()
         assert s and s != "unknown status"
@@ -304,3 +305,49 @@ def test_scan_output_may_not_overlap_an_input(lib):
     n = 2 * 3 * 5 * 4
     assert lib.ssm_scan_fwd(*scan_args(**{**disjoint, "y": P + n - 4})) == _native.SSM_ERR_ARG
     assert lib.ssm_scan_fwd(*scan_args(**{**disjoint, "y": P + n})) in (_native.SSM_OK, _native.SSM_ERR_LAUNCH)
+
+
+def ws_args(ws, nbytes, **over):
+    """ssm_scan_fwd_ws arguments: ssm_scan_fwd's plus h0 (none), the discretization and a workspace."""
+    args = scan_args(**over)
+    return args[:9] + [None] + args[9:16] + [_native.SSM_DISC_DELTA_B, ws, nbytes, args[16]]
+
+
+def test_workspace_scan_validation(lib):
+    """ssm_scan_fwd_ws validates like ssm_scan_fwd_ex, and its workspace must be 16-byte aligned and
+    overlap no other argument; a NULL workspace is allowed (the scan then runs unsplit)."""
+    MB = 1 << 20
+    disjoint = dict(u=P, delta=P + MB, z=P + 2 * MB, B=P + 3 * MB, C=P + 4 * MB, y=P + 5 * MB, last=P + 6 * MB,
+                    A=P + 7 * MB, D=P + 8 * MB, dt_bias=P + 9 * MB)
+    ws = P + 10 * MB
+    assert lib.ssm_scan_fwd_ws(*ws_args(ws, MB, **disjoint)) in (_native.SSM_OK, _native.SSM_ERR_LAUNCH)
+    assert lib.ssm_scan_fwd_ws(*ws_args(None, 0, **disjoint)) in (_native.SSM_OK, _native.SSM_ERR_LAUNCH)
+    assert lib.ssm_scan_fwd_ws(*ws_args(ws + 8, MB, **disjoint)) == _native.SSM_ERR_ALIGN
+    for k in ("u", "delta", "z", "B", "C", "y", "last", "A", "D", "dt_bias"):
+        assert lib.ssm_scan_fwd_ws(*ws_args(disjoint[k], 64, **disjoint)) == _native.SSM_ERR_ARG, k
+    # a workspace ending inside y's first element overlaps it; one ending right before does not
+    assert lib.ssm_scan_fwd_ws(*ws_args(disjoint["y"] - 64, 65, **disjoint)) == _native.SSM_ERR_ARG
+    assert lib.ssm_scan_fwd_ws(*ws_args(disjoint["y"] - 64, 64, **disjoint)) in (_native.SSM_OK,
+                                                                                _native.SSM_ERR_LAUNCH)
+    assert lib.ssm_scan_fwd_ws(*ws_args(ws, MB, **{**disjoint, "u": None})) == _native.SSM_ERR_NULL
+    assert lib.ssm_scan_fwd_ws(*ws_args(ws, MB, **{**disjoint, "dstate": 17})) == _native.SSM_ERR_UNSUPPORTED
+    args = ws_args(ws, MB, **disjoint)
+    args[17] = 3  # discretization
+    assert lib.ssm_scan_fwd_ws(*args) == _native.SSM_ERR_ARG
+
+
+def test_workspace_size_validation(lib):
+    n = ctypes.c_size_t(123)
+    assert lib.ssm_scan_fwd_workspace_size(1, 64, 16, 8192, 1, 0, 1, None) == _native.SSM_ERR_NULL
+    assert lib.ssm_scan_fwd_workspace_size(-1, 64, 16, 8192, 1, 0, 1, ctypes.byref(n)) == _native.SSM_ERR_SHAPE
+    assert n.value == 0
+    assert lib.ssm_scan_fwd_workspace_size(1, 64, 17, 8192, 1, 0, 1, ctypes.byref(n)) == _native.SSM_ERR_UNSUPPORTED
+    assert lib.ssm_scan_fwd_workspace_size(1, 64, 16, 8192, 9, 0, 1, ctypes.byref(n)) == _native.SSM_ERR_DTYPE
+    assert lib.ssm_scan_fwd_workspace_size(1, 64, 16, 8192, 1, 4, 1, ctypes.byref(n)) == _native.SSM_ERR_ARG
+    assert lib.ssm_scan_fwd_workspace_size(0, 64, 16, 8192, 1, 0, 1, ctypes.byref(n)) == _native.SSM_OK
+    assert n.value == 0
+    # float32 io never splits; with no device the query of a bf16 scan reports SSM_ERR_LAUNCH
+    assert lib.ssm_scan_fwd_workspace_size(1, 64, 16, 8192, 0, 0, 1, ctypes.byref(n)) == _native.SSM_OK
+    assert n.value == 0
+    assert lib.ssm_scan_fwd_workspace_size(1, 64, 16, 8192, 1, 0, 1, ctypes.byref(n)) in (_native.SSM_OK,
+                                                                                         _native.SSM_ERR_LAUNCH)

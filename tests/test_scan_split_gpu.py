@@ -152,3 +152,68 @@ def test_split_stream_capture(monkeypatch):
         g.replay()
         torch.cuda.synchronize()
         check_oracle(y, last, inp, what="graph replay")
+
+
+def workspace_for(inp, disc="delta_b"):
+    """A float32 workspace of the bytes the scan of `inp` reports, and that byte count."""
+    batch, dim, L = inp["u"].shape
+    N = inp["A"].shape[1]
+    n = ssm.scan_fwd_workspace_size(batch, dim, N, L, inp["u"].dtype, disc)
+    return torch.empty(n // 4, dtype=torch.float32, device=DEV), n
+
+
+def test_workspace_size(monkeypatch):
+    """Split shapes need 4 (dstate + 1) bytes per batch row, channel and carry segment; others none."""
+    set_split(monkeypatch, None)
+    for (batch, dim, N, L) in SHAPES:
+        n = ssm.scan_fwd_workspace_size(batch, dim, N, L)
+        assert n > 0 and n % (4 * batch * dim * (N + 1)) == 0, (batch, dim, N, L, n)
+    assert ssm.scan_fwd_workspace_size(8, 1536, 16, 2048) == 0
+    assert ssm.scan_fwd_workspace_size(1, 64, 16, 8192, dtype=torch.float32) == 0
+    set_split(monkeypatch, "off")
+    assert ssm.scan_fwd_workspace_size(1, 64, 16, 8192) == 0
+
+
+@pytest.mark.parametrize("disc", ["delta_b", "zoh"])
+def test_workspace_scan_equals_allocating_scan(disc, monkeypatch):
+    """ssm_scan_fwd_ws with the reported workspace runs the same split, bit for bit; with one float
+    too few it runs unsplit, bit for bit the SSM_SCAN_SPLIT=off result."""
+    inp = to_device(wl.random_scan_case(2, 64, 16, 8232, io="bf16", seed=31, h0=True), DEV)
+    ya, sa = run(inp, monkeypatch, None, disc, inp["h0"])
+    ws, n = workspace_for(inp, disc)
+    assert n > 0 and ws.numel() * 4 == n
+    yw, sw = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                              inp["dt_bias"], h0=inp["h0"], discretization=disc, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(ya, yw) and torch.equal(sa, sw)
+    small = torch.empty(n // 4 - 1, dtype=torch.float32, device=DEV)
+    ys, ss = ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                              inp["dt_bias"], h0=inp["h0"], discretization=disc, workspace=small)
+    torch.cuda.synchronize()
+    yo, so = run(inp, monkeypatch, "off", disc, inp["h0"])
+    assert torch.equal(ys, yo) and torch.equal(ss, so)
+    check_oracle(yw, sw, inp, disc, inp["h0"], "workspace")
+
+
+def test_workspace_scan_in_a_graph(monkeypatch):
+    """With a workspace the split enqueues kernels only, so a captured graph of it replays with no
+    allocation node; replayed twice against the oracle."""
+    inp = to_device(wl.random_scan_case(1, 64, 16, 8192, io="bf16", seed=17), DEV)
+    set_split(monkeypatch, None)
+    ws, n = workspace_for(inp)
+    y = torch.empty_like(inp["u"])
+    last = torch.empty((1, 64, 16), dtype=torch.float32, device=DEV)
+    s = torch.cuda.Stream()
+    call = ssm.prepare_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"],
+                                inp["dt_bias"], y=y, last_state=last, workspace=ws, stream=s)
+    torch.cuda.synchronize()
+    call()
+    s.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for _ in range(2):
+        y.zero_(), last.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        check_oracle(y, last, inp, what="workspace graph replay")
