@@ -804,8 +804,9 @@ def run_decode(device, steps_graph=3, warmup=1):
 
 def profile_mode(which: str) -> int:
     """A few launches of one kernel for an ncu capture: the mid-size scan with either
-    discretisation (about 0.6 GB on the device), the long scan (about 2.7 GB; with its split
-    form, three launches per step), the causal conv1d on the same activation shape
+    discretisation (about 0.6 GB on the device), the long scans (about 2.7 GB, and 0.8 GB for the
+    narrow one, whose split form makes three launches per step: carry pass, combine, segments),
+    the causal conv1d on the same activation shape
     (about 0.1 GB), or decode steps of the decode workload without a graph (about 0.2 GB)."""
     from selective_state_space_155_b300 import build as _build
     _build.build()
@@ -815,6 +816,9 @@ def profile_mode(which: str) -> int:
         fn = run.step
     elif which == "long":
         run = ScanRun(wl.LONG, device, copies=1)
+        fn = run.step
+    elif which == "long_narrow":
+        run = ScanRun(wl.LONG_NARROW, device, copies=1)
         fn = run.step
     elif which == "zoh":
         run = ScanRun(wl.MID, device, copies=1, discretization="zoh")
@@ -865,7 +869,8 @@ def main(argv=None):
     ap.add_argument("--no-zoh", action="store_true")
     ap.add_argument("--no-conv", action="store_true")
     ap.add_argument("--no-train", action="store_true")
-    ap.add_argument("--profile", choices=["scan", "zoh", "long", "bwd", "bwd_zoh", "conv", "decode"], default=None,
+    ap.add_argument("--profile", choices=["scan", "zoh", "long", "long_narrow", "bwd", "bwd_zoh", "conv", "decode"],
+                    default=None,
                     help="run 2 warm-up and 3 profiled launches of one kernel on its workload and exit "
                          "(a small command for ncu; prints no JSON line)")
     args = ap.parse_args(argv)

@@ -931,11 +931,12 @@ bool launch_fused(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, c
 // C, z or output) over the carry segments gives each one's end state from a zero state and its
 // step-size sum, a combine folds them into the state entering each segment, and the full pass
 // scans every segment from it.  The carry pass costs about 0.7 of the full scan per element over
-// (segments - 1) / segments of the sequence, so the split is taken only where kSegs segments fit the
-// SMs' groups at once (at most 3 units per SM); carry segments per segment (at most kMaxCarries) are
-// as many as the groups hold.  Both lengths are multiples of two chunks.
+// (segments - 1) / segments of the sequence, so the split is taken only where at least
+// kMinSegs segments fit the SMs' groups at once (at most 3 units per SM); then as many segments
+// as fit (up to kMaxPlanSegs), and as many carry segments per segment as the groups hold (up to
+// kMaxCarries, at most kMaxPlanSegs in all).  Both lengths are multiples of two chunks.
 constexpr int kSplitMinLen = 8192;  // the shortest sequence split (the extra launches must pay)
-constexpr int kSegs = 4, kMaxCarries = 4;
+constexpr int kMinSegs = 4, kMaxCarries = 4;
 
 bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   p = SplitPlan{};
@@ -946,7 +947,7 @@ bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   if (h0 && ls && h0 < ls + nst && ls < h0 + nst) return false;
   const long long units = (long long)a.batch * (a.dim / 8), cap = (long long)sms * kFusedGroups * 4;
   if (units == 0) return false;
-  long long segs = kSegs, per = 0;
+  long long segs = std::min<long long>(kMaxPlanSegs, cap / units), per = 0;
   const char* force = std::getenv("SSM_SCAN_SPLIT");
   if (force && std::strcmp(force, "off") == 0) return false;
   int fs = 0, fr = 0;
@@ -954,8 +955,9 @@ bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
     segs = fs, per = fr;  // forced (for measurements and tests)
     if (units * segs > cap || units * (segs - 1) * per > cap) return false;
   } else {
-    if (units * segs > cap) return false;
-    per = std::min<long long>(kMaxCarries, cap / (units * (segs - 1)));
+    if (segs < kMinSegs) return false;
+    per = std::min<long long>(std::min<long long>(kMaxCarries, cap / (units * (segs - 1))),
+                              kMaxPlanSegs / (segs - 1));
   }
   const long long step = 2 * kChunk;
   const long long clen = ((a.seqlen + segs * per - 1) / (segs * per) + step - 1) / step * step;
