@@ -686,8 +686,14 @@ def run_long_narrow(device, steps=10, warmup=3):
     hbm, _ = measured_peaks()
     nbytes = w.algorithmic_bytes()
     gbs = nbytes / (ms * 1e-3) / 1e9
+    # DRAM bytes of one step's three launches (carry pass, combine, segments) from the committed
+    # capture of this workload; the carry pass re-reads u, delta and B for most of the sequence
+    parts = [committed_traffic(k) for k in ("scan_fwd_fused_kernel_carry_long_narrow",
+                                            "scan_carry_combine_kernel_long_narrow",
+                                            "scan_fwd_fused_kernel_segments_long_narrow")]
+    dram = sum(parts) if form == "split" and all(v is not None for v in parts) else None
     return {"workload": w.name, "form": form, "us_per_step": ms * 1e3, "elements_per_s": w.elements / (ms * 1e-3),
-            "workspace_us_per_step": ms_ws * 1e3,
+            "dram_bytes_per_step": dram, "workspace_us_per_step": ms_ws * 1e3,
             "algorithmic_bytes_per_launch": nbytes, "hbm_gbs": gbs, "frac_of_hbm": gbs / hbm,
             "unsplit_us_per_step": ms_off * 1e3, "split_speedup": ms_off / ms, "steps": steps,
             "l2": "one input set of 0.6 GB (above L2)"}
