@@ -313,6 +313,50 @@ def test_resume_from_last_state():
     np.testing.assert_array_equal(lb, last)
 
 
+def test_segment_carries_combine_to_the_sequential_scan():
+    """The split scan's decomposition, in float64: each segment scanned from a zero state (the first
+    from h0) gives its end state, its decay is exp(A * sum of its Delta), and folding the (decay,
+    end state) pairs with the pair operator (53ai.com section 3.3) gives the state entering every
+    segment; scanning each segment from that state reproduces the sequential scan's y and final
+    state.  The sums of Delta come from softplus(delta + dt_bias) written out here, not from the
+    scan."""
+    rng = np.random.default_rng(23)
+    batch, dim, N, L, seg = 2, 3, 8, 96, 24
+    A = -np.exp(rng.uniform(-3.0, 0.5, size=(dim, N)))  # slow decays: the carries matter
+    u, delta, z = (rng.standard_normal((batch, dim, L)) for _ in range(3))
+    B, C = (rng.standard_normal((batch, N, L)) for _ in range(2))
+    D = rng.standard_normal(dim)
+    bias = rng.uniform(-5.0, -3.0, size=dim)
+    h0 = rng.standard_normal((batch, dim, N))
+    y, last = oracle.scan(u, delta, A, B, C, D=D, z=z, dt_bias=bias, h0=h0)
+    sl = [slice(k, k + seg) for k in range(0, L, seg)]
+    ends, decays = [], []
+    for j, s_ in enumerate(sl):
+        _, h_end = oracle.scan(u[..., s_], delta[..., s_], A, B[..., s_], C[..., s_], D=D, z=z[..., s_],
+                               dt_bias=bias, h0=h0 if j == 0 else None)
+        x = delta[..., s_] + bias[None, :, None]
+        dsum = np.sum(np.maximum(x, 0.0) + np.log1p(np.exp(-np.abs(x))), axis=-1)  # (batch, dim)
+        ends.append(h_end)
+        decays.append(np.exp(A[None, :, :] * dsum[:, :, None]))
+    starts = np.zeros((len(sl), batch, dim, N))
+    for b in range(batch):
+        for d in range(dim):
+            for n in range(N):
+                _, hs = oracle.assoc_scan([dk[b, d, n] for dk in decays], [ek[b, d, n] for ek in ends])
+                starts[:, b, d, n] = hs  # state after segment j (segment 0 started from h0)
+    ys = []
+    for j, s_ in enumerate(sl):
+        yj, lj = oracle.scan(u[..., s_], delta[..., s_], A, B[..., s_], C[..., s_], D=D, z=z[..., s_],
+                             dt_bias=bias, h0=h0 if j == 0 else starts[j - 1])
+        ys.append(yj)
+    np.testing.assert_allclose(np.concatenate(ys, axis=-1), y, rtol=1e-11, atol=1e-12)
+    np.testing.assert_allclose(lj, last, rtol=1e-11, atol=1e-12)
+    # the carries are not negligible here: without them the later segments differ
+    y_nocarry, _ = oracle.scan(u[..., sl[-1]], delta[..., sl[-1]], A, B[..., sl[-1]], C[..., sl[-1]], D=D,
+                               z=z[..., sl[-1]], dt_bias=bias)
+    assert np.max(np.abs(y_nocarry - y[..., sl[-1]])) > 1e-3
+
+
 def test_empty_and_thread_count_independence():
     rng = np.random.default_rng(23)
     A = -np.ones((3, 2))
