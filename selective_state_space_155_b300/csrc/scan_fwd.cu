@@ -41,6 +41,13 @@
 //    Delta = 0.  Both leave the state unchanged, so one code path serves every size.
 //  * With a checkpoint buffer (the training forward, its own instantiation), the recurrence lanes
 //    also store the state before every 8th step, which is what the backward pass restarts from.
+//  * Few channels and a long sequence leave an SM one warp group, which is latency-bound.  The
+//    split form then scans segments of the sequence side by side: a carry pass (the same groups
+//    without C, z or output) gives each carry segment's end state from zero and its sum of Delta, a
+//    small kernel folds them with the associative pair operator (a1, b1) o (a2, b2) =
+//    (a1 a2, a2 b1 + b2) into the state entering each segment (the parallel associative scan of the
+//    53ai.com Mamba article, section 3.3, applied once per segment), and the segment pass scans
+//    every segment from it.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
