@@ -159,6 +159,9 @@ cudaError_t scan_fwd_form(const ScanArgs& a, bool vec, int& form, int& ctas);
 // when the scan is not split.
 struct SplitPlan {
   int segs, carries_per_seg, seg_len, carry_len, ncarry;
+  // whole_groups > 0: only the tail of the last batch row (8-channel units from tail_p0 on) is
+  // split; the other units run whole rows, whole_groups 4-unit groups per SM, in the segment pass
+  int whole_groups, tail_p0;
   size_t workspace_bytes;
 };
 cudaError_t scan_fwd_split(const ScanArgs& a, bool vec, SplitPlan& p);

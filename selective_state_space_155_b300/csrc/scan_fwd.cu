@@ -242,8 +242,14 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   const int warp = tid >> 5, lane = tid & 31;
   const int L = a.seqlen, N = a.dstate;
   const bool has_z = !CARRY && a.z != nullptr;
-  const int nchunks = SEGS ? kc1 - kc0 : (L + kChunk - 1) / kChunk;  // chunks of the group's range
-  const int T0 = SEGS ? kc0 * kChunk : 0;                              // its first step
+  // The group's chunk count and first step.  For a segment they are kept in the group's shared
+  // words and read where used (a few loads per chunk), not held in registers across the loops: both
+  // warp roles are at their register limits, and for whole rows they are constants or
+  // kernel-parameter expressions the compiler recomputes for free.
+  volatile int* gvals = reinterpret_cast<volatile int*>(smem + Cfg::kBarOfs + 6 * sizeof(uint64_t)) + 1;
+  if (SEGS && tid == 0) gvals[0] = kc1 - kc0, gvals[1] = kc0 * kChunk;  // read after the init barrier
+  auto n_chunks = [&]() -> int { return SEGS ? gvals[0] : (L + kChunk - 1) / kChunk; };
+  auto t_first = [&]() -> int { return SEGS ? gvals[1] : 0; };
 
   // mbarriers: FULL[s] completes when the prep threads have written table stage s (one arrival
   // after their closing barrier), EMPTY[s] when every recurrence warp holding a channel of the
@@ -372,7 +378,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
     // still in flight.
     volatile int* decide = reinterpret_cast<volatile int*>(smem + Cfg::kBarOfs + 6 * sizeof(uint64_t));
     const bool tma_ok = (smem_u32(raw) & 127u) == 0;  // tensor copies need a 128-byte aligned destination
-    const int nstages = (nchunks + (1 << lg) - 1) >> lg;  // raw-stage uses
+    auto n_stages = [&]() { return (n_chunks() + (1 << lg) - 1) >> lg; };  // raw-stage uses
     int pend0 = -1, pend1 = -1;
     if (VEC && !tma_ok && ptid == 0) {
       *abort = 1;  // give up at once rather than copy
@@ -380,19 +386,19 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
     }
     if (VEC && tma_ok) {
       if (ptid == 0) {
-        if (nstages > 0) mbar_arrive_expect_tx(&mb[4], stage_bytes), pend0 = 0;
-        if (nstages > 1) mbar_arrive_expect_tx(&mb[5], stage_bytes), pend1 = 1;
+        if (n_stages() > 0) mbar_arrive_expect_tx(&mb[4], stage_bytes), pend0 = 0;
+        if (n_stages() > 1) mbar_arrive_expect_tx(&mb[5], stage_bytes), pend1 = 1;
       }
       bar_sync(bPrep, PT);
       if (lane == 0) {
-        if (nstages > 0) issue_copies(0, T0);
-        if (nstages > 1) issue_copies(1, T0 + (kChunk << lg));
+        if (n_stages() > 0) issue_copies(0, t_first());
+        if (n_stages() > 1) issue_copies(1, t_first() + (kChunk << lg));
       }
     }
 
-    for (int k = 0; k < nchunks; ++k) {
+    for (int k = 0; k < n_chunks(); ++k) {
       const int s = k & 1;
-      const int t0 = T0 + k * kChunk;
+      const int t0 = t_first() + k * kChunk;
       const int su = k >> lg, rs = su & 1;   // raw-stage use and raw stage of chunk k
       const int slot = k & ((1 << lg) - 1);  // its slot within the stage
       if (VEC) {
@@ -460,15 +466,15 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
         }
       }
 
-      const bool last_of_stage = slot == (1 << lg) - 1 || k == nchunks - 1;
+      const bool last_of_stage = slot == (1 << lg) - 1 || k == n_chunks() - 1;
       if (VEC && ptid == 0 && last_of_stage) {
-        const bool refill = su + 2 < nstages && (rs ? pend1 : pend0) < 0 && !*abort;
+        const bool refill = su + 2 < n_stages() && (rs ? pend1 : pend0) < 0 && !*abort;
         if (refill) mbar_arrive_expect_tx(&mb[4 + rs], stage_bytes), (rs ? pend1 : pend0) = su + 2;
         *decide = refill ? 1 : 0;
       }
       bar_sync(bPrep, PT);  // every prep thread is done reading chunk k; the decision is visible
       if (ptid == 0) mbar_arrive(&mb[s]);  // table stage s is written (the barrier above ordered every prep write)
-      if (VEC && lane == 0 && last_of_stage && *decide) issue_copies(rs, T0 + (su + 2) * (kChunk << lg));
+      if (VEC && lane == 0 && last_of_stage && *decide) issue_copies(rs, t_first() + (su + 2) * (kChunk << lg));
     }
     if (VEC && ptid == 0) {  // these last waits ignore the CTA's give-up flag
       if (pend0 >= 0) mbar_wait(&mb[4], (pend0 >> 1) & 1, nullptr, kWaitLimit, &g_scan_wait_timeouts, kPrepBackoff);
@@ -512,8 +518,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   }
   float dsum = 0.0f;  // the carry pass: sum of this channel's Delta over the segment
   // the output row from the group's first step on, and the steps left in the row from there
-  T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L + T0;
-  const int Lr = L - T0;
+  T* yrow = static_cast<T*>(a.y) + (size_t(b) * a.dim + (ch_ok ? d : 0)) * L + t_first();
 
   // two chunks per iteration: more independent work for the scheduler around the hand-offs (not
   // with the zero-order hold, whose longer step body would then outgrow the instruction cache)
@@ -541,7 +546,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
   };
 
 #pragma unroll kChunkUnroll
-  for (int k = 0; k < nchunks; ++k) {
+  for (int k = 0; k < n_chunks(); ++k) {
     const int s = k & 1;
     const int t0 = k * kChunk;  // from the group's first step
     mbar_wait(&mb[s], (k >> 1) & 1, abort, kWaitLimit, &g_scan_wait_timeouts, kRecBackoff);
@@ -585,7 +590,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       for (int j = 0; j < kWin; ++j) {
         const int t = w + j;
         if constexpr (CK) {
-          if (j % kCkptSteps == 0) checkpoint(T0 + t0 + t);
+          if (j % kCkptSteps == 0) checkpoint(t_first() + t0 + t);
         }
         const float2 p = Ps[cl * PSS + t];
         const float4 bb = *reinterpret_cast<const float4*>(Bs + t * NPAD + 4 * g);
@@ -652,7 +657,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
         ov[j] = o.x, ov[j + 1] = o.y;
       }
       const int tg = t0 + tb;  // first step, from the group's first
-      if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, Lr - tg);
+      if (ch_ok) store_out<T, OPL, VEC>(yrow + tg, ov, L - t_first() - tg);
     }
     __syncwarp();  // every lane of the warp is done reading table stage s ...
     if (lane == 0) mbar_arrive(&mb[2 + s]);  // ... which one arrival (release) then reports
@@ -669,7 +674,7 @@ __device__ __forceinline__ void scan_group(const ScanArgs& a, const TmaMaps& map
       }
       if (g == 0) a.carry_d[row] = dsum;
     }
-  } else if (a.last_state && ch_ok && nchunks * kChunk >= Lr) {  // the last segment holds the final state
+  } else if (a.last_state && ch_ok && n_chunks() * kChunk >= L - t_first()) {  // the last segment ends the row
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int n = 4 * g + i;
@@ -699,8 +704,8 @@ __global__ void __launch_bounds__(ScanCfg<T, NPAD>::NT, 3)
 // j, and the segment's decay is the product of its Abar, exp(A S_j).  Folding the slots left to right
 // with the associative pair operator (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2) leaves in slot j the
 // state after carry segment j, from which the next segment starts; only the running state is kept.
-__global__ void __launch_bounds__(256) scan_carry_combine_kernel(const ScanArgs a, int ncarry) {
-  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+__global__ void __launch_bounds__(256) scan_carry_combine_kernel(const ScanArgs a, int ncarry, long long first) {
+  const long long i = first + (long long)blockIdx.x * blockDim.x + threadIdx.x;  // from the split channels on
   const long long per = (long long)a.batch * a.dim * a.dstate;
   if (i >= per) return;
   const long long row = i / a.dstate;  // b * dim + d
@@ -722,6 +727,8 @@ __global__ void __launch_bounds__(256) scan_carry_combine_kernel(const ScanArgs 
 constexpr int kFusedGroups = 3;
 constexpr int kMaxFusedCtas = 160;
 constexpr int kSegShift = 28, kMaxPlanSegs = 16, kMaxSplitBatch = 1 << 12;
+// segment field of a segment-pass entry that scans its whole row (a split of the tail only)
+constexpr int kWholeSeg = kMaxPlanSegs - 1;
 struct FusedPlan {
   uint32_t e[kFusedGroups * kMaxFusedCtas];
 };
@@ -748,7 +755,11 @@ __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
   if (MODE != kWhole) {
     const int nck = (a.seqlen + kChunk - 1) / kChunk;
     seg = int(e >> kSegShift), b &= kMaxSplitBatch - 1;
-    kc0 = seg * (a.seg_len / kChunk), kc1 = min(nck, kc0 + a.seg_len / kChunk);
+    if (MODE == kSegments && seg == kWholeSeg) {
+      seg = 0, kc1 = nck;  // a whole row beside the split tail: from h0, to the final state
+    } else {
+      kc0 = seg * (a.seg_len / kChunk), kc1 = min(nck, kc0 + a.seg_len / kChunk);
+    }
   }
   scan_group<T, NPAD, VEC, ZOH, CK, MODE != kWhole, MODE == kCarries>(
       a, maps, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0, min(a.dim, d0 + nch), seg, kc0, kc1,
@@ -761,33 +772,45 @@ __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
 // units.  Returns the CTA count, or 0 when the plan does not apply or (with `against_plain`) does
 // not lower the busiest SM's load below that of the plain kernel (32-channel CTAs spread over the
 // SMs; the passes of a split sequence have no plain alternative).
-int make_fused_plan(const ScanArgs& a, long long rows, int sms, FusedPlan& plan, bool against_plain = true) {
+// Fills group slots [slot0, kFusedGroups) of CTAs 0.. with the units at positions [p0, units per
+// row) of `rows` plan rows, CTA c taking ceil(units left / CTAs left).  Plan row r is batch row
+// r % batch of segment r / batch, or, with tail_b >= 0, batch row tail_b of segment r.  Returns the
+// CTA count (0 if the units do not fit) and the busiest CTA's units in `worst`.
+int fill_plan(const ScanArgs& a, long long rows, long long p0, int tail_b, int sms, int slot0, FusedPlan& plan,
+              long long& worst) {
+  worst = 0;
   if (a.dim % 8 != 0 || rows >= (1 << 16) || a.dim / 8 >= (1 << 12) || sms <= 0 || sms > kMaxFusedCtas) return 0;
-  const long long ur = a.dim / 8, units = rows * ur;
-  if (units == 0 || units > (long long)sms * kFusedGroups * 4) return 0;
-  const long long blocks = rows * ((a.dim + 31) / 32);
-  const long long plain_max = 4 * ((blocks + sms - 1) / sms);  // units on the busiest SM, plain kernel
-  long long left = units, row = 0, pos = 0, worst = 0;
+  const long long ur = a.dim / 8, units = rows * (ur - p0);
+  if (units <= 0 || units > (long long)sms * (kFusedGroups - slot0) * 4) return 0;
+  long long left = units, row = 0, pos = p0;
   int ctas = 0;
   for (int c = 0; c < sms && left > 0; ++c) {
     const long long target = (left + (sms - c) - 1) / (sms - c);
     long long load = 0;
-    for (int g = 0; g < kFusedGroups; ++g) {
+    for (int g = slot0; g < kFusedGroups; ++g) {
       uint32_t entry = 0;
       if (load < target && row < rows) {
         const long long take = std::min(std::min(4LL, target - load), ur - pos);
-        // whole rows: row = b; split passes: row = segment * batch + b, segment < 16, batch < 4096
-        entry = uint32_t(row % a.batch) << 16 | uint32_t(row / a.batch) << kSegShift | uint32_t(pos) << 4 |
-                uint32_t(take);
+        // whole rows: row = b; split passes: segment < 16 in the top bits, batch < 4096
+        const long long b = tail_b >= 0 ? tail_b : row % a.batch, sg = tail_b >= 0 ? row : row / a.batch;
+        entry = uint32_t(b) << 16 | uint32_t(sg) << kSegShift | uint32_t(pos) << 4 | uint32_t(take);
         load += take, pos += take, left -= take;
-        if (pos == ur) ++row, pos = 0;
+        if (pos == ur) ++row, pos = p0;
       }
       plan.e[c * kFusedGroups + g] = entry;
     }
     worst = std::max(worst, load);
     ctas = c + 1;
   }
-  return (left == 0 && (worst < plain_max || !against_plain)) ? ctas : 0;
+  return left == 0 ? ctas : 0;
+}
+
+int make_fused_plan(const ScanArgs& a, long long rows, int sms, FusedPlan& plan, bool against_plain = true) {
+  long long worst = 0;
+  const int ctas = fill_plan(a, rows, 0, -1, sms, 0, plan, worst);
+  const long long blocks = rows * ((a.dim + 31) / 32);
+  const long long plain_max = 4 * ((blocks + sms - 1) / sms);  // units on the busiest SM, plain kernel
+  return (ctas > 0 && (worst < plain_max || !against_plain)) ? ctas : 0;
 }
 
 // The driver's tensor-map encoder, looked up once through the runtime (no link against the
@@ -940,8 +963,8 @@ bool launch_fused(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, c
 // scans every segment from it.  The carry pass costs about 0.7 of the full scan per element over
 // (segments - 1) / segments of the sequence, so the split is taken only where at least
 // kMinSegs segments fit the SMs' groups at once (at most 3 units per SM); then as many segments
-// as fit (up to kMaxPlanSegs), and as many carry segments per segment as the groups hold (up to
-// kMaxCarries, at most kMaxPlanSegs in all).  Both lengths are multiples of two chunks.
+// as fit (up to 15), and as many carry segments per segment as the groups hold (up to
+// kMaxCarries, at most 15 in all).  Both lengths are multiples of two chunks.
 constexpr int kSplitMinLen = 8192;  // the shortest sequence split (the extra launches must pay)
 constexpr int kMinSegs = 4, kMaxCarries = 4;
 
@@ -954,25 +977,41 @@ bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   if (h0 && ls && h0 < ls + nst && ls < h0 + nst) return false;
   const long long units = (long long)a.batch * (a.dim / 8), cap = (long long)sms * kFusedGroups * 4;
   if (units == 0) return false;
-  long long segs = std::min<long long>(kMaxPlanSegs, cap / units), per = 0;
+  // segment values below kWholeSeg (which marks whole rows in the segment pass)
+  const long long maxsegs = kWholeSeg;
+  long long segs = std::min<long long>(maxsegs, cap / units), per = 0;
+  long long whole = 0, p0 = 0;  // the split of the tail only (below)
   const char* force = std::getenv("SSM_SCAN_SPLIT");
   if (force && std::strcmp(force, "off") == 0) return false;
   int fs = 0, fr = 0;
   if (force && std::sscanf(force, "%d,%d", &fs, &fr) == 2 && fs >= 2 && fr >= 1) {
     segs = fs, per = fr;  // forced (for measurements and tests)
     if (units * segs > cap || units * (segs - 1) * per > cap) return false;
+  } else if (segs >= kMinSegs) {
+    per = std::min<long long>(std::min<long long>(kMaxCarries, cap / (units * (segs - 1))), maxsegs / (segs - 1));
   } else {
+    // Too many units to split them all, but whole rows would give every SM one full 4-unit group
+    // and some SMs a second, smaller group whose per-chunk costs slow the SM down: run the full
+    // groups on whole rows and split only the tail of the last batch row over the group slots
+    // left free, as many segments as fit.  (With two full groups per SM the balanced plan already
+    // keeps the SMs busy.)
+    const long long ur = a.dim / 8;
+    whole = units / (4LL * sms);
+    const long long tail = units - 4LL * sms * whole;
+    p0 = 4LL * sms * whole - (long long)(a.batch - 1) * ur;  // first tail unit within the last row
+    if (whole != 1 || tail <= 0 || ur % 4 != 0 || p0 < 0) return false;
+    segs = std::min<long long>(maxsegs, (kFusedGroups - whole) * 4LL * sms / tail);
     if (segs < kMinSegs) return false;
-    per = std::min<long long>(std::min<long long>(kMaxCarries, cap / (units * (segs - 1))),
-                              kMaxPlanSegs / (segs - 1));
+    per = std::min<long long>(std::min<long long>(kMaxCarries, cap / (tail * (segs - 1))), maxsegs / (segs - 1));
   }
   const long long step = 2 * kChunk;
   const long long clen = ((a.seqlen + segs * per - 1) / (segs * per) + step - 1) / step * step;
   const long long slen = clen * per;
   const long long nseg = (a.seqlen + slen - 1) / slen;
-  if (nseg < 2 || a.batch >= kMaxSplitBatch || (nseg - 1) * per > kMaxPlanSegs || nseg > kMaxPlanSegs) return false;
+  if (nseg < 2 || a.batch >= kMaxSplitBatch || (nseg - 1) * per > maxsegs || nseg > maxsegs) return false;
   p.segs = int(nseg), p.carries_per_seg = int(per), p.seg_len = int(slen), p.carry_len = int(clen);
   p.ncarry = int((nseg - 1) * per);
+  p.whole_groups = int(whole), p.tail_p0 = int(p0);
   p.workspace_bytes = size_t(p.ncarry) * a.batch * a.dim * (size_t(a.dstate) + 1) * sizeof(float);
   return true;
 }
@@ -984,11 +1023,31 @@ bool split_plans(const ScanArgs& a, SplitPlan& sp, FusedPlan& p1, int& c1, Fused
     return false;
   } else {
     int dev = 0, sms = 0;
+    p1 = FusedPlan{}, p2 = FusedPlan{};
     if (!balanced_allowed() || (err = device_sms(dev, sms)) != cudaSuccess || !make_split(a, sms, sp)) return false;
-    c1 = fused_ctas<T, NPAD, true, ZOH, false, kCarries>(a, (long long)sp.ncarry * a.batch, p1, dev, err);
-    if (err != cudaSuccess || c1 == 0) return false;
-    c2 = fused_ctas<T, NPAD, true, ZOH, false, kSegments>(a, (long long)sp.segs * a.batch, p2, dev, err);
-    return err == cudaSuccess && c2 > 0;
+    if (sp.whole_groups == 0) {
+      c1 = fused_ctas<T, NPAD, true, ZOH, false, kCarries>(a, (long long)sp.ncarry * a.batch, p1, dev, err);
+      if (err != cudaSuccess || c1 == 0) return false;
+      c2 = fused_ctas<T, NPAD, true, ZOH, false, kSegments>(a, (long long)sp.segs * a.batch, p2, dev, err);
+      return err == cudaSuccess && c2 > 0;
+    }
+    // the tail split: the carry pass over the tail's carry segments; the segment pass with
+    // whole_groups whole-row groups of 4 units on every CTA, then the tail's segments
+    const long long ur = a.dim / 8;
+    long long worst = 0;
+    c1 = fill_plan(a, sp.ncarry, sp.tail_p0, a.batch - 1, sms, 0, p1, worst);
+    for (int c = 0; c < sms; ++c)
+      for (int g = 0; g < sp.whole_groups; ++g) {
+        const long long u = (long long)(c * sp.whole_groups + g) * 4;
+        p2.e[c * kFusedGroups + g] = uint32_t(u / ur) << 16 | uint32_t(kWholeSeg) << kSegShift |
+                                     uint32_t(u % ur) << 4 | 4u;
+      }
+    c2 = fill_plan(a, sp.segs, sp.tail_p0, a.batch - 1, sms, sp.whole_groups, p2, worst) > 0 ? sms : 0;
+    if (c1 == 0 || c2 == 0) return false;
+    for (int c = c1; c < sms; ++c)  // CTAs past the carry plan's are not launched
+      for (int g = 0; g < kFusedGroups; ++g) p1.e[c * kFusedGroups + g] = 0;
+    return fused_ready<T, NPAD, true, ZOH, false, kCarries>(dev, err) &&
+           fused_ready<T, NPAD, true, ZOH, false, kSegments>(dev, err);
   }
 }
 
@@ -1019,10 +1078,13 @@ bool launch_split(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, c
     c.seg_len = sp.carry_len, c.seg_carries = 0;
     err = launch_fused_plan<T, NPAD, true, ZOH, false, kCarries>(c, maps, p1, c1, stream);
     if (err == cudaSuccess) {
-      const long long per = (long long)a.batch * a.dim * a.dstate;
+      // the carried states: every channel, or those of the tail of the last batch row
+      long long first = ((long long)(a.batch - 1) * a.dim + 8LL * sp.tail_p0) * a.dstate;
+      if (sp.whole_groups == 0) first = 0;
+      const long long n = (long long)a.batch * a.dim * a.dstate - first;
       int ncarry = sp.ncarry;
-      void* params[] = {&c, &ncarry};
-      err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_carry_combine_kernel), dim3(unsigned((per + 255) / 256)),
+      void* params[] = {&c, &ncarry, &first};
+      err = cudaLaunchKernel(reinterpret_cast<const void*>(scan_carry_combine_kernel), dim3(unsigned((n + 255) / 256)),
                              dim3(256), params, 0, stream);
     }
     if (err == cudaSuccess) {

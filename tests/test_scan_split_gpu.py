@@ -60,8 +60,9 @@ def test_split_form_chosen(monkeypatch):
         assert ssm.scan_fwd_form(*shape)[0] == "split", shape
     assert ssm.scan_fwd_form(*shape, discretization="zoh")[0] == "split"
     assert ssm.scan_fwd_form(1, 2048, 16, 32768)[0] == "split"
-    # the long workload: 640 units, four segments would not fit the SMs' groups at once
-    assert ssm.scan_fwd_form(1, 5120, 16, 65536)[0] == "balanced"
+    # the long workload: 640 units, one full group per SM on whole rows and its 48-unit tail split
+    assert ssm.scan_fwd_form(1, 5120, 16, 65536)[0] == "split"
+    assert ssm.scan_fwd_form(1, 4736, 16, 65536)[0] == "plain"  # 592 units: one full group per SM, no tail
     assert ssm.scan_fwd_form(8, 1536, 16, 2048)[0] == "balanced"  # the mid workload: many channels
     assert ssm.scan_fwd_form(1, 64, 16, 4096)[0] == "balanced"  # too short
     assert ssm.scan_fwd_form(1, 64, 16, 8192, aligned_rows=False)[0] != "split"
@@ -217,3 +218,26 @@ def test_workspace_scan_in_a_graph(monkeypatch):
         g.replay()
         torch.cuda.synchronize()
         check_oracle(y, last, inp, what="workspace graph replay")
+
+
+# Tail splits: one full 4-unit group per SM runs whole rows and the last batch row's remaining
+# units are split (batch 1 with 4800 channels: a 48-unit tail; batch 2 with 2400: the tail starts
+# inside the last row).
+TAIL_SHAPES = [(1, 4800, 16, 8192), (2, 2400, 16, 8192)]
+
+
+@pytest.mark.parametrize("shape", TAIL_SHAPES, ids=lambda s: "b{}_d{}_n{}_l{}".format(*s))
+@pytest.mark.parametrize("mode", ["plain_args", "h0_zoh"])
+def test_tail_split_against_oracle(shape, mode, monkeypatch):
+    batch, dim, N, L = shape
+    inp = to_device(wl.random_scan_case(batch, dim, N, L, io="bf16", seed=dim + 7, h0=mode == "h0_zoh"), DEV)
+    disc = "zoh" if mode == "h0_zoh" else "delta_b"
+    h0 = inp["h0"] if mode == "h0_zoh" else None
+    set_split(monkeypatch, None)
+    assert form_of(inp, disc) == "split"
+    y, last = run(inp, monkeypatch, None, disc, h0)
+    check_oracle(y, last, inp, disc, h0, f"tail split {mode}")
+    yo, so = run(inp, monkeypatch, "off", disc, h0)
+    y, yo, last, so = (wl.to_f64(t) for t in (y, yo, last, so))
+    assert np.max(np.abs(y - yo) / (1.0 + np.abs(yo))) <= 2.0 ** -7
+    assert np.max(np.abs(last - so) / (1.0 + np.abs(so))) <= 2e-5
