@@ -741,11 +741,7 @@ __global__ void __launch_bounds__(kFusedGroups * ScanCfg<T, NPAD>::NT, 1)
   if (MODE != kWhole) {
     const int nck = (a.seqlen + kChunk - 1) / kChunk;
     seg = int(e >> kSegShift), b &= kMaxSplitBatch - 1;
-    if (MODE == kSegments && seg == kWholeSeg) {
-      seg = 0, kc1 = nck;  // a whole row beside the split tail: from h0, to the final state
-    } else {
-      kc0 = seg * (a.seg_len / kChunk), kc1 = min(nck, kc0 + a.seg_len / kChunk);
-    }
+    kc0 = seg * (a.seg_len / kChunk), kc1 = min(nck, kc0 + a.seg_len / kChunk);
   }
   scan_group<T, NPAD, VEC, ZOH, CK, MODE != kWhole, MODE == kCarries>(
       a, maps, smem + grp * Cfg::kSmem, threadIdx.x - grp * Cfg::NT, b, d0, min(a.dim, d0 + nch), seg, kc0, kc1,
@@ -897,14 +893,16 @@ bool launch_fused(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, c
 // The split for `a` on the current device, with both passes' plans; false when the scan runs
 // unsplit.
 template <typename T, int NPAD, bool ZOH>
-bool split_plans(const ScanArgs& a, SplitPlan& sp, FusedPlan& p1, int& c1, FusedPlan& p2, int& c2, cudaError_t& err) {
+bool split_plans(const ScanArgs& a, SplitPlan& sp, FusedPlan& pw, int& cw, FusedPlan& p1, int& c1, FusedPlan& p2,
+                 int& c2, cudaError_t& err) {
   if constexpr (NPAD != 16 || !std::is_same<T, __nv_bfloat16>::value) {
     return false;
   } else {
     int dev = 0, sms = 0;
     if (!balanced_allowed() || (err = device_sms(dev, sms)) != cudaSuccess) return false;
-    if (!make_split_plans(a, sms, sp, p1, c1, p2, c2)) return false;
-    return fused_ready<T, NPAD, true, ZOH, false, kCarries>(dev, err) &&
+    if (!make_split_plans(a, sms, sp, pw, cw, p1, c1, p2, c2)) return false;
+    return (cw == 0 || fused_ready<T, NPAD, true, ZOH, false, kWhole>(dev, err)) &&
+           fused_ready<T, NPAD, true, ZOH, false, kCarries>(dev, err) &&
            fused_ready<T, NPAD, true, ZOH, false, kSegments>(dev, err);
   }
 }
@@ -919,9 +917,9 @@ bool launch_split(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, c
     return false;
   } else {
     SplitPlan sp;
-    FusedPlan p1, p2;
-    int c1 = 0, c2 = 0;
-    if (!split_plans<T, NPAD, ZOH>(a, sp, p1, c1, p2, c2, err)) return err != cudaSuccess;
+    FusedPlan pw, p1, p2;
+    int cw = 0, c1 = 0, c2 = 0;
+    if (!split_plans<T, NPAD, ZOH>(a, sp, pw, cw, p1, c1, p2, c2, err)) return err != cudaSuccess;
     void* buf = nullptr;
     if (a.ws_given) {
       if (!a.ws || a.ws_bytes < sp.workspace_bytes) return false;  // no room: unsplit
@@ -934,7 +932,9 @@ bool launch_split(const ScanArgs& a, const TmaMaps& maps, cudaStream_t stream, c
     c.carry_h = static_cast<float*>(buf);
     c.carry_d = c.carry_h + size_t(sp.ncarry) * a.batch * a.dim * a.dstate;
     c.seg_len = sp.carry_len, c.seg_carries = 0;
-    err = launch_fused_plan<T, NPAD, true, ZOH, false, kCarries>(c, maps, p1, c1, stream);
+    // a tail split first scans the whole rows, one full group per SM, with the whole-row kernel
+    if (cw > 0) err = launch_fused_plan<T, NPAD, true, ZOH, false, kWhole>(a, maps, pw, cw, stream);
+    if (err == cudaSuccess) err = launch_fused_plan<T, NPAD, true, ZOH, false, kCarries>(c, maps, p1, c1, stream);
     if (err == cudaSuccess) {
       // the carried states: every channel, or those of the tail of the last batch row
       long long first = ((long long)(a.batch - 1) * a.dim + 8LL * sp.tail_p0) * a.dstate;
@@ -1032,10 +1032,10 @@ cudaError_t split_form(const ScanArgs& a, bool vec, SplitPlan& p, int& ctas) {
   p = SplitPlan{};
   ctas = 0;
   if (vec && a.io == kBF16 && a.dstate > 8 && !a.ckpt) {
-    FusedPlan p1, p2;
-    int c1 = 0;
-    const bool split = a.zoh ? split_plans<__nv_bfloat16, 16, true>(a, p, p1, c1, p2, ctas, err)
-                             : split_plans<__nv_bfloat16, 16, false>(a, p, p1, c1, p2, ctas, err);
+    FusedPlan pw, p1, p2;
+    int cw = 0, c1 = 0;
+    const bool split = a.zoh ? split_plans<__nv_bfloat16, 16, true>(a, p, pw, cw, p1, c1, p2, ctas, err)
+                             : split_plans<__nv_bfloat16, 16, false>(a, p, pw, cw, p1, c1, p2, ctas, err);
     if (!split) p = SplitPlan{}, ctas = 0;
   }
   return err;

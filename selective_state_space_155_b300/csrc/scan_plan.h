@@ -23,8 +23,6 @@ namespace ssm {
 constexpr int kFusedGroups = 3;
 constexpr int kMaxFusedCtas = 160;
 constexpr int kSegShift = 28, kMaxPlanSegs = 16, kMaxSplitBatch = 1 << 12;
-// segment field of a segment-pass entry that scans its whole row (a split of the tail only)
-constexpr int kWholeSeg = kMaxPlanSegs - 1;
 struct FusedPlan {
   uint32_t e[kFusedGroups * kMaxFusedCtas];
 };
@@ -98,8 +96,7 @@ inline bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   if (h0 && ls && h0 < ls + nst && ls < h0 + nst) return false;
   const long long units = (long long)a.batch * (a.dim / 8), cap = (long long)sms * kFusedGroups * 4;
   if (units == 0) return false;
-  // segment values below kWholeSeg (which marks whole rows in the segment pass)
-  const long long maxsegs = kWholeSeg;
+  const long long maxsegs = kMaxPlanSegs;  // the plan entry's 4-bit segment field
   long long segs = std::min<long long>(maxsegs, cap / units), per = 0;
   long long whole = 0, p0 = 0;  // the split of the tail only (below)
   const char* force = std::getenv("SSM_SCAN_SPLIT");
@@ -112,16 +109,16 @@ inline bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
     per = std::min<long long>(std::min<long long>(kMaxCarries, cap / (units * (segs - 1))), maxsegs / (segs - 1));
   } else {
     // Too many units to split them all, but whole rows would give every SM one full 4-unit group
-    // and some SMs a second, smaller group whose per-chunk costs slow the SM down: run the full
-    // groups on whole rows and split only the tail of the last batch row over the group slots
-    // left free, as many segments as fit.  (With two full groups per SM the balanced plan already
-    // keeps the SMs busy.)
+    // and some SMs a second, smaller group whose per-chunk costs slow the SM down by a third: run
+    // the full groups on whole rows (one group per SM) and then the tail of the last batch row as
+    // a split of its own.  (With two full groups per SM the balanced plan already keeps the SMs
+    // busy.)
     const long long ur = a.dim / 8;
     whole = units / (4LL * sms);
     const long long tail = units - 4LL * sms * whole;
     p0 = 4LL * sms * whole - (long long)(a.batch - 1) * ur;  // first tail unit within the last row
     if (whole != 1 || tail <= 0 || ur % 4 != 0 || p0 < 0) return false;
-    segs = std::min<long long>(maxsegs, (kFusedGroups - whole) * 4LL * sms / tail);
+    segs = std::min<long long>(maxsegs, cap / tail);
     if (segs < kMinSegs) return false;
     per = std::min<long long>(std::min<long long>(kMaxCarries, cap / (tail * (segs - 1))), maxsegs / (segs - 1));
   }
@@ -137,30 +134,31 @@ inline bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   return true;
 }
 
-// Both passes' plans of the split for `a` on `sms` SMs (no device calls): the carry pass's in p1
-// over c1 CTAs, the segment pass's in p2 over c2 CTAs.  False when the scan runs unsplit.
-inline bool make_split_plans(const ScanArgs& a, int sms, SplitPlan& sp, FusedPlan& p1, int& c1, FusedPlan& p2,
-                             int& c2) {
-  p1 = FusedPlan{}, p2 = FusedPlan{};
-  c1 = c2 = 0;
+// The plans of the split for `a` on `sms` SMs (no device calls): for a tail split the whole-row
+// launch's in pw over cw CTAs (cw = 0 otherwise), then the carry pass's in p1 over c1 CTAs and the
+// segment pass's in p2 over c2 CTAs.  False when the scan runs unsplit.
+inline bool make_split_plans(const ScanArgs& a, int sms, SplitPlan& sp, FusedPlan& pw, int& cw, FusedPlan& p1,
+                             int& c1, FusedPlan& p2, int& c2) {
+  pw = FusedPlan{}, p1 = FusedPlan{}, p2 = FusedPlan{};
+  cw = c1 = c2 = 0;
   if (!make_split(a, sms, sp)) return false;
   if (sp.whole_groups == 0) {
     c1 = make_fused_plan(a, (long long)sp.ncarry * a.batch, sms, p1, false);
     c2 = make_fused_plan(a, (long long)sp.segs * a.batch, sms, p2, false);
     return c1 > 0 && c2 > 0;
   }
-  // the tail split: the carry pass over the tail's carry segments; the segment pass with
-  // whole_groups whole-row groups of 4 units on every CTA, then the tail's segments
+  // the tail split: whole_groups whole-row groups of 4 units per CTA in their own launch, then the
+  // carry pass and the segment pass over the tail of the last batch row
   const long long ur = a.dim / 8;
   long long worst = 0;
-  c1 = fill_plan(a, sp.ncarry, sp.tail_p0, a.batch - 1, sms, 0, p1, worst);
   for (int c = 0; c < sms; ++c)
     for (int g = 0; g < sp.whole_groups; ++g) {
       const long long u = (long long)(c * sp.whole_groups + g) * 4;
-      p2.e[c * kFusedGroups + g] = uint32_t(u / ur) << 16 | uint32_t(kWholeSeg) << kSegShift |
-                                   uint32_t(u % ur) << 4 | 4u;
+      pw.e[c * kFusedGroups + g] = uint32_t(u / ur) << 16 | uint32_t(u % ur) << 4 | 4u;
     }
-  c2 = fill_plan(a, sp.segs, sp.tail_p0, a.batch - 1, sms, sp.whole_groups, p2, worst) > 0 ? sms : 0;
+  cw = sms;
+  c1 = fill_plan(a, sp.ncarry, sp.tail_p0, a.batch - 1, sms, 0, p1, worst);
+  c2 = fill_plan(a, sp.segs, sp.tail_p0, a.batch - 1, sms, 0, p2, worst);
   return c1 > 0 && c2 > 0;
 }
 

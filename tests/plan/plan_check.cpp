@@ -3,8 +3,9 @@
 // an SM count and checks, by walking the plan entries exactly as the kernel decodes them:
 //  * balanced form: every (batch row, channel) in exactly one group, at most 4 units per group and
 //    3 groups per CTA;
-//  * split form, segment pass: every (batch row, channel, chunk) scanned exactly once (whole-row
-//    groups of a tail split cover all chunks), segment indices below the whole-row marker;
+//  * split form: every (batch row, channel, chunk) scanned exactly once by the segment pass, or, for
+//    a tail split, by the whole-row launch (all chunks of the rows it holds) and the segment pass
+//    over the tail;
 //  * split form, carry pass: every carry segment of every split channel scanned exactly once, none
 //    reaching into the last segment;
 //  * the workspace size: 4 (dstate + 1) bytes per batch row, channel and carry segment.
@@ -58,36 +59,40 @@ static void check_split(int batch, int dim, int L, int sms, const char* expect) 
   ScanArgs a{};
   a.batch = batch, a.dim = dim, a.dstate = 16, a.seqlen = L, a.io = kBF16;
   SplitPlan sp{};
-  FusedPlan p1, p2;
-  int c1 = 0, c2 = 0;
-  const bool split = make_split_plans(a, sms, sp, p1, c1, p2, c2);
+  FusedPlan pw, p1, p2;
+  int cw = 0, c1 = 0, c2 = 0;
+  const bool split = make_split_plans(a, sms, sp, pw, cw, p1, c1, p2, c2);
   std::printf("split b%d d%d L%d on %d SMs: %s", batch, dim, L, sms, split ? "" : "unsplit\n");
   if (split)
-    std::printf("%d segments of %d, %d carry segments of %d, whole groups %d, tail from unit %d; CTAs %d + %d\n",
-                sp.segs, sp.seg_len, sp.ncarry, sp.carry_len, sp.whole_groups, sp.tail_p0, c1, c2);
+    std::printf("%d segments of %d, %d carry segments of %d, whole groups %d, tail from unit %d; CTAs %d + %d + %d\n",
+                sp.segs, sp.seg_len, sp.ncarry, sp.carry_len, sp.whole_groups, sp.tail_p0, cw, c1, c2);
   EXPECT(split == (expect[0] != 'u'), "expected %s", expect);
   if (!split) return;
   EXPECT(sp.seg_len % 64 == 0 && sp.carry_len % 64 == 0 && sp.seg_len == sp.carry_len * sp.carries_per_seg,
          "segment lengths");
-  EXPECT(sp.ncarry == (sp.segs - 1) * sp.carries_per_seg && sp.segs < kWholeSeg + 1 && sp.ncarry <= kWholeSeg,
+  EXPECT(sp.ncarry == (sp.segs - 1) * sp.carries_per_seg && sp.segs <= kMaxPlanSegs && sp.ncarry <= kMaxPlanSegs,
          "segment counts");
+  EXPECT((cw > 0) == (sp.whole_groups > 0), "whole-row launch only for a tail split");
   EXPECT((long long)(sp.segs - 1) * sp.seg_len < L && (long long)sp.segs * sp.seg_len >= L, "segments cover L");
   EXPECT(sp.workspace_bytes == size_t(sp.ncarry) * batch * dim * 17 * 4, "workspace bytes");
-  EXPECT(c1 <= sms && c2 <= sms, "at most one CTA per SM");
+  EXPECT(c1 <= sms && c2 <= sms && cw <= sms, "at most one CTA per SM");
   const int nck = (L + kScanChunk - 1) / kScanChunk;
   std::vector<int> cov(size_t(batch) * dim * nck, 0);
+  for (int c = 0; c < cw; ++c)  // the whole-row launch of a tail split: every chunk of its rows
+    for (int g = 0; g < kFusedGroups; ++g) {
+      const uint32_t e = pw.e[c * kFusedGroups + g];
+      if (!e) continue;
+      const Entry x = decode(e, false);
+      for (int d = x.d0; d < x.d0 + x.nch && d < dim; ++d)
+        for (int k = 0; k < nck; ++k) cov[(size_t(x.b) * dim + d) * nck + k]++;
+    }
   for (int c = 0; c < c2; ++c)
     for (int g = 0; g < kFusedGroups; ++g) {
       const uint32_t e = p2.e[c * kFusedGroups + g];
       if (!e) continue;
       const Entry x = decode(e, true);
-      int k0 = 0, k1 = nck;
-      if (x.seg != kWholeSeg) {
-        EXPECT(x.seg < sp.segs, "segment %d of %d", x.seg, sp.segs);
-        k0 = x.seg * (sp.seg_len / kScanChunk), k1 = std::min(nck, k0 + sp.seg_len / kScanChunk);
-      } else {
-        EXPECT(sp.whole_groups > 0, "whole-row marker in a full split");
-      }
+      EXPECT(x.seg < sp.segs, "segment %d of %d", x.seg, sp.segs);
+      const int k0 = x.seg * (sp.seg_len / kScanChunk), k1 = std::min(nck, k0 + sp.seg_len / kScanChunk);
       for (int d = x.d0; d < x.d0 + x.nch && d < dim; ++d)
         for (int k = k0; k < k1; ++k) cov[(size_t(x.b) * dim + d) * nck + k]++;
     }
