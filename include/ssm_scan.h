@@ -146,9 +146,9 @@ int ssm_scan_fwd_ex(const void* u, const void* delta, const float* A, const void
  *   SSM_FORM_SPLIT     the balanced form with the sequence split into segments scanned side by
  *                      side, for few channels and long sequences (four segments fit the SMs'
  *                      warp groups at once: at most 3 eight-channel units per SM; or one full
- *                      group per SM plus a tail in the last batch row, when only the tail is
- *                      split; seqlen >= 8192, 16-byte aligned rows, no checkpoints, last_state
- *                      not overlapping h0).  A carry pass scans each carry segment from a zero
+ *                      group per SM plus a tail in the last batch row, when the whole rows run
+ *                      first and only the tail is split; seqlen >= 8192, 16-byte aligned rows, no
+ *                      checkpoints, last_state not overlapping h0).  A carry pass scans each carry segment from a zero
  *                      state (the first from h0) for its end state and step-size sum; a combine
  *                      folds them with the associative pair operator (a1, b1) o (a2, b2) =
  *                      (a1 a2, a2 b1 + b2), a segment's decay a = exp(A * sum of its Delta) (53ai.com
