@@ -18,11 +18,11 @@ namespace ssm {
 // channels of one batch row) from a host plan that evens out the channels per SM.  With 32-channel
 // CTAs an SM carries 64 or 96 channels when the total is not a multiple of 96 per SM; the plan
 // gives every SM within 8 channels of the mean.  Plan entry: b << 16 | (d0 / 8) << 4 | (channels / 8),
-// 0 for an empty group; for the passes of a split sequence b takes 12 bits and the group's segment
-// (it then scans that segment's steps only) the top 4.
+// 0 for an empty group; for the passes of a split sequence b takes 11 bits and the group's segment
+// (it then scans that segment's steps only) the top 5.
 constexpr int kFusedGroups = 3;
 constexpr int kMaxFusedCtas = 160;
-constexpr int kSegShift = 28, kMaxPlanSegs = 16, kMaxSplitBatch = 1 << 12;
+constexpr int kSegShift = 27, kMaxPlanSegs = 32, kMaxSplitBatch = 1 << 11;
 struct FusedPlan {
   uint32_t e[kFusedGroups * kMaxFusedCtas];
 };
@@ -46,7 +46,7 @@ inline int fill_plan(const ScanArgs& a, long long rows, long long p0, int tail_b
       uint32_t entry = 0;
       if (load < target && row < rows) {
         const long long take = std::min(std::min(4LL, target - load), ur - pos);
-        // whole rows: row = b; split passes: segment < 16 in the top bits, batch < 4096
+        // whole rows: row = b; split passes: segment < 32 in the top bits, batch < 2048
         const long long b = tail_b >= 0 ? tail_b : row % a.batch, sg = tail_b >= 0 ? row : row / a.batch;
         entry = uint32_t(b) << 16 | uint32_t(sg) << kSegShift | uint32_t(pos) << 4 | uint32_t(take);
         load += take, pos += take, left -= take;
@@ -86,6 +86,7 @@ inline int make_fused_plan(const ScanArgs& a, long long rows, int sms, FusedPlan
 // kMaxCarries, at most 15 in all).  Both lengths are multiples of two chunks.
 constexpr int kSplitMinLen = 8192;  // the shortest sequence split (the extra launches must pay)
 constexpr int kMinSegs = 4, kMaxCarries = 4;
+constexpr int kMinSegLen = 1024;
 
 inline bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   p = SplitPlan{};
@@ -96,7 +97,9 @@ inline bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   if (h0 && ls && h0 < ls + nst && ls < h0 + nst) return false;
   const long long units = (long long)a.batch * (a.dim / 8), cap = (long long)sms * kFusedGroups * 4;
   if (units == 0) return false;
-  const long long maxsegs = kMaxPlanSegs;  // the plan entry's 4-bit segment field
+  // the plan entry's 5-bit segment field, and segments of at least kMinSegLen steps (shorter ones
+  // spend more of their time filling the copy and table pipelines)
+  const long long maxsegs = std::min<long long>(kMaxPlanSegs, std::max<long long>(kMinSegs, a.seqlen / kMinSegLen));
   long long segs = std::min<long long>(maxsegs, cap / units), per = 0;
   long long whole = 0, p0 = 0;  // the split of the tail only (below)
   const char* force = std::getenv("SSM_SCAN_SPLIT");
@@ -126,7 +129,7 @@ inline bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
   const long long clen = ((a.seqlen + segs * per - 1) / (segs * per) + step - 1) / step * step;
   const long long slen = clen * per;
   const long long nseg = (a.seqlen + slen - 1) / slen;
-  if (nseg < 2 || a.batch >= kMaxSplitBatch || (nseg - 1) * per > maxsegs || nseg > maxsegs) return false;
+  if (nseg < 2 || a.batch >= kMaxSplitBatch || (nseg - 1) * per > kMaxPlanSegs || nseg > kMaxPlanSegs) return false;
   p.segs = int(nseg), p.carries_per_seg = int(per), p.seg_len = int(slen), p.carry_len = int(clen);
   p.ncarry = int((nseg - 1) * per);
   p.whole_groups = int(whole), p.tail_p0 = int(p0);

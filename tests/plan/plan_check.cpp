@@ -142,7 +142,7 @@ int main() {
   check_split(8, 1536, 2048, 148, "unsplit");   // too short
   check_split(8, 1536, 8192, 148, "unsplit");   // many channels
   check_split(1, 64, 4096, 148, "unsplit");     // too short
-  check_split(5000, 8, 8192, 148, "unsplit");   // batch beyond the split's 12 bits
+  check_split(3000, 8, 8192, 148, "unsplit");   // batch beyond the split's 11 bits
   check_split(1, 1536, 65536, 132, "split");
   check_split(1, 5120, 65536, 132, "split (tail)");
   std::printf(fails ? "FAILED (%d)\n" : "all ok\n", fails);

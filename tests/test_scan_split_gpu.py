@@ -102,6 +102,8 @@ def test_split_equals_unsplit(disc, monkeypatch):
 def test_forced_segment_counts(split, monkeypatch):
     """Every (segments, carry segments per segment) the switch can force gives the oracle's result."""
     inp = to_device(wl.random_scan_case(1, 64, 16, 8192, io="bf16", seed=5, h0=True), DEV)
+    set_split(monkeypatch, split)
+    assert form_of(inp) == "split", split
     y, last = run(inp, monkeypatch, split, "delta_b", inp["h0"])
     check_oracle(y, last, inp, "delta_b", inp["h0"], f"split {split}")
 

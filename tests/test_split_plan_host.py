@@ -24,5 +24,5 @@ def test_plans_cover_every_channel_and_chunk_once(tmp_path):
     run = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert run.returncode == 0 and run.stdout.strip().endswith("all ok"), run.stdout + run.stderr
     # the long workload takes the tail split, the mid workload stays whole
-    assert "split b1 d5120 L65536 on 148 SMs: 16 segments" in run.stdout
+    assert "split b1 d5120 L65536 on 148 SMs: 32 segments" in run.stdout
     assert "split b8 d1536 L2048 on 148 SMs: unsplit" in run.stdout
