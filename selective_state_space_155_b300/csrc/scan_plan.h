@@ -82,8 +82,9 @@ inline int make_fused_plan(const ScanArgs& a, long long rows, int sms, FusedPlan
 // scans every segment from it.  The carry pass costs about 0.7 of the full scan per element over
 // (segments - 1) / segments of the sequence, so the split is taken only where at least
 // kMinSegs segments fit the SMs' groups at once (at most 3 units per SM); then as many segments
-// as fit (up to 15), and as many carry segments per segment as the groups hold (up to
-// kMaxCarries, at most 15 in all).  Both lengths are multiples of two chunks.
+// as fit (up to kMaxPlanSegs, each at least kMinSegLen steps), and as many carry segments per
+// segment as the groups hold (up to kMaxCarries, at most kMaxPlanSegs in all).  Both lengths are
+// multiples of two chunks.
 constexpr int kSplitMinLen = 8192;  // the shortest sequence split (the extra launches must pay)
 constexpr int kMinSegs = 4, kMaxCarries = 4;
 constexpr int kMinSegLen = 1024;
