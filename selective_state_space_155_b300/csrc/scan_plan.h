@@ -139,8 +139,9 @@ inline bool make_split(const ScanArgs& a, int sms, SplitPlan& p) {
 }
 
 // The plans of the split for `a` on `sms` SMs (no device calls): for a tail split the whole-row
-// launch's in pw over cw CTAs (cw = 0 otherwise), then the carry pass's in p1 over c1 CTAs and the
-// segment pass's in p2 over c2 CTAs.  False when the scan runs unsplit.
+// launch's in pw over cw CTAs (cw = 0 otherwise; its group c is the plain kernel's 32-channel block
+// c, which is what runs it), then the carry pass's in p1 over c1 CTAs and the segment pass's in p2
+// over c2 CTAs.  False when the scan runs unsplit.
 inline bool make_split_plans(const ScanArgs& a, int sms, SplitPlan& sp, FusedPlan& pw, int& cw, FusedPlan& p1,
                              int& c1, FusedPlan& p2, int& c2) {
   pw = FusedPlan{}, p1 = FusedPlan{}, p2 = FusedPlan{};
