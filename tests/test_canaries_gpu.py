@@ -62,6 +62,32 @@ def test_scan_outputs_stay_in_bounds(shape, variant, monkeypatch):
     yz.check("y (zoh)")
 
 
+# split forms: a full split with a ragged length (one chunk per copy), padded states and three rows
+# of 40 channels, and a tail split (whole rows first, then the last row's tail)
+SPLIT_SHAPES = [(2, 64, 12, 8232), (3, 40, 16, 8256), (1, 4800, 16, 8192)]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=lambda s: "b{}_d{}_n{}_l{}".format(*s))
+@pytest.mark.parametrize("disc", ["delta_b", "zoh"])
+def test_split_scan_writes_stay_in_bounds(shape, disc, monkeypatch):
+    """The split's outputs and its caller-owned carry buffers: nothing is written outside y,
+    last_state or the workspace the scan reports."""
+    monkeypatch.delenv("SSM_SCAN_VARIANT", raising=False)
+    monkeypatch.delenv("SSM_SCAN_SPLIT", raising=False)
+    batch, dim, N, L = shape
+    assert ssm.scan_fwd_form(batch, dim, N, L, discretization=disc)[0] == "split"
+    inp = to_device(wl.random_scan_case(batch, dim, N, L, io="bf16", seed=L + 3, h0=True), DEV)
+    nbytes = ssm.scan_fwd_workspace_size(batch, dim, N, L, discretization=disc)
+    ws = Guarded((nbytes // 4,), torch.float32)
+    y = Guarded((batch, dim, L), inp["u"].dtype)
+    last = Guarded((batch, dim, N), torch.float32)
+    ssm.ssm_scan_fwd(inp["u"], inp["delta"], inp["A"], inp["B"], inp["C"], inp["D"], inp["z"], inp["dt_bias"],
+                     h0=inp["h0"], y=y.view, last_state=last.view, discretization=disc, workspace=ws.view)
+    ws.check("workspace")
+    y.check("y (split)")
+    last.check("last_state (split)")
+
+
 @pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "b{}_d{}_n{}_l{}_{}".format(*s))
 @pytest.mark.parametrize("disc", ["delta_b", "zoh"])
 def test_training_pair_outputs_stay_in_bounds(shape, disc):
