@@ -713,9 +713,25 @@ __global__ void __launch_bounds__(256) scan_carry_combine_kernel(const ScanArgs 
   const int d = int(row % a.dim), n = int(i - row * a.dstate);
   const float al = a.A[size_t(d) * a.dstate + n] * kLog2e;
   float h = a.carry_h[i];
-  for (int j = 1; j < ncarry; ++j) {
-    h = __fmaf_rn(ex2_approx(al * a.carry_d[j * ((long long)a.batch * a.dim) + row]), h, a.carry_h[j * per + i]);
-    a.carry_h[j * per + i] = h;
+  const long long rows = (long long)a.batch * a.dim;
+  // the slots' loads, eight at a time, ahead of the dependent chain and its stores
+  constexpr int kBatch = 8;
+  for (int j0 = 1; j0 < ncarry; j0 += kBatch) {
+    float sd[kBatch], he[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int j = j0 + k;
+      sd[k] = j < ncarry ? a.carry_d[j * rows + row] : 0.0f;
+      he[k] = j < ncarry ? a.carry_h[j * per + i] : 0.0f;
+    }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) {
+      const int j = j0 + k;
+      if (j < ncarry) {
+        h = __fmaf_rn(ex2_approx(al * sd[k]), h, he[k]);
+        a.carry_h[j * per + i] = h;
+      }
+    }
   }
 }
 
